@@ -1,0 +1,136 @@
+"""Deliberately broken oracles must fail the pins ("deliberately broken kernels fail
+them", page "A 297-line kernel file that decodes faster than vLLM", section
+"Correctness").  Every mistake is planted in a CPU copy of an oracle function."""
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import moe_oracle as mo
+from synthetic import make_layer, random_topk_idx
+from tests import oracle_checks as oc
+
+_real_decode = mo.decode_mxfp4
+
+
+def _decode_swapped_nibbles(codes, scales, dtype=np.float32):
+    codes = np.asarray(codes, np.uint8)
+    swapped = ((codes >> 4) | (codes << 4)).astype(np.uint8)
+    return _real_decode(swapped, scales, dtype)
+
+
+def _decode_no_scale(codes, scales, dtype=np.float32):
+    return _real_decode(codes, np.full_like(np.asarray(scales), 127), dtype)
+
+
+def _decode_scale_off_by_one(codes, scales, dtype=np.float32):
+    return _real_decode(codes, np.asarray(scales) + 1, dtype) if np.max(scales) < 254 else \
+        _real_decode(codes, np.minimum(np.asarray(scales), 253), dtype) * 2
+
+
+def _topk_ties_to_high_index(logits, k, dtype=np.float32):
+    lg = np.asarray(logits)
+    T, E = lg.shape
+    idx = np.empty((T, k), np.int32)
+    for t in range(T):
+        order = np.lexsort((-np.arange(E), -lg[t].astype(np.float64)))
+        idx[t] = order[:k]
+    sel = np.take_along_axis(lg, idx, 1).astype(dtype)
+    ex = np.exp(sel - sel[:, :1])
+    return idx, (ex / ex.sum(1, keepdims=True)).astype(dtype)
+
+
+def _topk_softmax_over_all(logits, k, dtype=np.float32):
+    idx, _ = mo.topk_softmax(logits, k, dtype)
+    lg = np.asarray(logits, dtype)
+    ex = np.exp(lg - lg.max(1, keepdims=True))
+    p = ex / ex.sum(1, keepdims=True)
+    return idx, np.take_along_axis(p, idx, 1).astype(dtype)
+
+
+def _tile_table_unstable(idx, E, bm):
+    res = mo.tile_table(idx, E, bm)
+    perm = res["perm"].copy()
+    for e in range(E):  # reverse order within each expert
+        a, b = res["offsets"][e], res["offsets"][e + 1]
+        perm[a:b] = perm[a:b][::-1]
+    res["perm"] = perm
+    res["inv_perm"][perm] = np.arange(perm.size, dtype=np.int32)
+    return res
+
+
+def _hidden_gate_up_swapped(x_rows, c, s, I, dtype=np.float32):
+    w = mo.decode_mxfp4(c, s, dtype)
+    g = np.asarray(x_rows, dtype) @ w[:I].T
+    u = np.asarray(x_rows, dtype) @ w[I:2 * I].T
+    return (mo.silu(u) * g).astype(dtype)
+
+
+def _hidden_silu_sign(x_rows, c, s, I, dtype=np.float32):
+    w = mo.decode_mxfp4(c, s, dtype)
+    g = np.asarray(x_rows, dtype) @ w[:I].T
+    u = np.asarray(x_rows, dtype) @ w[I:2 * I].T
+    return (g / (1 + np.exp(g)) * u).astype(dtype)
+
+
+def _output_transposed(h_rows, c, s, dtype=np.float32):
+    w = mo.decode_mxfp4(c, s, dtype)
+    return (np.asarray(h_rows, dtype) @ w).astype(dtype)
+
+
+def test_broken_decoders_fail_enumeration():
+    for bad in (_decode_swapped_nibbles, _decode_no_scale, _decode_scale_off_by_one):
+        with pytest.raises(AssertionError):
+            oc.check_decode_enumeration(bad, np.float32)
+
+
+def test_broken_ffn_fails_brute_force():
+    for hid, outp in ((_hidden_gate_up_swapped, mo.expert_output),
+                      (_hidden_silu_sign, mo.expert_output),
+                      (mo.expert_hidden, _output_transposed)):
+        with pytest.raises(AssertionError):
+            oc.check_brute_force(hid, outp, mo.bf16_to_f32, np.float64, 1e-12)
+
+
+def test_broken_decoder_fails_brute_force(monkeypatch):
+    monkeypatch.setattr(mo, "decode_mxfp4", _decode_swapped_nibbles)
+    with pytest.raises(AssertionError):
+        oc.check_brute_force(mo.expert_hidden, mo.expert_output, mo.bf16_to_f32, np.float64, 1e-12)
+
+
+def test_broken_topk_fails():
+    for bad in (_topk_ties_to_high_index, _topk_softmax_over_all):
+        with pytest.raises(AssertionError):
+            oc.check_topk(bad)
+
+
+def test_unstable_tile_table_fails():
+    idx = random_topk_idx(64, 32, 4, seed=2)
+    with pytest.raises(AssertionError):
+        oc.check_tile_table(_tile_table_unstable, [(idx, 32, 16)])
+
+
+def test_skipped_slot_fails_identical_expert_invariant(monkeypatch):
+    real = mo.topk_softmax
+
+    def drop_last_slot(logits, k, dtype=np.float32):
+        idx, w = real(logits, k, dtype)
+        w = w.copy()
+        w[:, -1] = 0
+        return idx, w
+
+    monkeypatch.setattr(mo, "topk_softmax", drop_last_slot)
+    inp = make_layer(T=6, H=64, I=96, E=5, k=3, seed=7)
+    for arr in (inp.gu_codes, inp.gu_scales, inp.dn_codes, inp.dn_scales):
+        arr[:] = arr[0:1]
+    with pytest.raises(AssertionError):
+        oc.check_identical_experts(mo.moe_layer, mo.expert_hidden, mo.expert_output,
+                                   mo.bf16_to_f32, inp, np.float64)
+
+
+def test_truncating_bf16_fails_rounding_pin(monkeypatch):
+    def trunc(a):
+        return (np.ascontiguousarray(a, np.float32).view(np.uint32) & 0xFFFF0000).view(np.float32)
+
+    vals = np.array([1.0 + 3 * 2 ** -8], dtype=np.float32)
+    assert not np.array_equal(trunc(vals), oracle.bf16_round(vals))

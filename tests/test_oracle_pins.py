@@ -1,0 +1,138 @@
+"""Pins of the CPU oracle against things other than itself: the E2M1 format
+definition and its printed table, exact rational brute force, brute-force sorting,
+closed forms, invariants, and an independent library (torch CPU)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from synthetic import make_layer, make_config, random_topk_idx
+from tests import oracle_checks as oc
+
+
+def test_e2m1_table_matches_format_definition_and_golden():
+    gold = oc.golden_e2m1()
+    assert sorted(gold) == list(range(16))
+    for c in range(16):
+        want = oc.e2m1_from_bitfields(c)
+        assert float(gold[c]) == float(want)
+        assert oracle.E2M1_VALUES[c] == float(want)
+        if c == 8:
+            assert gold[c].startswith("-") and str(oracle.E2M1_VALUES[c]) == "-0.0"
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_decode_all_codes_all_scales(dtype):
+    oc.check_decode_enumeration(oracle.decode_mxfp4, dtype)
+
+
+def test_e8m0_nan_scale_rejected():
+    with pytest.raises(ValueError):
+        oracle.decode_mxfp4(np.zeros((1, 16), np.uint8), np.full((1, 1), 255, np.uint8))
+
+
+def test_nibble_order_reading():
+    # byte 0x21: even K index = low nibble = code 1 (0.5), odd K index = code 2 (1.0)
+    codes = np.zeros((1, 16), np.uint8)
+    codes[0, 0] = 0x21
+    v = oracle.decode_mxfp4(codes, np.full((1, 1), 127, np.uint8))
+    assert v[0, 0] == 0.5 and v[0, 1] == 1.0 and np.all(v[0, 2:] == 0)
+
+
+@pytest.mark.parametrize("dtype,rtol", [(np.float64, 1e-12), (np.float32, 2e-5)])
+def test_brute_force_one_block(dtype, rtol):
+    oc.check_brute_force(oracle.expert_hidden, oracle.expert_output, oracle.bf16_to_f32,
+                         dtype, rtol)
+
+
+def test_topk_against_full_sort_and_softmax_closed_form():
+    oc.check_topk(oracle.topk_softmax)
+    oc.check_topk(oracle.topk_softmax, T=17, E=128, k=4, seed=11)
+    oc.check_topk(oracle.topk_softmax, T=5, E=8, k=8, seed=2)
+
+
+def test_topk_single_expert_weight_is_one():
+    lg = np.random.default_rng(0).standard_normal((9, 8)).astype(np.float32)
+    idx, w = oracle.topk_softmax(lg, 1)
+    assert np.all(idx[:, 0] == lg.argmax(1)) and np.all(w == 1)
+
+
+def test_tile_table_brute_force_and_invariants():
+    cases = []
+    for (T, E, k, bm, skew, seed) in [(4, 8, 2, 16, 0, 0), (1, 32, 4, 16, 0, 1),
+                                       (64, 32, 4, 16, 0, 2), (64, 128, 4, 16, 0, 3),
+                                       (512, 128, 4, 64, 1.1, 4), (300, 16, 2, 128, 1.5, 5)]:
+        cases.append((random_topk_idx(T, E, k, seed=seed, skew=skew), E, bm))
+    # degenerate cases: one expert gets everything; an empty routing
+    cases.append((np.zeros((40, 1), np.int32), 4, 16))
+    cases.append((np.zeros((0, 2), np.int32), 4, 16))
+    oc.check_tile_table(oracle.tile_table, cases)
+
+
+def test_tile_bound_and_policy():
+    for T, E, k in [(1, 32, 4), (64, 32, 4), (64, 128, 4), (4096, 128, 4), (4, 8, 2)]:
+        bm = oracle.tile_rows_policy(T, k, E)
+        assert bm in (16, 64, 128)
+        for seed in range(3):
+            idx = random_topk_idx(T, E, k, seed=seed, skew=1.1 if T > 1000 else 0)
+            assert oracle.tile_table(idx, E, bm)["num_tiles"] <= oracle.max_tiles_bound(T, k, E, bm)
+    assert oracle.tile_rows_policy(64, 4, 32) == 16
+    assert oracle.tile_rows_policy(4096, 4, 128) == 128
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_identical_experts_make_output_independent_of_routing(dtype):
+    inp = make_layer(T=6, H=64, I=96, E=5, k=3, seed=7)
+    for arr in (inp.gu_codes, inp.gu_scales, inp.dn_codes, inp.dn_scales):
+        arr[:] = arr[0:1]
+    oc.check_identical_experts(oracle.moe_layer, oracle.expert_hidden, oracle.expert_output,
+                               oracle.bf16_to_f32, inp, dtype)
+
+
+def test_single_expert_layer_is_dense_ffn_by_loops():
+    inp = make_layer(T=2, H=32, I=64, E=1, k=1, seed=9)
+    ref = oc.dense_reference_loops(inp)
+    res = oracle.moe_layer(inp, dtype=np.float64)
+    assert np.allclose(res["out_unrounded"], ref, rtol=1e-12, atol=1e-12 * np.abs(ref).max())
+    assert np.all(res["w"] == 1.0)
+
+
+def test_weighted_combine_order_and_bf16_rounding():
+    inp = make_config("tiny")
+    res = oracle.moe_layer(inp, dtype=np.float64)
+    acc = sum(res["w"][:, j:j + 1] * res["y"][:, j] for j in range(inp.k))
+    assert np.allclose(res["out_unrounded"], acc, rtol=0, atol=1e-12 * np.abs(acc).max())
+    # bf16 rounding: at most half an ulp of bf16 (2^-8 relative) and exact bf16 values
+    r = oracle.bf16_round(acc.astype(np.float32))
+    assert np.all((r.view(np.uint32) & 0xFFFF) == 0)
+    assert np.all(np.abs(r - acc) <= np.abs(acc) * 2.0 ** -8 + 1e-30)
+
+
+def test_bf16_round_ties_to_even():
+    vals = np.array([1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -1.0 - 2 ** -8, 1.0 + 2 ** -8 + 2 ** -20],
+                    dtype=np.float32)
+    want = np.array([1.0, 1.0 + 2 ** -6, -1.0, 1.0 + 2 ** -7], dtype=np.float32)
+    assert np.array_equal(oracle.bf16_round(vals), want)
+
+
+def test_layer_matches_torch_cpu_library_path():
+    torch = pytest.importorskip("torch")
+    inp = make_config("tiny")
+    res = oracle.moe_layer(inp, dtype=np.float32, return_hidden=True)
+    x = torch.from_numpy(oracle.bf16_to_f32(inp.x))
+    wr = torch.from_numpy(oracle.bf16_to_f32(inp.w_router))
+    lg = x @ wr.T
+    top = torch.topk(lg, inp.k, dim=1)
+    w = torch.softmax(top.values, dim=1)
+    out = torch.zeros(inp.T, inp.H)
+    for t in range(inp.T):
+        for j in range(inp.k):
+            e = int(top.indices[t, j])
+            wgu = torch.from_numpy(oracle.decode_mxfp4(inp.gu_codes[e], inp.gu_scales[e]))
+            wd = torch.from_numpy(oracle.decode_mxfp4(inp.dn_codes[e], inp.dn_scales[e]))
+            g = wgu[:inp.I] @ x[t]
+            u = wgu[inp.I:] @ x[t]
+            out[t] += w[t, j] * (wd @ (torch.nn.functional.silu(g) * u))
+    assert np.array_equal(top.indices.numpy(), res["idx"])
+    ref = out.numpy()
+    assert np.abs(res["out_unrounded"] - ref).max() <= 1e-5 * np.abs(ref).max()

@@ -1,0 +1,363 @@
+"""Benchmark of the MXFP4 MoE layer on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one call of the whole layer (router + top-k + tile table + gather/encode
++ gate/up/SwiGLU + down/combine) over one batch of seeded synthetic gpt-oss-shaped
+input.  Inputs are resident in HBM when the timed region starts; weight copies are
+rotated so that every timed call streams its experts from HBM rather than L2.
+Prints one JSON line (rank 0).  For N > 1 (torchrun), every rank runs an independent
+replica of the layer (there is no exchange on this path), timings are max-reduced
+and `value` is the whole-job throughput.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MXFP4 MoE layer µs/call & tokens/s (batch 1/64/4096), % of HBM roofline"
+L2_BYTES = 129 * 1024 * 1024
+GATEUP_BYTES_PER_EXPERT = lambda H, I: 2 * I * H // 2 + 2 * I * H // 32   # codes + E8M0 scales
+DOWN_BYTES_PER_EXPERT = lambda H, I: H * I // 2 + H * I // 32
+DEFAULT_WORKLOAD = "gptoss20b_b1"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smmax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smmax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smmax) if smmax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- traffic from the committed ncu summary
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for fn in ("moe_gemm.cu", "moe_common.cuh", "sm100_ptx.cuh"):
+        with open(os.path.join(ROOT, "mxfp4_expert_layer_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from profiles/<kernel>_<workload>.md, or None
+    when absent or when the kernel source changed since the capture."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    txt = open(p).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    hm = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    if not m or not hm or hm.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------- CPU oracle baseline
+def cpu_baseline(inp, budget_s=12.0):
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload."""
+    import numpy as np
+    import oracle
+    T = inp.T
+    n_tok = T if T <= 8 else 8
+    tokens = np.arange(n_tok)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.moe_layer(inp, tokens=tokens)
+        done += n_tok
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{done} tokens of {inp.name} ({n_tok} per pass, full layer incl. MXFP4 decode of the "
+                      f"touched experts) in {dt:.1f} s; numpy, BLAS threads up to {os.cpu_count()}"}
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_init(n):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    return rank, world
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- reference arm (the oracle)
+def run_reference(args):
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if rank != 0:
+        return
+    from synthetic import make_config
+    inp = make_config(args.workload)
+    import numpy as np
+    import oracle
+    n_tok = min(inp.T, 8)
+    tokens = np.arange(n_tok)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle.moe_layer(inp, tokens=tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.moe_layer(inp, tokens=tokens)
+    dt = time.perf_counter() - t0
+    val = args.steps * n_tok / dt
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": inp.name, "T": inp.T, "H": inp.H, "I": inp.I, "E": inp.E, "k": inp.k,
+                       "sample_tokens_per_step": n_tok},
+            "cpu_baseline": {"value": val, "unit": "tokens/s", "kind": "oracle", "cores": os.cpu_count(),
+                             "sample": f"{n_tok} tokens of {inp.name} per step, full layer"},
+            "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------- our arm
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world = dist_init(args.gpus)
+    import numpy as np
+    import torch
+
+    import mxfp4_expert_layer_gb300 as pkg
+    from mxfp4_expert_layer_gb300 import _lib as L
+    from synthetic import make_config
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.build()
+    L.load()
+
+    inp = make_config(args.workload, seed=rank)
+    T, H, I, E, k = inp.T, inp.H, inp.I, inp.E, inp.k
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x = to(inp.x.view(np.int16)).view(torch.bfloat16)
+    wr = to(inp.w_router.view(np.int16)).view(torch.bfloat16)
+    bias = None if inp.router_bias is None else to(inp.router_bias)
+    layer = pkg.MoELayer.from_mxfp4(wr, to(inp.gu_codes), to(inp.gu_scales), to(inp.dn_codes), to(inp.dn_scales),
+                                    k=k, router_bias=bias)
+    # routing of the workload (same for every call): touched experts give the algorithmic bytes
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    wts = torch.empty(T, k, dtype=torch.float32, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    layer(x, out=out, topk_idx=idx, topk_w=wts)
+    torch.cuda.synchronize()
+    touched = int(torch.unique(idx).numel())
+    gu_bytes = touched * GATEUP_BYTES_PER_EXPERT(H, I)
+    dn_bytes = touched * DOWN_BYTES_PER_EXPERT(H, I)
+    alg_bytes = gu_bytes + dn_bytes
+
+    # rotate weight copies so the touched experts of every call come from HBM
+    copies = max(1, min(16, math.ceil(4 * L2_BYTES / max(alg_bytes, 1))))
+    wsets = [(layer.w_gateup, layer.w_down)] + [(layer.w_gateup.clone(), layer.w_down.clone())
+                                               for _ in range(copies - 1)]
+    ws = layer.workspace(T)
+    stream = torch.cuda.current_stream()
+
+    def call(i, events=None):
+        wgu, wd = wsets[i % copies]
+        b = None if bias is None else bias.data_ptr()
+        if events is None:
+            st = L.moe_forward(x.data_ptr(), wr.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
+                               ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, stream.cuda_stream)
+        else:
+            st = L.moe_forward_timed(x.data_ptr(), wr.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
+                                     ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, events,
+                                     stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"moe_forward failed: {L.moe_error_string(st).decode()}")
+
+    launches = L.moe_forward_launches(T, H, I, E, k)
+    clocks = ClockSampler(local)
+    # pre-warm: bring clocks up (~0.5 s of calls), then the W warm-up steps
+    t_end = time.perf_counter() + 0.5
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(20):
+            call(i)
+            i += 1
+        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        call(i)
+        i += 1
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for s in range(args.steps):
+        call(i + s)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms, world)
+    i += args.steps
+
+    # per-kernel split with events between the launches (same calls, separate loop)
+    nk = launches
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
+    for row in evs:          # torch creates the CUDA event on its first record
+        for e in row:
+            e.record(stream)
+    handles = [(ctypes_array(e)) for e in evs]
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        call(i + s, handles[s])
+    torch.cuda.synchronize()
+    per_kernel = [0.0] * nk
+    for s in range(args.steps):
+        for j in range(nk):
+            per_kernel[j] += evs[s][j].elapsed_time(evs[s][j + 1])
+    per_kernel = [v / args.steps for v in per_kernel]
+    names = ["route_topk_table", "gather_encode_x", "gateup_swiglu", "down_combine"]
+    alg = {"gateup_swiglu": gu_bytes, "down_combine": dn_bytes}
+    dom = max(alg, key=lambda n: per_kernel[names.index(n)])
+    dom_ms = per_kernel[names.index(dom)]
+    peak, peak_kind = measured_peaks()
+    achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
+    clk = clocks.stop()
+
+    # end to end: pinned host input -> device, layer, device -> pinned host output, every step
+    hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(x.cpu())
+    hout = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for s in range(args.steps):
+        x.copy_(hx, non_blocking=True)
+        call(i + s)
+        hout.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+
+    status = layer.device_status(T)
+    if rank != 0:
+        return
+    us = ms * 1e3
+    line = {
+        "metric": METRIC, "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e4m3(2-term) -> f32 accum; bf16 out",
+        "data": "synthetic",
+        "config": {"workload": inp.name, "T": T, "H": H, "I": I, "E": E, "k": k,
+                   "tile_rows": L.moe_tile_rows(T, k, E), "touched_experts": touched,
+                   "l2": f"{copies} rotating weight copies ({copies * alg_bytes / 1e6:.0f} MB touched per "
+                         f"rotation > 4x L2)", "parallelism": f"replicas x{world}"},
+        "us_per_call": us,
+        "layer_hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+        "layer_roofline_frac": alg_bytes / (ms * 1e-3) / 1e9 / peak,
+        "per_kernel_us": {n: v * 1e3 for n, v in zip(names, per_kernel)},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": alg[dom],
+                     "traffic": committed_traffic(dom, inp.name)},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+                "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+        "device_status": status,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    print(json.dumps(line))
+
+
+def ctypes_array(events):
+    import ctypes
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return arr
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * moe_mxfp4.h -- C ABI of the MXFP4 mixture-of-experts layer for GB300 (sm_103a).
+ *
+ * The layer (the MoE block of a gpt-oss-style decoder) is:
+ *   router GEMV/GEMM -> top-k with softmax over the selected logits -> per-expert
+ *   tile table -> permute -> grouped gate/up GEMM with SwiGLU -> down GEMM with the
+ *   weighted top-k combine and unpermute.
+ * Sources: "A 297-line kernel file that decodes faster than vLLM" (cloudy.so),
+ * section "Where the time went" (rows "Router + top-k", "MoE gate/up + SwiGLU",
+ * "MoE down + combine") and section "Optimizations" (rows "MXFP4 MoE on tensor
+ * cores", "Per-expert routing tile table", "Fixed decode tiles", "MoE token tile
+ * follows tokens per expert"); "triton-kernels" README (bassrehab), section
+ * "Quick Start", "Fused MoE Dispatch" (router -> permute -> fused expert FFN ->
+ * unpermute, returning output, expert indices and expert weights).
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated otherwise.  The
+ *    library never allocates or frees device memory on these paths.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and never synchronise the host, except moe_get_device_status.
+ *  - The return value is a status: MOE_OK (0) or a negative MOE_ERR_* code.  On an
+ *    error nothing has been launched unless the code is MOE_ERR_CUDA.
+ *  - Shapes: 1 <= T, H % 32 == 0, I % 32 == 0, 1 <= k <= E <= 256, k <= 32.
+ *  - bf16 arrays are raw bf16 bit patterns (uint16_t).
+ *  - Expert weights: MXFP4 = FP4 E2M1 codes in blocks of 32 along K sharing one
+ *    E8M0 scale, value = E2M1[code] * 2^(scale - 127) (OCP MX v1.0).  Raw layout:
+ *    codes [E][rows][K/2] bytes with the even K index in the low nibble, scales
+ *    [E][rows][K/32] bytes.  Gate/up rows: gate rows 0..I-1 then up rows I..2I-1
+ *    (K = H).  Down rows: H rows (K = I).
+ *  - Alignment: every device pointer 16-byte aligned; workspace and prepared
+ *    weights 256-byte aligned.
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
+
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)       /* null pointer, bad alignment, bad flag      */
+#define MOE_ERR_UNSUPPORTED_SHAPE (-2) /* shape outside the supported set above      */
+#define MOE_ERR_WORKSPACE_TOO_SMALL (-3)
+#define MOE_ERR_CUDA (-4)              /* a launch or driver call failed             */
+#define MOE_ERR_DEVICE_TIMEOUT (-5)    /* a bounded device-side wait gave up          */
+#define MOE_ERR_NAN_SCALE (-6)         /* an E8M0 scale byte of 255 (NaN) in weights */
+
+#define MOE_WEIGHTS_GATEUP 0
+#define MOE_WEIGHTS_DOWN 1
+
+#define MOE_ROUTE_FROM_LOGITS 1 /* moe_route: `logits` is an input, skip the GEMV */
+
+/* Static description of a status code; never NULL. */
+const char* moe_error_string(int status);
+
+/* ------------------------------------------------------------------ weights
+ * One-time re-layout of raw MXFP4 expert weights into the layout the tensor-core
+ * kernels stream: rows are padded along K to a multiple of 128 codes (pad codes 0)
+ * and the E8M0 scales are regrouped into 512-byte atoms of 128 rows x 4 MX blocks,
+ * the order in which the block-scaled MMA reads them.  No value is re-quantised;
+ * the bytes are only moved ("MXFP4 MoE on tensor cores": weights permuted once at
+ * load).
+ *   kind  MOE_WEIGHTS_GATEUP: rows = 2*I (gate then up), K = H.
+ *         MOE_WEIGHTS_DOWN:   rows = H, K = I.
+ *   codes [E][rows][K/2], scales [E][rows][K/32]: device, read only.
+ *   dst: device, moe_prepared_weight_bytes(...) bytes, 256-byte aligned, written.
+ * Scale bytes of 255 are rejected: the call returns MOE_ERR_NAN_SCALE after the
+ * stream has finished (it synchronises `stream`, as a load-time call may).
+ */
+size_t moe_prepared_weight_bytes(int E, int rows, int K, int kind);
+int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E, int rows, int K, int kind,
+                        void* dst, size_t dst_bytes, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ sizes
+ * Token rows per tile chosen for a shape (16, 64 or 128 from the mean tokens per
+ * expert T*k/E; fixed per shape, never autotuned) and the bound on tile count.  */
+int moe_tile_rows(int T, int k, int E);
+int moe_max_tiles(int T, int k, int E, int tile_rows);
+
+/* Bytes of device workspace needed by moe_forward and the stage calls below for
+ * this shape; 0 for an unsupported shape.  The workspace holds routing results,
+ * quantised activations, the slot buffer of the combine, arrival counters and a
+ * status word.  Zero-fill it once after allocation (cudaMemset); every call leaves
+ * its counters at zero again, so it can serve consecutive calls on one stream.
+ * Calls that overlap on the GPU must not share a workspace.                       */
+size_t moe_workspace_bytes(int T, int H, int I, int E, int k);
+
+/* ------------------------------------------------------------------ stage calls
+ * moe_route: logits[t, e] = sum_h x[t, h] * w_router[e, h] (+ router_bias[e]) in
+ * fp32; then per token the k largest logits (ties: lower expert index first),
+ * listed in that order, and weights = softmax over those k logits.
+ *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL.
+ *   logits f32 [T, E]: written, or read when flags has MOE_ROUTE_FROM_LOGITS (then
+ *   x, w_router and router_bias may be NULL).
+ *   topk_idx i32 [T, k], topk_w f32 [T, k]: written.
+ *   workspace: zero-filled once, at least moe_workspace_bytes(T, 32, 32, E, k)
+ *   bytes; only its status word and routing arrival counters are used.
+ * Source: "Where the time went", row "Router + top-k"; "Quick Start",
+ * fused_moe_forward(..., gating="softmax").                                        */
+int moe_route(const uint16_t* x, const uint16_t* w_router, const float* router_bias, int T, int H, int E, int k,
+              float* logits, int flags, int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+              moe_stream_t stream);
+
+/* moe_build_tile_table: the per-expert tile table of a routing ("Per-expert
+ * routing tile table": each expert writes its own tiles).  Atomic-free counting
+ * sort, deterministic:
+ *   counts[e] (i32 [E]); offsets (i32 [E+1], exclusive prefix sum, offsets[E] = T*k);
+ *   perm[s] (i32 [T*k]) = assignment t*k+j at sorted row s, rows sorted by expert
+ *   then ascending t*k+j; inv_perm (i32 [T*k]) its inverse;
+ *   tiles (i32 [max_tiles][4]) = {expert, first sorted row, rows (1..tile_rows),
+ *   tile*tile_rows}, experts ascending, ceil(counts[e]/tile_rows) tiles each;
+ *   num_tiles (i32 [1]).
+ *   tile_rows: 16, 64 or 128, or 0 for moe_tile_rows(T, k, E).
+ *   topk_idx i32 [T, k] with entries in [0, E): read.                              */
+int moe_build_tile_table(const int32_t* topk_idx, int T, int k, int E, int tile_rows, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* tiles, int32_t* num_tiles,
+                         moe_stream_t stream);
+
+/* moe_mxfp4_gateup_swiglu: for every tile (expert e, rows of perm) and every
+ * hidden feature i: g = x_t . W_gate[e][i], u = x_t . W_up[e][i], h = silu(g) * u.
+ * x rows are gathered by perm (the permute step) and encoded as two E4M3 terms
+ * with E8M0 block scales; the weights stay MXFP4 and their scales feed the
+ * block-scaled MMA directly.  h is left in the workspace (two-term E4M3 in tile
+ * row order) for moe_mxfp4_down_combine.
+ *   x bf16 [T, H]; perm, tiles, num_tiles as written by moe_build_tile_table with
+ *   the same tile_rows (0 = policy); w_gateup: moe_prepare_weights(MOE_WEIGHTS_GATEUP).
+ * Source: "Where the time went", row "MoE gate/up + SwiGLU".                       */
+int moe_mxfp4_gateup_swiglu(const uint16_t* x, const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles,
+                            int tile_rows, const void* w_gateup, int T, int H, int I, int E, int k, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream);
+
+/* moe_mxfp4_down_combine: y_tj = h_tj . W_down[e_tj]^T for every assignment, then
+ * out[t] = sum_{j=0..k-1} topk_w[t, j] * y_tj summed in fp32 in ascending j and
+ * rounded once to bf16 -- deterministic run to run.  Reads h from the workspace
+ * (written by moe_mxfp4_gateup_swiglu for the same routing).
+ *   topk_w f32 [T, k]; w_down: moe_prepare_weights(MOE_WEIGHTS_DOWN); out bf16 [T, H].
+ * Source: "Where the time went", row "MoE down + combine".                         */
+int moe_mxfp4_down_combine(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows,
+                           const float* topk_w, const void* w_down, int T, int H, int I, int E, int k,
+                           void* workspace, size_t workspace_bytes, uint16_t* out, moe_stream_t stream);
+
+/* moe_hidden_dequant: expand the workspace's two-term encoded h into f32
+ * [T*k, I] rows in assignment order (t*k + j); a test and inspection aid.          */
+int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows, int T,
+                       int H, int I, int E, int k, const void* workspace, size_t workspace_bytes, float* h_out,
+                       moe_stream_t stream);
+
+/* ------------------------------------------------------------------ whole layer
+ * moe_forward: the whole layer, out = MoE(x), on one stream with no host sync.
+ *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL;
+ *   w_gateup / w_down: prepared weights; out bf16 [T, H];
+ *   topk_idx_out i32 [T, k] and topk_w_out f32 [T, k]: optional copies (NULL to skip).
+ *   workspace: moe_workspace_bytes(T, H, I, E, k) bytes.                           */
+int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
+                const void* w_down, int T, int H, int I, int E, int k, void* workspace, size_t workspace_bytes,
+                uint16_t* out, int32_t* topk_idx_out, float* topk_w_out, moe_stream_t stream);
+
+/* moe_forward_timed: moe_forward that also records caller-created CUDA events
+ * (cudaEvent_t, passed as void*) on `stream`: events[i] just before launch i and
+ * events[n] after the last one, n = moe_forward_launches(...); the launches are
+ * route + tile table, gather + encode of x, gate/up + SwiGLU, down + combine.  It
+ * gives the per-kernel time split ("Where the time went": per-section times of a
+ * decode step).  events must hold n + 1 valid events.                             */
+int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
+                      const void* w_down, int T, int H, int I, int E, int k, void* workspace,
+                      size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                      void* const* events, moe_stream_t stream);
+
+/* Number of kernels moe_forward launches for a shape (for launch accounting). */
+int moe_forward_launches(int T, int H, int I, int E, int k);
+
+/* Synchronises `stream`, reads the workspace's device status word into *status
+ * (bit 0: main-loop wait timed out, bit 1: epilogue wait timed out, bit 2:
+ * producer wait timed out; 0 = healthy) and clears it.  Returns MOE_OK, or
+ * MOE_ERR_DEVICE_TIMEOUT when any bit was set.  Not for the hot path.              */
+int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_MXFP4_H */

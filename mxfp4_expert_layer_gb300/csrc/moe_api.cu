@@ -1,0 +1,456 @@
+// C ABI of the MXFP4 MoE layer: argument checks, workspace carving, TMA tensor
+// maps and the launch sequence of the hot path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "moe_common.cuh"
+#include "moe_kernels.cuh"
+
+using namespace moe;
+
+namespace {
+
+// ------------------------------------------------------------------ checks
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int kMaxDim = 8192;
+
+int check_shape(int T, int H, int I, int E, int k) {
+  if (T < 1 || H < 32 || I < 32 || E < 1 || k < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 32 || I % 32 || H > kMaxDim || I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)T * k > (1LL << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int resolve_bm(int T, int k, int E, int tile_rows) {
+  if (tile_rows == 0) return tile_rows_policy(T, k, E);
+  if (tile_rows == 16 || tile_rows == 64 || tile_rows == 128) return tile_rows;
+  return -1;
+}
+
+// ------------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  int dtype, rank;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4];
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+
+struct MapCache {
+  static constexpr int kSlots = 64;
+  MapKey keys[kSlots];
+  CUtensorMap maps[kSlots];
+  bool used[kSlots] = {};
+  int next = 0;
+  std::mutex mu;
+};
+
+MapCache& map_cache() {
+  static MapCache c;
+  return c;
+}
+
+// Encodes (or fetches from a small cache) a tiled tensor map; false on failure.
+bool make_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box) {
+  MapKey key;
+  std::memset(&key, 0, sizeof key);
+  key.ptr = ptr;
+  key.dtype = (int)dtype;
+  key.rank = rank;
+  for (int i = 0; i < rank; ++i) {
+    key.dims[i] = dims[i];
+    key.box[i] = box[i];
+    if (i < rank - 1) key.strides[i] = strides[i];
+  }
+  MapCache& c = map_cache();
+  std::lock_guard<std::mutex> lock(c.mu);
+  for (int i = 0; i < MapCache::kSlots; ++i) {
+    if (c.used[i] && c.keys[i] == key) {
+      *out = c.maps[i];
+      return true;
+    }
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = enc(out, dtype, rank, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  const int slot = c.next;
+  c.next = (c.next + 1) % MapCache::kSlots;
+  c.keys[slot] = key;
+  c.maps[slot] = *out;
+  c.used[slot] = true;
+  return true;
+}
+
+// MXFP4 codes of one prepared family as a 4-D map {Kp, rows per group, groups, E}.
+bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P) {
+  cuuint64_t dims[4] = {(cuuint64_t)P.Kp, (cuuint64_t)P.rows_per_group, (cuuint64_t)P.groups, (cuuint64_t)P.E};
+  const cuuint64_t row = (cuuint64_t)P.Kp / 2;
+  cuuint64_t strides[3] = {row, row * P.rows_per_group, row * P.rows_per_group * P.groups};
+  cuuint32_t box[4] = {(cuuint32_t)kKGroup, (cuuint32_t)kMTile, 1, 1};
+  return make_map(out, prepared, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, dims, strides, box);
+}
+
+// E4M3 activation rows {K, pad_rows}, boxes of 128 x bm.
+bool act_map(CUtensorMap* out, const void* base, int K, int rows, int bm) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {(cuuint32_t)kKGroup, (cuuint32_t)bm};
+  return make_map(out, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims, strides, box);
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// ------------------------------------------------------------------ stage bodies
+int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm,
+               const void* w_gateup, int T, int H, int I, int E, int k, void* ws, const WsLayout& L,
+               cudaStream_t stream, void* const* events = nullptr) {
+  // events (optional): [0] before the gather/encode launch, [1] before the GEMM
+  if (events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[0]), stream);
+  QuantXParams q{};
+  q.x = x;
+  q.perm = perm;
+  q.tiles = tiles;
+  q.num_tiles = num_tiles;
+  q.T = T; q.H = H; q.k = k; q.bm = bm; q.max_tiles = L.max_tiles; q.kg = L.kg_h;
+  q.q_hi = ws_ptr<uint8_t>(ws, L.x_hi);
+  q.q_lo = ws_ptr<uint8_t>(ws, L.x_lo);
+  q.sf_hi = ws_ptr<uint8_t>(ws, L.x_sf_hi);
+  q.sf_lo = ws_ptr<uint8_t>(ws, L.x_sf_lo);
+  q.zero_buf = ws_ptr<int32_t>(ws, L.combine_cnt);
+  q.zero_count = T * L.mt_h;
+  cudaError_t e = launch_quant_x(q, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  const PreparedLayout P = make_prepared_layout(E, 2 * I, H, 2);
+  GemmParams g{};
+  if (!weight_map(&g.tm_w, w_gateup, P)) return MOE_ERR_CUDA;
+  if (!act_map(&g.tm_act_hi, q.q_hi, H, L.pad_rows, bm)) return MOE_ERR_CUDA;
+  if (!act_map(&g.tm_act_lo, q.q_lo, H, L.pad_rows, bm)) return MOE_ERR_CUDA;
+  g.w_sf = static_cast<const uint8_t*>(w_gateup) + P.scales_off;
+  g.act_sf_hi = q.sf_hi;
+  g.act_sf_lo = q.sf_lo;
+  g.tiles = tiles;
+  g.num_tiles = num_tiles;
+  g.perm = perm;
+  g.T = T; g.H = H; g.I = I; g.E = E; g.k = k; g.bm = bm; g.max_tiles = L.max_tiles;
+  g.K = H;
+  g.kg = P.kg;
+  g.mt = L.mt_i;
+  g.rows_out = I;
+  g.w_groups = 2;
+  g.group_tiles = bm >= 64 ? 8 : 1;
+  g.h_hi = ws_ptr<uint8_t>(ws, L.h_hi);
+  g.h_lo = ws_ptr<uint8_t>(ws, L.h_lo);
+  g.h_sf_hi = ws_ptr<uint8_t>(ws, L.h_sf_hi);
+  g.h_sf_lo = ws_ptr<uint8_t>(ws, L.h_sf_lo);
+  g.kg_out = L.kg_i;
+  g.status = ws_ptr<uint32_t>(ws, L.status);
+  if (events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[1]), stream);
+  return cuda_status(launch_gateup(g, stream));
+}
+
+int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm, const float* topk_w,
+             const void* w_down, int T, int H, int I, int E, int k, void* ws, const WsLayout& L, uint16_t* out,
+             cudaStream_t stream) {
+  const PreparedLayout P = make_prepared_layout(E, H, I, 1);
+  GemmParams g{};
+  if (!weight_map(&g.tm_w, w_down, P)) return MOE_ERR_CUDA;
+  if (!act_map(&g.tm_act_hi, ws_ptr<uint8_t>(ws, L.h_hi), I, L.pad_rows, bm)) return MOE_ERR_CUDA;
+  if (!act_map(&g.tm_act_lo, ws_ptr<uint8_t>(ws, L.h_lo), I, L.pad_rows, bm)) return MOE_ERR_CUDA;
+  g.w_sf = static_cast<const uint8_t*>(w_down) + P.scales_off;
+  g.act_sf_hi = ws_ptr<uint8_t>(ws, L.h_sf_hi);
+  g.act_sf_lo = ws_ptr<uint8_t>(ws, L.h_sf_lo);
+  g.tiles = tiles;
+  g.num_tiles = num_tiles;
+  g.perm = perm;
+  g.T = T; g.H = H; g.I = I; g.E = E; g.k = k; g.bm = bm; g.max_tiles = L.max_tiles;
+  g.K = I;
+  g.kg = P.kg;
+  g.mt = L.mt_h;
+  g.rows_out = H;
+  g.w_groups = 1;
+  g.group_tiles = bm >= 64 ? 8 : 1;
+  g.topk_w = topk_w;
+  g.slots = ws_ptr<float>(ws, L.slots);
+  g.combine_cnt = ws_ptr<int32_t>(ws, L.combine_cnt);
+  g.out = out;
+  g.status = ws_ptr<uint32_t>(ws, L.status);
+  return cuda_status(launch_down(g, stream));
+}
+
+RouteParams route_params(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E, int k,
+                         float* logits, int from_logits, int32_t* idx, float* w, void* ws, const WsLayout& L) {
+  RouteParams r{};
+  r.x = x;
+  r.w_router = w_router;
+  r.bias = bias;
+  r.T = T; r.H = H; r.E = E; r.k = k;
+  r.from_logits = from_logits;
+  r.experts_per_block = T <= 64 ? 8 : 32;
+  r.logits = logits;
+  r.topk_idx = idx;
+  r.topk_w = w;
+  r.sync = ws_ptr<uint32_t>(ws, L.route_sync);
+  r.status = ws_ptr<uint32_t>(ws, L.status);
+  return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_error_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, misalignment or bad flag)";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA launch or driver call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+    case MOE_ERR_NAN_SCALE: return "E8M0 scale 255 (NaN) in the weights";
+    default: return "unknown status";
+  }
+}
+
+size_t moe_prepared_weight_bytes(int E, int rows, int K, int kind) {
+  if (E < 1 || rows < 1 || K < 32 || K % 32 || (kind != MOE_WEIGHTS_GATEUP && kind != MOE_WEIGHTS_DOWN)) return 0;
+  const int groups = kind == MOE_WEIGHTS_GATEUP ? 2 : 1;
+  if (rows % (groups * 32)) return 0;
+  return make_prepared_layout(E, rows, K, groups).total;
+}
+
+int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E, int rows, int K, int kind, void* dst,
+                        size_t dst_bytes, moe_stream_t stream) {
+  const size_t need = moe_prepared_weight_bytes(E, rows, K, kind);
+  if (need == 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!codes || !scales || !dst || !aligned(codes, 16) || !aligned(dst, 256)) return MOE_ERR_INVALID_ARG;
+  if (dst_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int groups = kind == MOE_WEIGHTS_GATEUP ? 2 : 1;
+  const PreparedLayout P = make_prepared_layout(E, rows, K, groups);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* flag = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(dst) + P.flag_off);
+  if (cudaMemsetAsync(flag, 0, 256, s) != cudaSuccess) return MOE_ERR_CUDA;
+  PrepareParams pp{};
+  pp.codes = codes;
+  pp.scales = scales;
+  pp.E = E; pp.R = rows; pp.K = K; pp.Kp = P.Kp; pp.groups = groups; pp.rows_per_group = P.rows_per_group;
+  pp.mt = P.mt; pp.kg = P.kg;
+  pp.dst_codes = static_cast<uint8_t*>(dst);
+  pp.dst_scales = static_cast<uint8_t*>(dst) + P.scales_off;
+  pp.flag = flag;
+  if (launch_prepare(pp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t h = 0;
+  if (cudaMemcpyAsync(&h, flag, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return h ? MOE_ERR_NAN_SCALE : MOE_OK;
+}
+
+int moe_tile_rows(int T, int k, int E) {
+  if (T < 1 || k < 1 || E < 1) return 0;
+  return tile_rows_policy(T, k, E);
+}
+
+int moe_max_tiles(int T, int k, int E, int tile_rows) {
+  if (T < 1 || k < 1 || E < 1 || tile_rows < 1) return 0;
+  return max_tiles_bound(T, k, E, tile_rows);
+}
+
+size_t moe_workspace_bytes(int T, int H, int I, int E, int k) {
+  if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
+  return make_ws_layout(T, H, I, E, k, tile_rows_policy(T, k, E)).total;
+}
+
+int moe_route(const uint16_t* x, const uint16_t* w_router, const float* router_bias, int T, int H, int E, int k,
+              float* logits, int flags, int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
+              moe_stream_t stream) {
+  if (flags & ~MOE_ROUTE_FROM_LOGITS) return MOE_ERR_INVALID_ARG;
+  const int from_logits = (flags & MOE_ROUTE_FROM_LOGITS) ? 1 : 0;
+  const int Hs = from_logits ? 32 : H;
+  int st = check_shape(T, Hs, 32, E, k);
+  if (st != MOE_OK) return st;
+  if (!logits || !topk_idx || !topk_w || !workspace || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  if (!from_logits && (!x || !w_router || !aligned(x, 16) || !aligned(w_router, 16))) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_ws_layout(T, 32, 32, E, k, tile_rows_policy(T, k, E));
+  if (workspace_bytes < L.route_sync + sizeof(uint32_t) * (size_t)(ceil_div(T, 8) + 1))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  RouteParams r = route_params(x, w_router, router_bias, T, Hs, E, k, logits, from_logits, topk_idx, topk_w,
+                               workspace, L);
+  r.build_table = 0;
+  return cuda_status(launch_route(r, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_build_tile_table(const int32_t* topk_idx, int T, int k, int E, int tile_rows, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, int32_t* inv_perm, int32_t* tiles, int32_t* num_tiles,
+                         moe_stream_t stream) {
+  if (T < 1 || k < 1 || E < 1 || E > kMaxExperts || k > E || (long long)T * k > (1LL << 24))
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int bm = resolve_bm(T, k, E, tile_rows);
+  if (bm < 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!topk_idx || !counts || !offsets || !perm || !inv_perm || !tiles || !num_tiles || !aligned(tiles, 16))
+    return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_tile_table(topk_idx, T * k, E, bm, counts, offsets, perm, inv_perm,
+                                       reinterpret_cast<TileEntry*>(tiles), num_tiles,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int moe_mxfp4_gateup_swiglu(const uint16_t* x, const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles,
+                            int tile_rows, const void* w_gateup, int T, int H, int I, int E, int k, void* workspace,
+                            size_t workspace_bytes, moe_stream_t stream) {
+  int st = check_shape(T, H, I, E, k);
+  if (st != MOE_OK) return st;
+  const int bm = resolve_bm(T, k, E, tile_rows);
+  if (bm != tile_rows_policy(T, k, E)) return MOE_ERR_UNSUPPORTED_SHAPE;  // workspace is sized for the policy tile
+  if (!x || !perm || !tiles || !num_tiles || !w_gateup || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(tiles, 16) || !aligned(w_gateup, 256) || !aligned(workspace, 256))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return run_gateup(x, perm, reinterpret_cast<const TileEntry*>(tiles), num_tiles, bm, w_gateup, T, H, I, E, k,
+                    workspace, L, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_mxfp4_down_combine(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows,
+                           const float* topk_w, const void* w_down, int T, int H, int I, int E, int k,
+                           void* workspace, size_t workspace_bytes, uint16_t* out, moe_stream_t stream) {
+  int st = check_shape(T, H, I, E, k);
+  if (st != MOE_OK) return st;
+  const int bm = resolve_bm(T, k, E, tile_rows);
+  if (bm != tile_rows_policy(T, k, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!perm || !tiles || !num_tiles || !topk_w || !w_down || !workspace || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(tiles, 16) || !aligned(w_down, 256) || !aligned(workspace, 256) || !aligned(out, 16))
+    return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return run_down(perm, reinterpret_cast<const TileEntry*>(tiles), num_tiles, bm, topk_w, w_down, T, H, I, E, k,
+                  workspace, L, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows, int T,
+                       int H, int I, int E, int k, const void* workspace, size_t workspace_bytes, float* h_out,
+                       moe_stream_t stream) {
+  int st = check_shape(T, H, I, E, k);
+  if (st != MOE_OK) return st;
+  const int bm = resolve_bm(T, k, E, tile_rows);
+  if (bm != tile_rows_policy(T, k, E)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!perm || !tiles || !num_tiles || !workspace || !h_out) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = const_cast<void*>(workspace);
+  HiddenDequantParams hp{};
+  hp.perm = perm;
+  hp.tiles = reinterpret_cast<const TileEntry*>(tiles);
+  hp.num_tiles = num_tiles;
+  hp.I = I; hp.bm = bm; hp.max_tiles = L.max_tiles; hp.kg = L.kg_i;
+  hp.h_hi = ws_ptr<uint8_t>(ws, L.h_hi);
+  hp.h_lo = ws_ptr<uint8_t>(ws, L.h_lo);
+  hp.sf_hi = ws_ptr<uint8_t>(ws, L.h_sf_hi);
+  hp.sf_lo = ws_ptr<uint8_t>(ws, L.h_sf_lo);
+  hp.out = h_out;
+  return cuda_status(launch_hidden_dequant(hp, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float* router_bias,
+                        const void* w_gateup, const void* w_down, int T, int H, int I, int E, int k,
+                        void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out,
+                        float* topk_w_out, void* const* events, moe_stream_t stream) {
+  int st = check_shape(T, H, I, E, k);
+  if (st != MOE_OK) return st;
+  if (!x || !w_router || !w_gateup || !w_down || !workspace || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(out, 16) || !aligned(w_gateup, 256) ||
+      !aligned(w_down, 256) || !aligned(workspace, 256))
+    return MOE_ERR_INVALID_ARG;
+  const int bm = tile_rows_policy(T, k, E);
+  const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  int32_t* idx = topk_idx_out ? topk_idx_out : ws_ptr<int32_t>(ws, L.idx);
+  float* w = topk_w_out ? topk_w_out : ws_ptr<float>(ws, L.w);
+  int32_t* perm = ws_ptr<int32_t>(ws, L.perm);
+  TileEntry* tiles = ws_ptr<TileEntry>(ws, L.tiles);
+  int32_t* num_tiles = ws_ptr<int32_t>(ws, L.num_tiles);
+
+  RouteParams r = route_params(x, w_router, router_bias, T, H, E, k, ws_ptr<float>(ws, L.logits), 0, idx, w, ws, L);
+  r.build_table = 1;
+  r.bm = bm;
+  r.counts = ws_ptr<int32_t>(ws, L.counts);
+  r.offsets = ws_ptr<int32_t>(ws, L.offsets);
+  r.perm = perm;
+  r.inv_perm = ws_ptr<int32_t>(ws, L.inv_perm);
+  r.tiles = tiles;
+  r.num_tiles = num_tiles;
+  bool ev_ok = true;
+  auto mark = [&](int i) {
+    if (events && cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) != cudaSuccess) ev_ok = false;
+  };
+  mark(0);
+  if (!ev_ok) return MOE_ERR_INVALID_ARG;
+  if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
+  st = run_gateup(x, perm, tiles, num_tiles, bm, w_gateup, T, H, I, E, k, ws, L, s, events ? events + 1 : nullptr);
+  if (st != MOE_OK) return st;
+  mark(3);
+  st = run_down(perm, tiles, num_tiles, bm, w, w_down, T, H, I, E, k, ws, L, out, s);
+  mark(4);
+  return st;
+}
+
+int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
+                const void* w_down, int T, int H, int I, int E, int k, void* workspace, size_t workspace_bytes,
+                uint16_t* out, int32_t* topk_idx_out, float* topk_w_out, moe_stream_t stream) {
+  return forward_impl(x, w_router, router_bias, w_gateup, w_down, T, H, I, E, k, workspace, workspace_bytes, out,
+                      topk_idx_out, topk_w_out, nullptr, stream);
+}
+
+int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
+                      const void* w_down, int T, int H, int I, int E, int k, void* workspace,
+                      size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                      void* const* events, moe_stream_t stream) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x, w_router, router_bias, w_gateup, w_down, T, H, I, E, k, workspace, workspace_bytes, out,
+                      topk_idx_out, topk_w_out, events, stream);
+}
+
+int moe_forward_launches(int T, int H, int I, int E, int k) {
+  if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
+  return 4;  // route+table, gather+encode, gate/up, down+combine
+}
+
+int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream) {
+  if (!workspace || !status || workspace_bytes < 256) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t h = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&h, workspace, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h && cudaMemset(workspace, 0, 256) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = (int)h;
+  return h ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+}  // extern "C"

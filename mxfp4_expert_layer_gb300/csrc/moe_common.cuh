@@ -1,0 +1,197 @@
+// Shared definitions of the MXFP4 MoE layer kernels: shapes, workspace layout,
+// the two-term E4M3 activation encoding and device status reporting.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "moe_mxfp4.h"
+
+namespace moe {
+
+// ----------------------------------------------------------------- constants
+constexpr int kMxBlock = 32;         // K values sharing one E8M0 scale
+constexpr int kKGroup = 128;         // K values per pipeline stage (4 MX blocks)
+constexpr int kMTile = 128;          // weight rows per MMA tile (MMA M)
+constexpr int kSfAtomBytes = 512;    // scale-factor atom: 128 rows x 4 MX blocks
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+
+// Device status word bits (read back with moe_get_device_status).
+constexpr uint32_t kStatusTimeoutMain = 1u << 0;
+constexpr uint32_t kStatusTimeoutEpi = 1u << 1;
+constexpr uint32_t kStatusTimeoutProducer = 1u << 2;
+constexpr uint32_t kStatusBadIndex = 1u << 3;
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// K rounded up to whole pipeline stages (the prepared weight rows carry this many
+// 4-bit codes; codes past the real K are zero).
+__host__ __device__ inline int padded_k(int K) { return ceil_div(K, kKGroup) * kKGroup; }
+
+// Token rows per tile from the mean tokens per expert ("token tile follows tokens
+// per expert"): 16 for decode-sized loads, 64 for medium, 128 for prefill.
+__host__ __device__ inline int tile_rows_policy(int T, int k, int E) {
+  long long tk = (long long)T * k;
+  if (tk <= 16LL * E) return 16;
+  if (tk <= 64LL * E) return 64;
+  return 128;
+}
+
+__host__ __device__ inline int max_tiles_bound(int T, int k, int E, int bm) {
+  long long tk = (long long)T * k;
+  long long b = tk / bm + (E < tk ? E : tk);
+  return (int)b;
+}
+
+// ----------------------------------------------------------------- tiles
+struct TileEntry {
+  int32_t expert;     // expert of every row in the tile
+  int32_t row_begin;  // first sorted row (index into perm)
+  int32_t n_rows;     // valid rows, 1..bm
+  int32_t pad_row;    // first row of the tile in the padded activation buffers (= tile * bm)
+};
+
+// ----------------------------------------------------------------- workspace
+// Byte offsets of every region inside the caller-allocated workspace.
+struct WsLayout {
+  int T, H, I, E, k, bm, max_tiles, pad_rows;
+  int kg_h, kg_i;        // K groups (of 128) over H and over I
+  int mt_h, mt_i;        // M tiles (of 128) over H and over I
+  size_t status;         // uint32 device status word (+ padding)
+  size_t route_sync;     // uint32 [ceil(T/8) + 1] arrival counters of the routing kernel
+  size_t logits;         // f32 [T, E]
+  size_t idx;            // i32 [T, k]
+  size_t w;              // f32 [T, k]
+  size_t counts;         // i32 [E]
+  size_t offsets;        // i32 [E + 1]
+  size_t perm;           // i32 [T*k]
+  size_t inv_perm;       // i32 [T*k]
+  size_t tiles;          // TileEntry [max_tiles]
+  size_t num_tiles;      // i32
+  size_t x_hi, x_lo;     // e4m3 [pad_rows, H]
+  size_t x_sf_hi, x_sf_lo;  // scale atoms [max_tiles][kg_h][512 * sf_atoms_per_tile]
+  size_t h_hi, h_lo;     // e4m3 [pad_rows, I]
+  size_t h_sf_hi, h_sf_lo;  // scale atoms [max_tiles][kg_i][512 * sf_atoms_per_tile]
+  size_t slots;          // f32 [T*k, H]: weighted expert outputs awaiting the combine
+  size_t combine_cnt;    // i32 [T, mt_h]: arrivals per (token, output tile)
+  size_t total;
+};
+
+__host__ __device__ inline int sf_atoms_per_tile(int bm) { return bm > 128 ? 2 : 1; }
+
+inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
+  WsLayout L{};
+  L.T = T; L.H = H; L.I = I; L.E = E; L.k = k; L.bm = bm;
+  L.max_tiles = max_tiles_bound(T, k, E, bm);
+  L.pad_rows = L.max_tiles * bm;
+  L.kg_h = ceil_div(H, kKGroup);
+  L.kg_i = ceil_div(I, kKGroup);
+  L.mt_h = ceil_div(H, kMTile);
+  L.mt_i = ceil_div(I, kMTile);
+  const size_t A = 256;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, A); return r; };
+  const size_t tk = (size_t)T * k;
+  const size_t sfa = (size_t)sf_atoms_per_tile(bm) * kSfAtomBytes;
+  L.status = take(256);
+  L.route_sync = take(sizeof(uint32_t) * (size_t)(ceil_div(T, 8) + 1));
+  L.logits = take(sizeof(float) * (size_t)T * E);
+  L.idx = take(sizeof(int32_t) * tk);
+  L.w = take(sizeof(float) * tk);
+  L.counts = take(sizeof(int32_t) * (size_t)E);
+  L.offsets = take(sizeof(int32_t) * (size_t)(E + 1));
+  L.perm = take(sizeof(int32_t) * tk);
+  L.inv_perm = take(sizeof(int32_t) * tk);
+  L.tiles = take(sizeof(TileEntry) * (size_t)L.max_tiles);
+  L.num_tiles = take(sizeof(int32_t));
+  L.x_hi = take((size_t)L.pad_rows * H);
+  L.x_lo = take((size_t)L.pad_rows * H);
+  L.x_sf_hi = take((size_t)L.max_tiles * L.kg_h * sfa);
+  L.x_sf_lo = take((size_t)L.max_tiles * L.kg_h * sfa);
+  L.h_hi = take((size_t)L.pad_rows * I);
+  L.h_lo = take((size_t)L.pad_rows * I);
+  L.h_sf_hi = take((size_t)L.max_tiles * L.kg_i * sfa);
+  L.h_sf_lo = take((size_t)L.max_tiles * L.kg_i * sfa);
+  L.slots = take(sizeof(float) * tk * H);
+  L.combine_cnt = take(sizeof(int32_t) * (size_t)T * L.mt_h);
+  L.total = o;
+  return L;
+}
+
+template <typename P>
+__host__ __device__ inline P* ws_ptr(void* ws, size_t off) {
+  return reinterpret_cast<P*>(reinterpret_cast<uint8_t*>(ws) + off);
+}
+
+// ----------------------------------------------------------------- MXFP4 weights
+// Prepared weight layout of one matrix family (gate/up or down) for E experts:
+//   codes  [E][R][Kp/2]   R = rows of the family (2I gate+up rows, or H down rows),
+//                         Kp = K padded to a multiple of 128 (pad codes are zero)
+//   scales [E][G][MT][KG][512]  G = 2 for gate/up (gate rows, up rows), 1 for down;
+//                         MT = ceil(rows per group / 128), KG = Kp / 128; each 512-byte
+//                         atom holds the E8M0 scales of 128 rows x 4 MX blocks:
+//                         byte (l*16 + c*4 + b) = scale of row 32c + l, block b.
+//   trailer (256 bytes): a status word the preparing kernel sets when it meets
+//                         an E8M0 scale of 255 (NaN).
+struct PreparedLayout {
+  int E, R, K, Kp, groups, rows_per_group, mt, kg;
+  size_t codes_bytes;   // E * R * Kp / 2
+  size_t scales_off;    // aligned start of the scale atoms
+  size_t flag_off;      // status trailer
+  size_t total;
+};
+
+inline PreparedLayout make_prepared_layout(int E, int R, int K, int groups) {
+  PreparedLayout P{};
+  P.E = E; P.R = R; P.K = K; P.Kp = padded_k(K); P.groups = groups;
+  P.rows_per_group = R / groups;
+  P.mt = ceil_div(P.rows_per_group, kMTile);
+  P.kg = P.Kp / kKGroup;
+  P.codes_bytes = (size_t)E * R * (P.Kp / 2);
+  P.scales_off = align_up(P.codes_bytes, 256);
+  P.flag_off = align_up(P.scales_off + (size_t)E * groups * P.mt * P.kg * kSfAtomBytes, 256);
+  P.total = P.flag_off + 256;
+  return P;
+}
+
+// ----------------------------------------------------------------- activations
+// Two-term MX encoding of 32 real values v sharing a block: v ~= q1 * 2^p1 + q2 * 2^p2
+// with q1, q2 E4M3 and p1, p2 E8M0 exponents.  p is the smallest exponent that keeps
+// the block maximum within the E4M3 range (448); an all-zero block gets p = 0.
+// Exponents are kept in [-126, 127] so 2^p and 2^-p are normal floats and the
+// E8M0 byte p + 127 is never 255 (NaN).
+__device__ __forceinline__ float pow2_int(int e) { return __int_as_float((e + 127) << 23); }
+
+__device__ __forceinline__ int mx_e4m3_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int e = ilogbf(amax) - 8;                  // amax / 2^e in [256, 512)
+  if (e < -126) e = -126;
+  if (e > 127) e = 127;
+  if (amax > 448.f * pow2_int(e) && e < 127) e += 1;  // keep within E4M3's finite range
+  return e;
+}
+
+__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
+  __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(q), __NV_E4M3);
+  return __half2float(__half(hr));
+}
+
+// Scale atom byte offset of (row r within a tile, MX block b within a K group).
+__host__ __device__ inline int sf_atom_offset(int r, int b) {
+  return (r >> 7) * kSfAtomBytes + (r & 31) * 16 + ((r >> 5) & 3) * 4 + b;
+}
+
+__device__ __forceinline__ void report_status(uint32_t* status, uint32_t bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace moe

@@ -1,0 +1,314 @@
+// Router GEMV/GEMM, warp-shuffle top-k with softmax over the selected logits, and
+// the atomic-free per-expert tile table.
+//
+// Sources: "A 297-line kernel file that decodes faster than vLLM", section "Where
+// the time went" (row "Router + top-k") and section "Optimizations" (row
+// "Per-expert routing tile table": every expert writes its own tiles instead of a
+// kernel searching a tiles x experts grid); "triton-kernels" README, section
+// "Quick Start" (softmax gating + top-k, expert indices and weights returned).
+//
+// One launch does all three steps: blocks of (8 tokens x a slice of experts)
+// compute logits; the last block to finish a token group (an integer arrival
+// count, no spinning) selects the top-k of those tokens; the last token group to
+// finish builds the tile table.  Every result is computed by one fixed thread or
+// warp in a fixed order, so the outputs are bit-reproducible run to run.
+#include "moe_common.cuh"
+#include "moe_kernels.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kTokensPerGroup = 8;
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// (value, index) order used by top-k: larger value first, then smaller index.
+__device__ __forceinline__ bool topk_better(float v1, int i1, float v2, int i2) {
+  return v1 > v2 || (v1 == v2 && i1 < i2);
+}
+
+// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
+__device__ int block_exclusive_scan_256(int v, int* scratch /* >= 8 ints */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    int o = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += o;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  int warp_off = 0, sum = 0;
+#pragma unroll
+  for (int w = 0; w < kRouteWarps; ++w) {
+    int s = scratch[w];
+    if (w < warp) warp_off += s;
+    sum += s;
+  }
+  __syncthreads();
+  if (total) *total = sum;
+  return warp_off + incl - v;
+}
+
+}  // namespace
+
+// Deterministic counting sort of the assignments by expert, stable in t*k+j,
+// executed by one block of 256 threads.  Each warp owns a contiguous chunk of
+// assignments and a private histogram row; lanes with equal experts are grouped
+// with __match_any_sync, so no atomics are used anywhere.
+__device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, int E, int bm, int32_t* counts,
+                                       int32_t* offsets, int32_t* perm, int32_t* inv_perm, TileEntry* tiles,
+                                       int32_t* num_tiles, uint32_t* status) {
+  __shared__ int hist[kRouteWarps][kMaxExperts];
+  __shared__ int scan_scratch[kRouteWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kRouteWarps * kMaxExperts; i += kRouteThreads) (&hist[0][0])[i] = 0;
+  __syncthreads();
+  const int chunk = ceil_div(Tk, kRouteWarps);
+  const int a_begin = warp * chunk;
+  const int a_end = min(Tk, a_begin + chunk);
+  const unsigned lt_mask = (1u << lane) - 1u;
+  // phase 1: per-warp histograms
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    int e = -1;
+    if (a < a_end) {
+      e = __ldcg(idx + a);
+      if (e < 0 || e >= E) {
+        report_status(status, kStatusBadIndex);
+        e = -1;
+      }
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && (grp & lt_mask) == 0) hist[warp][e] += __popc(grp);
+  }
+  __syncthreads();
+  // phase 2: counts, offsets (exclusive scan over experts), per-warp bases
+  int cnt = 0;
+  if (tid < E) {
+    for (int w = 0; w < kRouteWarps; ++w) cnt += hist[w][tid];
+  }
+  int total = 0;
+  const int off = block_exclusive_scan_256(tid < E ? cnt : 0, scan_scratch, &total);
+  if (tid < E) {
+    counts[tid] = cnt;
+    offsets[tid] = off;
+    int run = off;
+    for (int w = 0; w < kRouteWarps; ++w) {
+      const int h = hist[w][tid];
+      hist[w][tid] = run;  // becomes the next free sorted row of (warp, expert)
+      run += h;
+    }
+  }
+  if (tid == 0) offsets[E] = total;
+  __syncthreads();
+  // phase 3: scatter assignments to their sorted rows (stable in a)
+  for (int base = a_begin; base < a_end; base += 32) {
+    const int a = base + lane;
+    int e = -1;
+    if (a < a_end) {
+      e = __ldcg(idx + a);
+      if (e < 0 || e >= E) e = -1;
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    int pos = 0;
+    if (e >= 0) pos = hist[warp][e] + __popc(grp & lt_mask);
+    __syncwarp();
+    if (e >= 0) {
+      perm[pos] = a;
+      inv_perm[a] = pos;
+      if ((grp & lt_mask) == 0) hist[warp][e] += __popc(grp);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // phase 4: tiles, experts ascending
+  const int nt = tid < E ? ceil_div(cnt, bm) : 0;
+  int ntotal = 0;
+  const int t0 = block_exclusive_scan_256(nt, scan_scratch, &ntotal);
+  if (tid < E) {
+    for (int q = 0; q < nt; ++q) {
+      TileEntry te;
+      te.expert = tid;
+      te.row_begin = off + q * bm;
+      te.n_rows = min(bm, cnt - q * bm);
+      te.pad_row = (t0 + q) * bm;
+      tiles[t0 + q] = te;
+    }
+  }
+  if (tid == 0) *num_tiles = ntotal;
+}
+
+// Top-k of one token by one warp: each lane holds logits e = lane + 32*i; k rounds
+// of a warp arg-max on (value desc, index asc).  Softmax over the k selected.
+__device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out) {
+  const int lane = threadIdx.x & 31;
+  float v[kMaxExperts / 32];
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (e < E) ? __ldcg(lg_row + e) : -INFINITY;
+  }
+  unsigned taken = 0;  // bit i: element e = lane + 32*i already selected
+  float sel_v[kMaxTopK];
+  int sel_i[kMaxTopK];
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && topk_better(v[i], e, bv, bi)) {
+        bv = v[i];
+        bi = e;
+      }
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+      if (topk_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    sel_v[j] = bv;
+    sel_i[j] = bi;
+  }
+  if (lane == 0) {
+    const float m = sel_v[0];
+    float ex[kMaxTopK];
+    float s = 0.f;
+    for (int j = 0; j < k; ++j) {
+      ex[j] = expf(sel_v[j] - m);
+      s += ex[j];
+    }
+    for (int j = 0; j < k; ++j) {
+      idx_out[j] = sel_i[j];
+      w_out[j] = ex[j] / s;
+    }
+  }
+}
+
+// grid = (token groups of 8, expert slices); block = 256 threads.
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
+  extern __shared__ __align__(16) uint8_t route_smem[];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = blockIdx.x;
+  const int t0 = g * kTokensPerGroup;
+  const int nt = min(kTokensPerGroup, p.T - t0);
+  if (!p.from_logits) {
+    // stage the group's activations in shared memory (16-byte vectors)
+    uint4* xs = reinterpret_cast<uint4*>(route_smem);
+    const int vec_per_row = p.H / 8;
+    for (int i = tid; i < nt * vec_per_row; i += kRouteThreads) {
+      const int r = i / vec_per_row, c = i % vec_per_row;
+      xs[i] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + r) * p.H) + c);
+    }
+    __syncthreads();
+    const int e_begin = blockIdx.y * p.experts_per_block;
+    const int e_end = min(p.E, e_begin + p.experts_per_block);
+    for (int e = e_begin + warp; e < e_end; e += kRouteWarps) {
+      float acc[kTokensPerGroup];
+#pragma unroll
+      for (int r = 0; r < kTokensPerGroup; ++r) acc[r] = 0.f;
+      const uint4* wr = reinterpret_cast<const uint4*>(p.w_router + (size_t)e * p.H);
+      for (int c = lane; c < vec_per_row; c += 32) {
+        const uint4 wv = __ldg(wr + c);
+        const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
+        const float w4 = bf16_lo(wv.z), w5 = bf16_hi(wv.z), w6 = bf16_lo(wv.w), w7 = bf16_hi(wv.w);
+#pragma unroll
+        for (int r = 0; r < kTokensPerGroup; ++r) {
+          if (r < nt) {
+            const uint4 xv = xs[r * vec_per_row + c];
+            float a = acc[r];
+            a = fmaf(bf16_lo(xv.x), w0, a);
+            a = fmaf(bf16_hi(xv.x), w1, a);
+            a = fmaf(bf16_lo(xv.y), w2, a);
+            a = fmaf(bf16_hi(xv.y), w3, a);
+            a = fmaf(bf16_lo(xv.z), w4, a);
+            a = fmaf(bf16_hi(xv.z), w5, a);
+            a = fmaf(bf16_lo(xv.w), w6, a);
+            a = fmaf(bf16_hi(xv.w), w7, a);
+            acc[r] = a;
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kTokensPerGroup; ++r) {
+        float a = acc[r];
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) a += __shfl_xor_sync(0xffffffffu, a, d);
+        if (lane == 0 && r < nt) {
+          if (p.bias) a += __ldg(p.bias + e);
+          p.logits[(size_t)(t0 + r) * p.E + e] = a;
+        }
+      }
+    }
+    // arrival of this expert slice for the token group
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      const unsigned old = atomicAdd(p.sync + g, 1u);
+      s_last = (old == gridDim.y - 1) ? 1 : 0;
+      if (s_last) p.sync[g] = 0;  // ready for the next call
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+  }
+  // top-k of the group's tokens: one warp per token
+  if (warp < nt) {
+    const int t = t0 + warp;
+    topk_softmax_warp(p.logits + (size_t)t * p.E, p.E, p.k, p.topk_idx + (size_t)t * p.k,
+                      p.topk_w + (size_t)t * p.k);
+  }
+  if (!p.build_table) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned old = atomicAdd(p.sync + gridDim.x, 1u);
+    s_last = (old == gridDim.x - 1) ? 1 : 0;
+    if (s_last) p.sync[gridDim.x] = 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
+                         p.num_tiles, p.status);
+}
+
+__global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t* idx, int Tk, int E, int bm,
+                                                                   int32_t* counts, int32_t* offsets, int32_t* perm,
+                                                                   int32_t* inv_perm, TileEntry* tiles,
+                                                                   int32_t* num_tiles) {
+  build_tile_table_block(idx, Tk, E, bm, counts, offsets, perm, inv_perm, tiles, num_tiles, nullptr);
+}
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
+  const int groups = ceil_div(p.T, kTokensPerGroup);
+  dim3 grid(groups, p.from_logits ? 1 : ceil_div(p.E, p.experts_per_block));
+  const size_t smem = p.from_logits ? 0 : (size_t)kTokensPerGroup * p.H * sizeof(uint16_t);
+  // static (tile-table scratch) + dynamic (activation tile) shared memory may exceed
+  // the 48 KB default window
+  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  route_kernel<<<grid, kRouteThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tile_table(const int32_t* idx, int Tk, int E, int bm, int32_t* counts, int32_t* offsets,
+                              int32_t* perm, int32_t* inv_perm, TileEntry* tiles, int32_t* num_tiles,
+                              cudaStream_t stream) {
+  tile_table_kernel<<<1, kRouteThreads, 0, stream>>>(idx, Tk, E, bm, counts, offsets, perm, inv_perm, tiles,
+                                                      num_tiles);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

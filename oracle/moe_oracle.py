@@ -72,15 +72,14 @@ def decode_mxfp4(codes: np.ndarray, scales: np.ndarray, dtype=np.float32) -> np.
     nibble), ``scales`` [..., K/32]; returns [..., K] in ``dtype``.  Every value is
     E2M1[code] * 2^(s - 127), exact in float32."""
     codes = np.asarray(codes, dtype=np.uint8)
-    lo = codes & 0x0F
-    hi = codes >> 4
-    nib = np.stack([lo, hi], axis=-1).reshape(codes.shape[:-1] + (codes.shape[-1] * 2,))
-    vals = np.asarray(E2M1_VALUES, dtype=dtype)[nib]
+    K = codes.shape[-1] * 2
+    # byte b holds two codes: (b & 15) at the even K index, (b >> 4) at the odd one
+    pair = np.array([[E2M1_VALUES[b & 0x0F], E2M1_VALUES[b >> 4]] for b in range(256)], dtype=dtype)
+    vals = pair[codes].reshape(codes.shape[:-1] + (K // 32, 32))
     sc = decode_e8m0(scales, dtype)
-    K = nib.shape[-1]
     if sc.shape[-1] * 32 != K:
         raise ValueError("scales must hold one byte per 32 codes")
-    return vals * np.repeat(sc, 32, axis=-1)
+    return (vals * sc[..., None]).reshape(codes.shape[:-1] + (K,))
 
 
 def router_logits(x_bits: np.ndarray, w_router_bits: np.ndarray, bias=None,

@@ -145,7 +145,7 @@ def random_logits(T: int, E: int, seed: int = 0, n_ties: int = 0) -> np.ndarray:
     planted between two experts so tie-breaking is exercised."""
     rng = np.random.Generator(np.random.PCG64(seed))
     lg = rng.standard_normal((T, E), dtype=np.float32)
-    for t in range(min(n_ties, T)):
+    for t in range(min(n_ties, T) if E >= 2 else 0):
         a, b = rng.choice(E, size=2, replace=False)
         lg[t, b] = lg[t, a]
     return lg

@@ -1,0 +1,179 @@
+"""GPU parity of the MXFP4 expert path: the one-time weight re-layout (byte
+exact), the gate/up + SwiGLU output h, and the whole layer against the oracle on
+the five gpt-oss-shaped workloads plus ragged and degenerate shapes."""
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from synthetic import make_config, make_layer
+from tests.gpu_helpers import TOL_MAX_ABS, TOL_REL_FROB, bf16_bits_to_f32, bf16_to_np, build_layer, errors, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def expected_prepared(codes: np.ndarray, scales: np.ndarray, groups: int) -> np.ndarray:
+    """The documented prepared layout, restated: codes [E][R][Kp/2] zero padded, then
+    (256-aligned) scale atoms [E][G][MT][KG][32 l][4 c][4 b] = scale of row
+    32c + l of the M tile, MX block 4*kg + b (127 outside the matrix), then a
+    256-byte status trailer."""
+    E, R, half = codes.shape
+    K = half * 2
+    Kp = math.ceil(K / 128) * 128
+    rpg = R // groups
+    MT = math.ceil(rpg / 128)
+    KG = Kp // 128
+    cp = np.zeros((E, R, Kp // 2), np.uint8)
+    cp[:, :, :half] = codes
+    sc = np.full((E, groups, MT, KG, 32, 4, 4), 127, np.uint8)
+    blocks = K // 32
+    for mt in range(MT):
+        for c in range(4):
+            for l in range(32):
+                row = mt * 128 + 32 * c + l
+                if row >= rpg:
+                    continue
+                for g in range(groups):
+                    src = scales[:, g * rpg + row, :]  # [E, blocks]
+                    for kg in range(KG):
+                        for b in range(4):
+                            blk = kg * 4 + b
+                            if blk < blocks:
+                                sc[:, g, mt, kg, l, c, b] = src[:, blk]
+    codes_bytes = cp.size
+    scales_off = (codes_bytes + 255) // 256 * 256
+    total = (scales_off + sc.size + 255) // 256 * 256 + 256
+    out = np.zeros(total, np.uint8)
+    out[:codes_bytes] = cp.reshape(-1)
+    out[scales_off:scales_off + sc.size] = sc.reshape(-1)
+    return out, scales_off + sc.size
+
+
+@pytest.mark.parametrize("E,I,H", [(8, 256, 256), (3, 96, 160), (2, 2880, 2880)])
+def test_prepare_weights_byte_exact(E, I, H):
+    import mxfp4_expert_layer_gb300 as pkg
+    from mxfp4_expert_layer_gb300 import _lib as L
+    pkg.build()
+    inp = make_layer(T=1, H=H, I=I, E=E, k=1, seed=11)
+    for codes, scales, kind, groups in ((inp.gu_codes, inp.gu_scales, L.MOE_WEIGHTS_GATEUP, 2),
+                                        (inp.dn_codes, inp.dn_scales, L.MOE_WEIGHTS_DOWN, 1)):
+        got = pkg.prepare_weights(to_dev(codes), to_dev(scales), kind).cpu().numpy()
+        want, used = expected_prepared(codes, scales, groups)
+        assert got.size == want.size
+        assert np.array_equal(got[:used], want[:used])
+
+
+def test_prepare_rejects_nan_scale():
+    import mxfp4_expert_layer_gb300 as pkg
+    from mxfp4_expert_layer_gb300 import _lib as L
+    pkg.build()
+    inp = make_layer(T=1, H=64, I=64, E=2, k=1, seed=1)
+    sc = inp.gu_scales.copy()
+    sc[1, 5, 1] = 255
+    with pytest.raises(L.MoEError) as ei:
+        pkg.prepare_weights(to_dev(inp.gu_codes), to_dev(sc), L.MOE_WEIGHTS_GATEUP)
+    assert ei.value.status == L.MOE_ERR_NAN_SCALE
+
+
+def run_layer(inp, tokens=None):
+    import torch
+    layer = build_layer(inp)
+    x = to_dev(inp.x)
+    idx = torch.empty(inp.T, inp.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(inp.T, inp.k, dtype=torch.float32, device="cuda")
+    out = layer(x, topk_idx=idx, topk_w=w)
+    torch.cuda.synchronize()
+    assert layer.device_status(inp.T) == 0
+    return layer, bf16_bits_to_f32(bf16_to_np(out)), idx.cpu().numpy(), w.cpu().numpy()
+
+
+def check_layer(inp, tokens=None, margin=1e-4):
+    layer, out, idx, w = run_layer(inp)
+    ref = oracle.moe_layer(inp, tokens=tokens)
+    tok = ref["tokens"]
+    # compare tokens whose routing is not a near tie under fp32 logit rounding
+    keep = oracle.topk_margin(ref["logits"], inp.k) > margin
+    assert keep.mean() > 0.9
+    assert np.array_equal(idx[tok][keep], ref["idx"][keep])
+    rel, mx = errors(out[tok][keep], ref["out"][keep])
+    assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)
+    return rel, mx
+
+
+def test_layer_tiny():
+    check_layer(make_config("tiny"))
+
+
+def test_layer_gptoss20b_b1():
+    check_layer(make_config("gptoss20b_b1"))
+
+
+def test_layer_gptoss20b_b64():
+    check_layer(make_config("gptoss20b_b64"))
+
+
+def test_layer_gptoss120b_b64_sampled():
+    check_layer(make_config("gptoss120b_b64"), tokens=np.arange(0, 64, 4))
+
+
+def test_layer_gptoss120b_prefill4096_sampled():
+    inp = make_config("gptoss120b_prefill4096")
+    check_layer(inp, tokens=np.random.default_rng(0).choice(inp.T, 24, replace=False))
+
+
+@pytest.mark.parametrize("T,H,I,E,k", [(200, 256, 256, 16, 2),    # 64-row tiles, ragged tails
+                                       (1000, 256, 512, 8, 2),    # 128-row tiles
+                                       (13, 160, 96, 3, 3),       # k = E, I < one M tile, K tails
+                                       (5, 64, 64, 1, 1),         # one expert: dense FFN
+                                       (33, 2880, 2880, 4, 1)])   # gpt-oss widths, K = 22.5 groups
+def test_layer_ragged_and_degenerate(T, H, I, E, k):
+    check_layer(make_layer(T, H, I, E, k, seed=T + E))
+
+
+def test_hidden_matches_oracle():
+    import torch
+    from mxfp4_expert_layer_gb300 import _lib as L
+    inp = make_config("gptoss20b_b64")
+    layer = build_layer(inp)
+    T, H, I, E, k = inp.T, inp.H, inp.I, inp.E, inp.k
+    x = to_dev(inp.x)
+    # identical routing on both sides: route on the oracle's logits
+    ref_lg = oracle.router_logits(inp.x, inp.w_router)
+    _, idx, w = __import__("mxfp4_expert_layer_gb300").route(None, None, k, logits=to_dev(ref_lg),
+                                                               from_logits=True)
+    tab = __import__("mxfp4_expert_layer_gb300").build_tile_table(idx, E)
+    ws = layer.workspace(T)
+    st = L.moe_mxfp4_gateup_swiglu(x.data_ptr(), tab["perm"].data_ptr(), tab["tiles"].data_ptr(),
+                                   tab["num_tiles"].data_ptr(), 0, layer.w_gateup.data_ptr(), T, H, I, E, k,
+                                   ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    h = torch.zeros(T * k, I, dtype=torch.float32, device="cuda")
+    st = L.moe_hidden_dequant(tab["perm"].data_ptr(), tab["tiles"].data_ptr(), tab["num_tiles"].data_ptr(), 0, T,
+                              H, I, E, k, ws.data_ptr(), ws.numel(), h.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    out = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    st = L.moe_mxfp4_down_combine(tab["perm"].data_ptr(), tab["tiles"].data_ptr(), tab["num_tiles"].data_ptr(), 0,
+                                  w.data_ptr(), layer.w_down.data_ptr(), T, H, I, E, k, ws.data_ptr(), ws.numel(),
+                                  out.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    ref = oracle.moe_layer(inp, logits=ref_lg, return_hidden=True)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    rel_h, mx_h = errors(h.cpu().numpy().reshape(T, k, I), ref["h"])
+    assert rel_h <= 3e-3, (rel_h, mx_h)
+    rel, mx = errors(bf16_bits_to_f32(bf16_to_np(out)), ref["out"])
+    assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)
+
+
+def test_layer_is_bit_reproducible():
+    import torch
+    inp = make_config("gptoss20b_b64")
+    layer = build_layer(inp)
+    x = to_dev(inp.x)
+    a = layer(x).clone()
+    b = layer(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

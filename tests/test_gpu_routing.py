@@ -1,0 +1,76 @@
+"""GPU parity of the routing stages against the oracle: top-k and softmax from
+identical logits (bit-exact indices), router logits, and the tile table
+(bit-exact counts, offsets, permutation and tiles)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from synthetic import make_config, make_layer, random_logits, random_topk_idx
+from tests.gpu_helpers import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def api():
+    import mxfp4_expert_layer_gb300 as pkg
+    pkg.build()
+    from mxfp4_expert_layer_gb300 import api
+    return api
+
+
+@pytest.mark.parametrize("T,E,k,seed", [(4, 8, 2, 0), (1, 32, 4, 1), (64, 32, 4, 2), (64, 128, 4, 3),
+                                        (4096, 128, 4, 4), (37, 256, 8, 5), (9, 5, 5, 6), (3, 1, 1, 7)])
+def test_topk_softmax_from_identical_logits(api, T, E, k, seed):
+    lg = random_logits(T, E, seed=seed, n_ties=T // 3)
+    _, idx, w = api.route(None, None, k, logits=to_dev(lg), from_logits=True)
+    ref_idx, ref_w = oracle.topk_softmax(lg, k)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("gptoss20b_b1", None), ("gptoss20b_b64", None),
+                                    ("gptoss120b_b64", None), ("gptoss120b_prefill4096", None)])
+def test_router_logits_and_selection(api, name, T):
+    inp = make_config(name, T=T)
+    x, wr = to_dev(inp.x), to_dev(inp.w_router)
+    bias = None if inp.router_bias is None else to_dev(inp.router_bias)
+    lg, idx, w = api.route(x, wr, inp.k, bias=bias)
+    ref = oracle.router_logits(inp.x, inp.w_router, inp.router_bias)
+    got = lg.cpu().numpy()
+    # fp32 sums of H products in a different order: bound by H * eps * sum|x w|
+    xa = np.abs(oracle.bf16_to_f32(inp.x)).astype(np.float64)
+    wa = np.abs(oracle.bf16_to_f32(inp.w_router)).astype(np.float64)
+    bound = inp.H * 2.0 ** -24 * (xa @ wa.T) + 1e-6
+    assert np.all(np.abs(got - ref) <= bound)
+    # selections agree wherever the top-k margin exceeds the logit error
+    margin = oracle.topk_margin(ref, inp.k)
+    ok = margin > 1e-4
+    ref_idx, ref_w = oracle.topk_softmax(ref, inp.k)
+    assert np.array_equal(idx.cpu().numpy()[ok], ref_idx[ok])
+    np.testing.assert_allclose(w.cpu().numpy()[ok], ref_w[ok], rtol=1e-4, atol=1e-6)
+    assert ok.mean() > 0.9
+
+
+CASES = [(4, 8, 2, 16, 0.0), (1, 32, 4, 16, 0.0), (64, 32, 4, 16, 0.0), (64, 128, 4, 16, 0.0),
+         (4096, 128, 4, 128, 1.1), (4096, 128, 4, 64, 0.0), (777, 16, 2, 64, 1.5), (300, 1, 1, 128, 0.0),
+         (50, 256, 8, 16, 0.7), (2048, 8, 8, 128, 0.0)]
+
+
+@pytest.mark.parametrize("T,E,k,bm,skew", CASES)
+def test_tile_table_bit_exact(api, T, E, k, bm, skew):
+    idx = random_topk_idx(T, E, k, seed=T + E + k, skew=skew)
+    got = api.build_tile_table(to_dev(idx), E, bm)
+    ref = oracle.tile_table(idx, E, bm)
+    for key in ("counts", "offsets", "perm", "inv_perm"):
+        assert np.array_equal(got[key].cpu().numpy(), ref[key]), key
+    n = int(got["num_tiles"].item())
+    assert n == ref["num_tiles"]
+    assert np.array_equal(got["tiles"].cpu().numpy()[:n], ref["tiles"])
+
+
+def test_tile_table_policy_rows(api):
+    for T, E, k in [(1, 32, 4), (64, 128, 4), (4096, 128, 4), (512, 32, 4)]:
+        assert api.tile_rows(T, k, E) == oracle.tile_rows_policy(T, k, E)
+        assert api.max_tiles(T, k, E, 16) == oracle.max_tiles_bound(T, k, E, 16)

@@ -106,6 +106,26 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* router_b
               float* logits, int flags, int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
               moe_stream_t stream);
 
+/* moe_route_noalloc: moe_route for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point; it exists for callers such as
+ * a serving runtime that owns a fixed memory pool, or a plugin that is handed only
+ * its input and output buffers, which have no way to call cudaMalloc for the
+ * workspace moe_route wants.  It computes exactly what moe_route computes, with
+ * the same arguments minus the workspace: the small scratch moe_route keeps in
+ * the workspace (a status word and the arrival counters of its last-block
+ * hand-off) lives instead in a fixed array compiled into the library,
+ * 256 + 4 * (8192 / 8 + 1) = 4356 bytes, which every GPU that loads the library
+ * holds until the process exits.
+ *   T must be <= 8192: larger T returns MOE_ERR_UNSUPPORTED_SHAPE.
+ *   The first call on a device looks up the array's device address for that
+ *   device (once per device, with it current); make that first call before any
+ *   stream capture.  Each call clears the counters it uses on `stream` before
+ *   launching, so it neither allocates nor needs initialised memory.
+ *   All calls share the one array: calls that overlap on the GPU (on different
+ *   streams, or from several threads) race and must be serialised by the caller. */
+int moe_route_noalloc(const uint16_t* x, const uint16_t* w_router, const float* router_bias, int T, int H, int E,
+                      int k, float* logits, int flags, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
 /* moe_build_tile_table: the per-expert tile table of a routing ("Per-expert
  * routing tile table": each expert writes its own tiles).  Atomic-free counting
  * sort, deterministic:

@@ -35,6 +35,7 @@ SIGNATURES = {
     "moe_max_tiles": (_I, [_I, _I, _I, _I]),
     "moe_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
+    "moe_route_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
     "moe_build_tile_table": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_mxfp4_gateup_swiglu": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _S, _P]),
     "moe_mxfp4_down_combine": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P]),
@@ -91,6 +92,7 @@ moe_tile_rows = _call("moe_tile_rows")
 moe_max_tiles = _call("moe_max_tiles")
 moe_workspace_bytes = _call("moe_workspace_bytes")
 moe_route = _call("moe_route")
+moe_route_noalloc = _call("moe_route_noalloc")
 moe_build_tile_table = _call("moe_build_tile_table")
 moe_mxfp4_gateup_swiglu = _call("moe_mxfp4_gateup_swiglu")
 moe_mxfp4_down_combine = _call("moe_mxfp4_down_combine")

@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA-graph replays")
+    ap.add_argument("--profile", action="store_true",
+                    help="minimal run for ncu: no pre-warm, no graphs, no CPU baseline, no clock sampling")
     return ap.parse_args()
 
 
@@ -241,40 +244,90 @@ def main():
     wsets = [(layer.w_gateup, layer.w_down)] + [(layer.w_gateup.clone(), layer.w_down.clone())
                                                for _ in range(copies - 1)]
     ws = layer.workspace(T)
-    stream = torch.cuda.current_stream()
 
     def call(i, events=None):
         wgu, wd = wsets[i % copies]
         b = None if bias is None else bias.data_ptr()
+        cs = torch.cuda.current_stream().cuda_stream
         if events is None:
             st = L.moe_forward(x.data_ptr(), wr.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
-                               ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, stream.cuda_stream)
+                               ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, cs)
         else:
             st = L.moe_forward_timed(x.data_ptr(), wr.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
-                                     ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, events,
-                                     stream.cuda_stream)
+                                     ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, events, cs)
         if st != 0:
             raise RuntimeError(f"moe_forward failed: {L.moe_error_string(st).decode()}")
 
     launches = L.moe_forward_launches(T, H, I, E, k)
+    if args.profile:
+        for s_ in range(args.warmup + args.steps):
+            call(s_)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": inp.name, "calls": args.warmup + args.steps,
+                          "status": layer.device_status(T)}))
+        return
+
+    # one CUDA graph per weight copy: a replay is one step (the layer runs inside a
+    # captured decode step in the pages' engine); --eager times plain launches
+    nk = launches
+    names = ["route_topk_table", "gather_encode_x", "gateup_swiglu", "down_combine"]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graphs, tgraphs, tevents = [], [], []
+    hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    hx.copy_(x.cpu())
+    hout = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    e2e_graphs = []
+    with torch.cuda.stream(side):
+        call(0)
+        torch.cuda.synchronize()
+        for j in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                call(j)
+            graphs.append(g)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+            for e in evs:
+                e.record(side)
+            torch.cuda.synchronize()
+            tg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(tg, stream=side):
+                call(j, ctypes_array(evs))
+            tgraphs.append(tg)
+            tevents.append(evs)
+            eg = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(eg, stream=side):
+                x.copy_(hx, non_blocking=True)
+                call(j)
+                hout.copy_(out, non_blocking=True)
+            e2e_graphs.append(eg)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        if args.eager:
+            call(i)
+        else:
+            graphs[i % copies].replay()
+
     clocks = ClockSampler(local)
-    # pre-warm: bring clocks up (~0.5 s of calls), then the W warm-up steps
+    # pre-warm: bring clocks up (~0.5 s of steps), then the W warm-up steps
     t_end = time.perf_counter() + 0.5
     i = 0
     while time.perf_counter() < t_end:
         for _ in range(20):
-            call(i)
+            step(i)
             i += 1
         torch.cuda.synchronize()
     for _ in range(args.warmup):
-        call(i)
+        step(i)
         i += 1
     barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for s in range(args.steps):
-        call(i + s)
+    for s_ in range(args.steps):
+        step(i + s_)
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -282,23 +335,25 @@ def main():
     ms = max_over_ranks(ms, world)
     i += args.steps
 
-    # per-kernel split with events between the launches (same calls, separate loop)
-    nk = launches
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(args.steps)]
-    for row in evs:          # torch creates the CUDA event on its first record
-        for e in row:
-            e.record(stream)
-    handles = [(ctypes_array(e)) for e in evs]
+    # eager launches, for reference (host launch overhead included)
     torch.cuda.synchronize()
-    for s in range(args.steps):
-        call(i + s, handles[s])
+    ev0.record(stream)
+    for s_ in range(args.steps):
+        call(i + s_)
+    ev1.record(stream)
     torch.cuda.synchronize()
+    eager_ms = ev0.elapsed_time(ev1) / args.steps
+
+    # per-kernel split: graphs with events between the launches
     per_kernel = [0.0] * nk
-    for s in range(args.steps):
-        for j in range(nk):
-            per_kernel[j] += evs[s][j].elapsed_time(evs[s][j + 1])
-    per_kernel = [v / args.steps for v in per_kernel]
-    names = ["route_topk_table", "gather_encode_x", "gateup_swiglu", "down_combine"]
+    reps = max(1, args.steps // copies)
+    for r in range(reps):
+        for j in range(copies):
+            tgraphs[j].replay()
+            torch.cuda.synchronize()
+            for q in range(nk):
+                per_kernel[q] += tevents[j][q].elapsed_time(tevents[j][q + 1])
+    per_kernel = [v / (reps * copies) for v in per_kernel]
     alg = {"gateup_swiglu": gu_bytes, "down_combine": dn_bytes}
     dom = max(alg, key=lambda n: per_kernel[names.index(n)])
     dom_ms = per_kernel[names.index(dom)]
@@ -306,17 +361,12 @@ def main():
     achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
     clk = clocks.stop()
 
-    # end to end: pinned host input -> device, layer, device -> pinned host output, every step
-    hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
-    hx.copy_(x.cpu())
-    hout = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    # end to end through the C ABI: pinned host input -> device, layer, device -> pinned host
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for s in range(args.steps):
-        x.copy_(hx, non_blocking=True)
-        call(i + s)
-        hout.copy_(out, non_blocking=True)
+    for s_ in range(args.steps):
+        e2e_graphs[(i + s_) % copies].replay()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
@@ -335,6 +385,8 @@ def main():
                    "l2": f"{copies} rotating weight copies ({copies * alg_bytes / 1e6:.0f} MB touched per "
                          f"rotation > 4x L2)", "parallelism": f"replicas x{world}"},
         "us_per_call": us,
+        "timing": "eager launches" if args.eager else "CUDA graph replay per step",
+        "eager_us_per_call": eager_ms * 1e3,
         "layer_hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "layer_roofline_frac": alg_bytes / (ms * 1e-3) / 1e9 / peak,
         "per_kernel_us": {n: v * 1e3 for n, v in zip(names, per_kernel)},

@@ -132,7 +132,7 @@ int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, c
                const void* w_gateup, int T, int H, int I, int E, int k, void* ws, const WsLayout& L,
                cudaStream_t stream, void* const* events = nullptr) {
   // events (optional): [0] before the gather/encode launch, [1] before the GEMM
-  if (events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[0]), stream);
+  if (events) cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(events[0]), stream, cudaEventRecordExternal);
   QuantXParams q{};
   q.x = x;
   q.perm = perm;
@@ -172,7 +172,7 @@ int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, c
   g.h_sf_lo = ws_ptr<uint8_t>(ws, L.h_sf_lo);
   g.kg_out = L.kg_i;
   g.status = ws_ptr<uint32_t>(ws, L.status);
-  if (events) cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[1]), stream);
+  if (events) cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(events[1]), stream, cudaEventRecordExternal);
   return cuda_status(launch_gateup(g, stream));
 }
 
@@ -408,7 +408,10 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   r.num_tiles = num_tiles;
   bool ev_ok = true;
   auto mark = [&](int i) {
-    if (events && cudaEventRecord(reinterpret_cast<cudaEvent_t>(events[i]), s) != cudaSuccess) ev_ok = false;
+    // external: during stream capture the record becomes a real event node of the graph
+    if (events && cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(events[i]), s, cudaEventRecordExternal) !=
+                      cudaSuccess)
+      ev_ok = false;
   };
   mark(0);
   if (!ev_ok) return MOE_ERR_INVALID_ARG;

@@ -12,20 +12,18 @@ namespace moe {
 namespace {
 constexpr int kAuxThreads = 256;
 
-__device__ __forceinline__ void encode_block_two_term(float v, uint8_t& q1, uint8_t& q2, int& p1, int& p2) {
-  float a = fabsf(v);
-  a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
-  p1 = mx_e4m3_exponent(a);
-  q1 = f32_to_e4m3(v * pow2_int(-p1));
-  const float r = v - e4m3_to_f32(q1) * pow2_int(p1);
-  float ar = fabsf(r);
-  ar = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(ar)));
-  p2 = mx_e4m3_exponent(ar);
-  q2 = f32_to_e4m3(r * pow2_int(-p2));
-}
 }  // namespace
 
-// One warp per padded tile row: gather x[token], encode each 32-value block.
+// Max over the 4 lanes (aligned groups of 4) that hold one 32-value MX block.
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  return v;
+}
+
+// One warp per padded tile row: gather x[token] and encode each 32-value block as
+// two E4M3 terms.  Each lane owns 8 consecutive values (one 16-byte load), so four
+// lanes form a block and a warp covers 256 values per step.
 __global__ void __launch_bounds__(kAuxThreads) quant_x_kernel(QuantXParams p) {
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
@@ -43,24 +41,63 @@ __global__ void __launch_bounds__(kAuxThreads) quant_x_kernel(QuantXParams p) {
   if (r >= te.n_rows) return;
   const int a = __ldg(p.perm + te.row_begin + r);
   const int t = a / p.k;
-  const uint16_t* xr = p.x + (size_t)t * p.H;
-  uint8_t* qh = p.q_hi + (size_t)row * p.H;
-  uint8_t* ql = p.q_lo + (size_t)row * p.H;
+  const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H);
+  uint2* qh = reinterpret_cast<uint2*>(p.q_hi + (size_t)row * p.H);
+  uint2* ql = reinterpret_cast<uint2*>(p.q_lo + (size_t)row * p.H);
   const int nb = sf_atoms_per_tile(p.bm);
   uint8_t* sfh = p.sf_hi + (size_t)tile * p.kg * (kSfAtomBytes * nb);
   uint8_t* sfl = p.sf_lo + (size_t)tile * p.kg * (kSfAtomBytes * nb);
-  const int blocks = p.H / kMxBlock;
-  for (int b = 0; b < blocks; ++b) {
-    const float v = __uint_as_float(static_cast<uint32_t>(__ldg(xr + b * kMxBlock + lane)) << 16);
-    uint8_t q1, q2;
-    int p1, p2;
-    encode_block_two_term(v, q1, q2, p1, p2);
-    qh[b * kMxBlock + lane] = q1;
-    ql[b * kMxBlock + lane] = q2;
-    if (lane == 0) {
-      const size_t off = (size_t)(b >> 2) * (kSfAtomBytes * nb) + sf_atom_offset(r, b & 3);
-      sfh[off] = static_cast<uint8_t>(p1 + 127);
-      sfl[off] = static_cast<uint8_t>(p2 + 127);
+  const int nvec = p.H / 8;
+  for (int v0 = 0; v0 < nvec; v0 += 32) {
+    const int v = v0 + lane;
+    const bool valid = v < nvec;
+    float f[8];
+    if (valid) {
+      const uint4 raw = __ldg(xr + v);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
+    amax = quad_max(amax);
+    const int p1 = mx_e4m3_exponent(amax);
+    const float inv1 = pow2_int(-p1), sc1 = pow2_int(p1);
+    uint8_t q1[8];
+    float res[8], amax2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      q1[i] = f32_to_e4m3(f[i] * inv1);
+      res[i] = f[i] - e4m3_to_f32(q1[i]) * sc1;
+      amax2 = fmaxf(amax2, fabsf(res[i]));
+    }
+    amax2 = quad_max(amax2);
+    const int p2 = mx_e4m3_exponent(amax2);
+    const float inv2 = pow2_int(-p2);
+    uint8_t q2[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q2[i] = f32_to_e4m3(res[i] * inv2);
+    if (valid) {
+      uint2 h, l;
+      h.x = q1[0] | (q1[1] << 8) | (q1[2] << 16) | ((uint32_t)q1[3] << 24);
+      h.y = q1[4] | (q1[5] << 8) | (q1[6] << 16) | ((uint32_t)q1[7] << 24);
+      l.x = q2[0] | (q2[1] << 8) | (q2[2] << 16) | ((uint32_t)q2[3] << 24);
+      l.y = q2[4] | (q2[5] << 8) | (q2[6] << 16) | ((uint32_t)q2[7] << 24);
+      qh[v] = h;
+      ql[v] = l;
+      if ((lane & 3) == 0) {
+        const int b = v >> 2;  // MX block index along H
+        const size_t off = (size_t)(b >> 2) * (kSfAtomBytes * nb) + sf_atom_offset(r, b & 3);
+        sfh[off] = static_cast<uint8_t>(p1 + 127);
+        sfl[off] = static_cast<uint8_t>(p2 + 127);
+      }
     }
   }
 }

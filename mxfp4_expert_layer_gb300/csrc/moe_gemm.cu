@@ -331,8 +331,16 @@ template <int BM, bool GATEUP>
 static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
   using C = GemmCfg<BM, GATEUP>;
   auto kern = moe_gemm_kernel<BM, GATEUP>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
+  }
   const int units = p.max_tiles * p.mt;
   kern<<<units, kGemmThreads, C::kSmemBytes, stream>>>(p);
   return cudaGetLastError();

@@ -297,8 +297,15 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
   const size_t smem = p.from_logits ? 0 : (size_t)kTokensPerGroup * p.H * sizeof(uint16_t);
   // static (tile-table scratch) + dynamic (activation tile) shared memory may exceed
   // the 48 KB default window
-  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static int configured_smem[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || configured_smem[dev] < (int)smem) {
+    e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) configured_smem[dev] = (int)smem;
+  }
   route_kernel<<<grid, kRouteThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }

@@ -75,12 +75,12 @@ MapCache& map_cache() {
 
 // Encodes (or fetches from a small cache) a tiled tensor map; false on failure.
 bool make_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box) {
+              const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
   MapKey key;
   std::memset(&key, 0, sizeof key);
   key.ptr = ptr;
   key.dtype = (int)dtype;
-  key.rank = rank;
+  key.rank = rank * 16 + (int)swizzle;
   for (int i = 0; i < rank; ++i) {
     key.dims[i] = dims[i];
     key.box[i] = box[i];
@@ -98,7 +98,7 @@ bool make_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, int 
   if (!enc) return false;
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = enc(out, dtype, rank, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return false;
   const int slot = c.next;
   c.next = (c.next + 1) % MapCache::kSlots;
@@ -108,54 +108,80 @@ bool make_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, int 
   return true;
 }
 
-// MXFP4 codes of one prepared family as a 4-D map {Kp, rows per group, groups, E}.
+// MXFP4 codes of one prepared family as a 4-D byte map {64 bytes = 128 codes, rows
+// per group, KG, E * groups}: one box = 128 consecutive rows of one K group, a
+// contiguous 8 KB kept packed in shared memory with the 64-byte swizzle.  Rows past
+// the group (the last M tile) are outside the map and read as zero.
 bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P) {
-  cuuint64_t dims[4] = {(cuuint64_t)P.Kp, (cuuint64_t)P.rows_per_group, (cuuint64_t)P.groups, (cuuint64_t)P.E};
-  const cuuint64_t row = (cuuint64_t)P.Kp / 2;
-  cuuint64_t strides[3] = {row, row * P.rows_per_group, row * P.rows_per_group * P.groups};
-  cuuint32_t box[4] = {(cuuint32_t)kKGroup, (cuuint32_t)kMTile, 1, 1};
-  return make_map(out, prepared, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, dims, strides, box);
+  cuuint64_t dims[4] = {64, (cuuint64_t)P.rows_per_group, (cuuint64_t)P.kg, (cuuint64_t)P.E * P.groups};
+  cuuint64_t strides[3] = {64, 64ull * P.rows_per_group, 64ull * P.rows_per_group * P.kg};
+  cuuint32_t box[4] = {64, (cuuint32_t)kMTile, 1, 1};
+  return make_map(out, prepared, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// E4M3 activation rows {K, pad_rows}, boxes of 128 x bm.
-bool act_map(CUtensorMap* out, const void* base, int K, int rows, int bm) {
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
-  cuuint32_t box[2] = {(cuuint32_t)kKGroup, (cuuint32_t)bm};
-  return make_map(out, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, dims, strides, box);
+// Encoded activations {64 bytes, max_tiles * kTerms * bm rows, KG}: one tile's
+// kTerms * bm rows of a K group are contiguous (boxes of at most 256 rows).
+bool act_map(CUtensorMap* out, const void* base, int K, int max_tiles, int bm) {
+  const cuuint64_t rows = (cuuint64_t)max_tiles * kTerms * bm;
+  cuuint64_t dims[3] = {64, rows, (cuuint64_t)ceil_div(K, kKGroup)};
+  cuuint64_t strides[2] = {64, 64 * rows};
+  const int box_rows = kTerms * bm < 256 ? kTerms * bm : 256;
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  return make_map(out, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Records a caller event; while the stream is being captured the record is made an
+// external event node so the event is recorded on every replay of the graph.
+cudaError_t record_event(void* ev, cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &cs);
+  if (e != cudaSuccess) return e;
+  if (cs == cudaStreamCaptureStatusActive)
+    return cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(ev), s, cudaEventRecordExternal);
+  return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), s);
+}
+
+// One persistent GEMM CTA per SM of the current device (cached per device).
+int persistent_ctas() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kMaxCtas;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int sms = kMaxCtas;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = kMaxCtas;
+  if (sms > kMaxCtas) sms = kMaxCtas;
+  if (sms < 1) sms = 1;
+  if (dev >= 0 && dev < 64) cached[dev] = sms;
+  return sms;
+}
 
 // ------------------------------------------------------------------ stage bodies
 int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm,
                const void* w_gateup, int T, int H, int I, int E, int k, void* ws, const WsLayout& L,
                cudaStream_t stream, void* const* events = nullptr) {
   // events (optional): [0] before the gather/encode launch, [1] before the GEMM
-  if (events) cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(events[0]), stream, cudaEventRecordExternal);
+  if (events) record_event(events[0], stream);
   QuantXParams q{};
   q.x = x;
   q.perm = perm;
   q.tiles = tiles;
   q.num_tiles = num_tiles;
   q.T = T; q.H = H; q.k = k; q.bm = bm; q.max_tiles = L.max_tiles; q.kg = L.kg_h;
-  q.q_hi = ws_ptr<uint8_t>(ws, L.x_hi);
-  q.q_lo = ws_ptr<uint8_t>(ws, L.x_lo);
-  q.sf_hi = ws_ptr<uint8_t>(ws, L.x_sf_hi);
-  q.sf_lo = ws_ptr<uint8_t>(ws, L.x_sf_lo);
+  q.q = ws_ptr<uint8_t>(ws, L.x_q);
+  q.sf = ws_ptr<uint8_t>(ws, L.x_sf);
   q.zero_buf = ws_ptr<int32_t>(ws, L.combine_cnt);
-  q.zero_count = T * L.mt_h;
+  q.zero_count = (int)(L.zero_bytes / sizeof(int32_t));
   cudaError_t e = launch_quant_x(q, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   const PreparedLayout P = make_prepared_layout(E, 2 * I, H, 2);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_gateup, P)) return MOE_ERR_CUDA;
-  if (!act_map(&g.tm_act_hi, q.q_hi, H, L.pad_rows, bm)) return MOE_ERR_CUDA;
-  if (!act_map(&g.tm_act_lo, q.q_lo, H, L.pad_rows, bm)) return MOE_ERR_CUDA;
+  if (!act_map(&g.tm_act, q.q, H, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_gateup) + P.scales_off;
-  g.act_sf_hi = q.sf_hi;
-  g.act_sf_lo = q.sf_lo;
+  g.act_sf = q.sf;
   g.tiles = tiles;
   g.num_tiles = num_tiles;
   g.perm = perm;
@@ -165,14 +191,15 @@ int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, c
   g.mt = L.mt_i;
   g.rows_out = I;
   g.w_groups = 2;
-  g.group_tiles = bm >= 64 ? 8 : 1;
-  g.h_hi = ws_ptr<uint8_t>(ws, L.h_hi);
-  g.h_lo = ws_ptr<uint8_t>(ws, L.h_lo);
-  g.h_sf_hi = ws_ptr<uint8_t>(ws, L.h_sf_hi);
-  g.h_sf_lo = ws_ptr<uint8_t>(ws, L.h_sf_lo);
+  g.group_tiles = bm >= 128 ? 32 : (bm >= 64 ? 16 : 1);
+  g.h_q = ws_ptr<uint8_t>(ws, L.h_q);
+  g.h_sf = ws_ptr<uint8_t>(ws, L.h_sf);
   g.kg_out = L.kg_i;
+  g.grid = persistent_ctas();
+  g.partials = ws_ptr<float>(ws, L.partials);
+  g.unit_cnt = ws_ptr<int32_t>(ws, L.unit_cnt);
   g.status = ws_ptr<uint32_t>(ws, L.status);
-  if (events) cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(events[1]), stream, cudaEventRecordExternal);
+  if (events) record_event(events[1], stream);
   return cuda_status(launch_gateup(g, stream));
 }
 
@@ -182,11 +209,9 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   const PreparedLayout P = make_prepared_layout(E, H, I, 1);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_down, P)) return MOE_ERR_CUDA;
-  if (!act_map(&g.tm_act_hi, ws_ptr<uint8_t>(ws, L.h_hi), I, L.pad_rows, bm)) return MOE_ERR_CUDA;
-  if (!act_map(&g.tm_act_lo, ws_ptr<uint8_t>(ws, L.h_lo), I, L.pad_rows, bm)) return MOE_ERR_CUDA;
+  if (!act_map(&g.tm_act, ws_ptr<uint8_t>(ws, L.h_q), I, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_down) + P.scales_off;
-  g.act_sf_hi = ws_ptr<uint8_t>(ws, L.h_sf_hi);
-  g.act_sf_lo = ws_ptr<uint8_t>(ws, L.h_sf_lo);
+  g.act_sf = ws_ptr<uint8_t>(ws, L.h_sf);
   g.tiles = tiles;
   g.num_tiles = num_tiles;
   g.perm = perm;
@@ -196,11 +221,14 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   g.mt = L.mt_h;
   g.rows_out = H;
   g.w_groups = 1;
-  g.group_tiles = bm >= 64 ? 8 : 1;
+  g.group_tiles = bm >= 128 ? 32 : (bm >= 64 ? 16 : 1);
   g.topk_w = topk_w;
   g.slots = ws_ptr<float>(ws, L.slots);
   g.combine_cnt = ws_ptr<int32_t>(ws, L.combine_cnt);
   g.out = out;
+  g.grid = persistent_ctas();
+  g.partials = ws_ptr<float>(ws, L.partials);
+  g.unit_cnt = ws_ptr<int32_t>(ws, L.unit_cnt);
   g.status = ws_ptr<uint32_t>(ws, L.status);
   return cuda_status(launch_down(g, stream));
 }
@@ -368,10 +396,8 @@ int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t*
   hp.tiles = reinterpret_cast<const TileEntry*>(tiles);
   hp.num_tiles = num_tiles;
   hp.I = I; hp.bm = bm; hp.max_tiles = L.max_tiles; hp.kg = L.kg_i;
-  hp.h_hi = ws_ptr<uint8_t>(ws, L.h_hi);
-  hp.h_lo = ws_ptr<uint8_t>(ws, L.h_lo);
-  hp.sf_hi = ws_ptr<uint8_t>(ws, L.h_sf_hi);
-  hp.sf_lo = ws_ptr<uint8_t>(ws, L.h_sf_lo);
+  hp.h_q = ws_ptr<uint8_t>(ws, L.h_q);
+  hp.sf = ws_ptr<uint8_t>(ws, L.h_sf);
   hp.out = h_out;
   return cuda_status(launch_hidden_dequant(hp, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -408,10 +434,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   r.num_tiles = num_tiles;
   bool ev_ok = true;
   auto mark = [&](int i) {
-    // external: during stream capture the record becomes a real event node of the graph
-    if (events && cudaEventRecordWithFlags(reinterpret_cast<cudaEvent_t>(events[i]), s, cudaEventRecordExternal) !=
-                      cudaSuccess)
-      ev_ok = false;
+    if (events && record_event(events[i], s) != cudaSuccess) ev_ok = false;
   };
   mark(0);
   if (!ev_ok) return MOE_ERR_INVALID_ARG;

@@ -6,6 +6,7 @@
 //  * hidden_dequant: expands the encoded SwiGLU output for inspection.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
 
@@ -21,106 +22,113 @@ __device__ __forceinline__ float quad_max(float v) {
   return v;
 }
 
-// One warp per padded tile row: gather x[token] and encode each 32-value block as
-// two E4M3 terms.  Each lane owns 8 consecutive values (one 16-byte load), so four
-// lanes form a block and a warp covers 256 values per step.
+// Gather + encode: one warp per (tile row, 256-value chunk of x), so every load of a
+// call is in flight at once.  Each lane owns 8 consecutive values (one 16-byte
+// load); four lanes form one 32-value MX block, and the block is written as kTerms
+// E2M1 terms x ~ sum_t q_t * 2^p_t, each term with its own E8M0 exponent chosen
+// for the residual left by the terms before.  Values past H up to the next
+// multiple of 64 are encoded as zeros so every 64-value MMA step reads finite data.
 __global__ void __launch_bounds__(kAuxThreads) quant_x_kernel(QuantXParams p) {
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
-  // clear the combine arrival counters of the down kernel (grid-stride)
+  const long long gw = ((long long)blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
+  // clear the arrival counters of the GEMM kernels (grid-stride)
   if (p.zero_buf) {
     for (int i = blockIdx.x * kAuxThreads + threadIdx.x; i < p.zero_count; i += gridDim.x * kAuxThreads)
       p.zero_buf[i] = 0;
   }
+  const int nvec_pad = ((p.H + 63) / 64) * 8;  // 8-value vectors per row, padded to 64 values
+  const int nchunks = (nvec_pad + 31) / 32;
+  const int row = (int)(gw / nchunks);
+  const int chunk = (int)(gw - (long long)row * nchunks);
   const int num_tiles = __ldg(p.num_tiles);
-  const int row = gw;
   const int tile = row / p.bm;
   if (tile >= num_tiles) return;
   const int r = row - tile * p.bm;
   const TileEntry te = p.tiles[tile];
   if (r >= te.n_rows) return;
   const int a = __ldg(p.perm + te.row_begin + r);
-  const int t = a / p.k;
-  const uint4* xr = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H);
-  uint2* qh = reinterpret_cast<uint2*>(p.q_hi + (size_t)row * p.H);
-  uint2* ql = reinterpret_cast<uint2*>(p.q_lo + (size_t)row * p.H);
-  const int nb = sf_atoms_per_tile(p.bm);
-  uint8_t* sfh = p.sf_hi + (size_t)tile * p.kg * (kSfAtomBytes * nb);
-  uint8_t* sfl = p.sf_lo + (size_t)tile * p.kg * (kSfAtomBytes * nb);
+  const int v = chunk * 32 + lane;
   const int nvec = p.H / 8;
-  for (int v0 = 0; v0 < nvec; v0 += 32) {
-    const int v = v0 + lane;
-    const bool valid = v < nvec;
-    float f[8];
-    if (valid) {
-      const uint4 raw = __ldg(xr + v);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float f[8];
+  if (v < nvec) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(a / p.k) * p.H) + v);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) f[i] = 0.f;
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = 0.f;
+  }
+  const int natoms = act_sf_atoms(p.bm);
+  uint8_t* sf = p.sf + (size_t)tile * p.kg * (kSfAtomBytes * natoms);
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t) {
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
     amax = quad_max(amax);
-    const int p1 = mx_e4m3_exponent(amax);
-    const float inv1 = pow2_int(-p1), sc1 = pow2_int(p1);
-    uint8_t q1[8];
-    float res[8], amax2 = 0.f;
+    const int pe = mx_e2m1_exponent(amax);
+    const float inv = pow2_int(-pe), sc = pow2_int(pe);
+    uint32_t word = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      q1[i] = f32_to_e4m3(f[i] * inv1);
-      res[i] = f[i] - e4m3_to_f32(q1[i]) * sc1;
-      amax2 = fmaxf(amax2, fabsf(res[i]));
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t pair = f32x2_to_e2m1x2(f[2 * i] * inv, f[2 * i + 1] * inv);
+      f[2 * i] -= e2m1_to_f32(pair & 15u) * sc;
+      f[2 * i + 1] -= e2m1_to_f32(pair >> 4) * sc;
+      word |= pair << (8 * i);
     }
-    amax2 = quad_max(amax2);
-    const int p2 = mx_e4m3_exponent(amax2);
-    const float inv2 = pow2_int(-p2);
-    uint8_t q2[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q2[i] = f32_to_e4m3(res[i] * inv2);
-    if (valid) {
-      uint2 h, l;
-      h.x = q1[0] | (q1[1] << 8) | (q1[2] << 16) | ((uint32_t)q1[3] << 24);
-      h.y = q1[4] | (q1[5] << 8) | (q1[6] << 16) | ((uint32_t)q1[7] << 24);
-      l.x = q2[0] | (q2[1] << 8) | (q2[2] << 16) | ((uint32_t)q2[3] << 24);
-      l.y = q2[4] | (q2[5] << 8) | (q2[6] << 16) | ((uint32_t)q2[7] << 24);
-      qh[v] = h;
-      ql[v] = l;
-      if ((lane & 3) == 0) {
-        const int b = v >> 2;  // MX block index along H
-        const size_t off = (size_t)(b >> 2) * (kSfAtomBytes * nb) + sf_atom_offset(r, b & 3);
-        sfh[off] = static_cast<uint8_t>(p1 + 127);
-        sfl[off] = static_cast<uint8_t>(p2 + 127);
+    // exponents of 4 consecutive MX blocks sit in lanes 0, 4, 8, 12 (and 16..28)
+    const uint32_t e8 = static_cast<uint32_t>(pe + 127);
+    const int base = lane & ~15;
+    const uint32_t sfw = __shfl_sync(0xffffffffu, e8, base) | (__shfl_sync(0xffffffffu, e8, base + 4) << 8) |
+                         (__shfl_sync(0xffffffffu, e8, base + 8) << 16) |
+                         (__shfl_sync(0xffffffffu, e8, base + 12) << 24);
+    if (v < nvec_pad) {
+      *reinterpret_cast<uint32_t*>(p.q + act_offset(tile, t, r, v * 8, p.max_tiles, p.bm)) = word;
+      if ((lane & 15) == 0) {
+        const int kgroup = v >> 4;  // 16 vectors = 128 values per K group
+        *reinterpret_cast<uint32_t*>(sf + (size_t)kgroup * (kSfAtomBytes * natoms) +
+                                     sf_atom_offset(t * p.bm + r, 0)) = sfw;
       }
     }
   }
 }
 
 cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t stream) {
-  const long long rows = (long long)p.max_tiles * p.bm;
-  const int blocks = (int)((rows * 32 + kAuxThreads - 1) / kAuxThreads);
-  quant_x_kernel<<<blocks, kAuxThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const int nvec_pad = ((p.H + 63) / 64) * 8;
+  const long long warps = (long long)p.max_tiles * p.bm * ((nvec_pad + 31) / 32);
+  const int blocks = (int)((warps * 32 + kAuxThreads - 1) / kAuxThreads);
+  return launch_pdl(quant_x_kernel, dim3(blocks), dim3(kAuxThreads), 0, stream, p);
 }
 
-// Codes: each row copied in 16-byte vectors, zero-padded from K/2 to Kp/2 bytes.
+// Codes: 16-byte vectors moved into the K-group-major layout
+// [E][G][KG][rows per group][64 bytes]; vectors past K/2 bytes of a row are zero.
 __global__ void prepare_codes_kernel(PrepareParams p) {
-  const int src_vec = p.K / 32;   // 16-byte vectors per source row (K/2 bytes)
-  const int dst_vec = p.Kp / 32;
-  const long long total = (long long)p.E * p.R * dst_vec;
+  const int src_bytes = p.K / 2;
+  const long long total = (long long)p.E * p.R * p.kg * 4;  // 4 vectors of 16 B per 64-byte run
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / dst_vec;
-    const int v = (int)(i - row * dst_vec);
+    long long t = i;
+    const int v = (int)(t & 3);
+    t >>= 2;
+    const int row = (int)(t % p.rows_per_group);
+    t /= p.rows_per_group;
+    const int kgi = (int)(t % p.kg);
+    t /= p.kg;
+    const int grp = (int)(t % p.groups);
+    const int e = (int)(t / p.groups);
+    const int byte0 = kgi * 64 + v * 16;
     uint4 val = make_uint4(0, 0, 0, 0);
-    if (v < src_vec) val = __ldg(reinterpret_cast<const uint4*>(p.codes + row * (p.K / 2)) + v);
-    reinterpret_cast<uint4*>(p.dst_codes + row * (p.Kp / 2))[v] = val;
+    if (byte0 < src_bytes) {
+      const size_t src_row = (size_t)e * p.R + (size_t)grp * p.rows_per_group + row;
+      val = __ldg(reinterpret_cast<const uint4*>(p.codes + src_row * src_bytes + byte0));
+    }
+    reinterpret_cast<uint4*>(p.dst_codes)[i] = val;
   }
 }
 
@@ -159,11 +167,11 @@ cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// out[a][i] = q_hi * 2^(s_hi - 127) + q_lo * 2^(s_lo - 127) for every tile row.
+// out[a][i] = sum_t e2m1(q_t) * 2^(s_t - 127) for every valid tile row.
 __global__ void hidden_dequant_kernel(HiddenDequantParams p) {
   const int num_tiles = __ldg(p.num_tiles);
   const long long total = (long long)num_tiles * p.bm * p.I;
-  const int nb = sf_atoms_per_tile(p.bm);
+  const int natoms = act_sf_atoms(p.bm);
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
        i += (long long)gridDim.x * blockDim.x) {
     const long long row = i / p.I;
@@ -173,9 +181,14 @@ __global__ void hidden_dequant_kernel(HiddenDequantParams p) {
     const TileEntry te = p.tiles[tile];
     if (r >= te.n_rows) continue;
     const int a = p.perm[te.row_begin + r];
-    const size_t off = ((size_t)tile * p.kg + (f >> 7)) * (kSfAtomBytes * nb) + sf_atom_offset(r, (f >> 5) & 3);
-    const float v = e4m3_to_f32(p.h_hi[row * p.I + f]) * pow2_int((int)p.sf_hi[off] - 127) +
-                    e4m3_to_f32(p.h_lo[row * p.I + f]) * pow2_int((int)p.sf_lo[off] - 127);
+    float v = 0.f;
+    for (int t = 0; t < kTerms; ++t) {
+      const uint8_t byte = p.h_q[act_offset(tile, t, r, f & ~1, p.max_tiles, p.bm)];
+      const uint32_t code = (f & 1) ? (byte >> 4) : (byte & 15u);
+      const size_t off = ((size_t)tile * p.kg + (f >> 7)) * (kSfAtomBytes * natoms) +
+                         sf_atom_offset(t * p.bm + r, (f >> 5) & 3);
+      v += e2m1_to_f32(code) * pow2_int((int)p.sf[off] - 127);
+    }
     p.out[(size_t)a * p.I + f] = v;
   }
 }

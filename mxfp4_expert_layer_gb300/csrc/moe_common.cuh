@@ -5,7 +5,6 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "moe_mxfp4.h"
@@ -19,6 +18,8 @@ constexpr int kMTile = 128;          // weight rows per MMA tile (MMA M)
 constexpr int kSfAtomBytes = 512;    // scale-factor atom: 128 rows x 4 MX blocks
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
+constexpr int kMaxCtas = 160;        // persistent GEMM CTAs (one per SM; GB300 has 152)
+constexpr int kTerms = 4;            // E2M1 terms of the activation encoding
 
 // Device status word bits (read back with moe_get_device_status).
 constexpr uint32_t kStatusTimeoutMain = 1u << 0;
@@ -73,16 +74,21 @@ struct WsLayout {
   size_t inv_perm;       // i32 [T*k]
   size_t tiles;          // TileEntry [max_tiles]
   size_t num_tiles;      // i32
-  size_t x_hi, x_lo;     // e4m3 [pad_rows, H]
-  size_t x_sf_hi, x_sf_lo;  // scale atoms [max_tiles][kg_h][512 * sf_atoms_per_tile]
-  size_t h_hi, h_lo;     // e4m3 [pad_rows, I]
-  size_t h_sf_hi, h_sf_lo;  // scale atoms [max_tiles][kg_i][512 * sf_atoms_per_tile]
+  size_t x_q;            // x encoded: [kg_h][max_tiles][kTerms][bm][64 bytes] packed E2M1
+  size_t x_sf;           // its scale atoms [max_tiles][kg_h][512 * act_sf_atoms(bm)]
+  size_t h_q;            // h encoded: [kg_i][max_tiles][kTerms][bm][64 bytes]
+  size_t h_sf;           // [max_tiles][kg_i][512 * act_sf_atoms(bm)]
   size_t slots;          // f32 [T*k, H]: weighted expert outputs awaiting the combine
   size_t combine_cnt;    // i32 [T, mt_h]: arrivals per (token, output tile)
+  size_t unit_cnt;       // i32 [max_tiles * max(mt_h, mt_i)]: arrivals per GEMM work unit
+  size_t zero_bytes;     // bytes from combine_cnt cleared before each layer call
+  size_t partials;       // f32 [2 * kMaxCtas][2 * bm * 128]: split-K partial accumulators
   size_t total;
 };
 
-__host__ __device__ inline int sf_atoms_per_tile(int bm) { return bm > 128 ? 2 : 1; }
+// Scale atoms (128 rows each) per tile and K group of an encoded activation: the
+// tile's rows are the kTerms terms of its bm token rows, term-major.
+__host__ __device__ inline int act_sf_atoms(int bm) { return (kTerms * bm + 127) / 128; }
 
 inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   WsLayout L{};
@@ -97,7 +103,7 @@ inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align_up(o + bytes, A); return r; };
   const size_t tk = (size_t)T * k;
-  const size_t sfa = (size_t)sf_atoms_per_tile(bm) * kSfAtomBytes;
+  const size_t sfa = (size_t)act_sf_atoms(bm) * kSfAtomBytes;
   L.status = take(256);
   L.route_sync = take(sizeof(uint32_t) * (size_t)(ceil_div(T, 8) + 1));
   L.logits = take(sizeof(float) * (size_t)T * E);
@@ -109,16 +115,15 @@ inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   L.inv_perm = take(sizeof(int32_t) * tk);
   L.tiles = take(sizeof(TileEntry) * (size_t)L.max_tiles);
   L.num_tiles = take(sizeof(int32_t));
-  L.x_hi = take((size_t)L.pad_rows * H);
-  L.x_lo = take((size_t)L.pad_rows * H);
-  L.x_sf_hi = take((size_t)L.max_tiles * L.kg_h * sfa);
-  L.x_sf_lo = take((size_t)L.max_tiles * L.kg_h * sfa);
-  L.h_hi = take((size_t)L.pad_rows * I);
-  L.h_lo = take((size_t)L.pad_rows * I);
-  L.h_sf_hi = take((size_t)L.max_tiles * L.kg_i * sfa);
-  L.h_sf_lo = take((size_t)L.max_tiles * L.kg_i * sfa);
+  L.x_q = take((size_t)L.kg_h * L.pad_rows * kTerms * 64);
+  L.x_sf = take((size_t)L.max_tiles * L.kg_h * sfa);
+  L.h_q = take((size_t)L.kg_i * L.pad_rows * kTerms * 64);
+  L.h_sf = take((size_t)L.max_tiles * L.kg_i * sfa);
   L.slots = take(sizeof(float) * tk * H);
   L.combine_cnt = take(sizeof(int32_t) * (size_t)T * L.mt_h);
+  L.unit_cnt = take(sizeof(int32_t) * (size_t)L.max_tiles * (L.mt_h > L.mt_i ? L.mt_h : L.mt_i));
+  L.zero_bytes = o - L.combine_cnt;
+  L.partials = take(sizeof(float) * (size_t)2 * kMaxCtas * 2 * bm * kMTile);
   L.total = o;
   return L;
 }
@@ -130,10 +135,12 @@ __host__ __device__ inline P* ws_ptr(void* ws, size_t off) {
 
 // ----------------------------------------------------------------- MXFP4 weights
 // Prepared weight layout of one matrix family (gate/up or down) for E experts:
-//   codes  [E][R][Kp/2]   R = rows of the family (2I gate+up rows, or H down rows),
+//   codes  [E][G][KG][rows per group][64]  K-group major: for every 128-code K group
+//                         the 64-byte code runs of all rows of a group are adjacent,
+//                         so a 128-row TMA box is one contiguous 8 KB read.  G = 2
+//                         for gate/up (gate rows, up rows), 1 for down; KG = Kp / 128,
 //                         Kp = K padded to a multiple of 128 (pad codes are zero)
-//   scales [E][G][MT][KG][512]  G = 2 for gate/up (gate rows, up rows), 1 for down;
-//                         MT = ceil(rows per group / 128), KG = Kp / 128; each 512-byte
+//   scales [E][G][MT][KG][512]  MT = ceil(rows per group / 128); each 512-byte
 //                         atom holds the E8M0 scales of 128 rows x 4 MX blocks:
 //                         byte (l*16 + c*4 + b) = scale of row 32c + l, block b.
 //   trailer (256 bytes): a status word the preparing kernel sets when it meets
@@ -160,29 +167,46 @@ inline PreparedLayout make_prepared_layout(int E, int R, int K, int groups) {
 }
 
 // ----------------------------------------------------------------- activations
-// Two-term MX encoding of 32 real values v sharing a block: v ~= q1 * 2^p1 + q2 * 2^p2
-// with q1, q2 E4M3 and p1, p2 E8M0 exponents.  p is the smallest exponent that keeps
-// the block maximum within the E4M3 range (448); an all-zero block gets p = 0.
 // Exponents are kept in [-126, 127] so 2^p and 2^-p are normal floats and the
 // E8M0 byte p + 127 is never 255 (NaN).
 __device__ __forceinline__ float pow2_int(int e) { return __int_as_float((e + 127) << 23); }
 
-__device__ __forceinline__ int mx_e4m3_exponent(float amax) {
+// E2M1 terms: p is the smallest exponent with amax <= 6 * 2^p (6 = largest E2M1).
+__device__ __forceinline__ int mx_e2m1_exponent(float amax) {
   if (!(amax > 0.f)) return 0;
-  int e = ilogbf(amax) - 8;                  // amax / 2^e in [256, 512)
+  // floor(log2(amax)) from the exponent field (subnormals clamp to the minimum below)
+  int e = (int)((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 2;  // amax / 2^e in [4, 8)
   if (e < -126) e = -126;
   if (e > 127) e = 127;
-  if (amax > 448.f * pow2_int(e) && e < 127) e += 1;  // keep within E4M3's finite range
+  if (amax > 6.f * pow2_int(e) && e < 127) e += 1;
   return e;
 }
 
-__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+// Nearest E2M1 codes of (lo, hi), ties to even, saturating at +-6, packed as one
+// byte: lo in bits 0-3, hi in bits 4-7 (the hardware conversion instruction puts its
+// first source operand in the upper half).
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+  uint16_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tmov.b16 %0, {t, 0};\n\t}"
+      : "=h"(r)
+      : "f"(lo), "f"(hi));
+  return static_cast<uint32_t>(r) & 0xFFu;
 }
 
-__device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
-  __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(q), __NV_E4M3);
-  return __half2float(__half(hr));
+// Nearest E2M1 code of v as a 4-bit code.
+__device__ __forceinline__ uint32_t f32_to_e2m1(float v) { return f32x2_to_e2m1x2(v, 0.f) & 0xFu; }
+
+// Value of a 4-bit E2M1 code: sign bit 3, exponent bits 2-1 (bias 1), mantissa bit 0.
+__device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
+  const uint32_t m = code & 7u;
+  const float mag = (m < 2u) ? 0.5f * (float)m : (1.f + 0.5f * (float)(m & 1u)) * (float)(1u << ((m >> 1) - 1u));
+  return (code & 8u) ? -mag : mag;
+}
+
+// Byte offset of the code byte holding values (k, k+1) (k even) of term t of row r
+// of tile `tile` in an encoded activation buffer [KG][max_tiles][kTerms][bm][64].
+__host__ __device__ inline size_t act_offset(int tile, int t, int r, int k, int max_tiles, int bm) {
+  return ((((size_t)(k >> 7) * max_tiles + tile) * kTerms + t) * bm + r) * 64 + ((k & 127) >> 1);
 }
 
 // Scale atom byte offset of (row r within a tile, MX block b within a K group).

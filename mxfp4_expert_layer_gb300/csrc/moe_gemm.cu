@@ -9,13 +9,22 @@
 // follows tokens per expert").
 //
 // Design (swap-AB): the MMA's M dimension is 128 weight rows (output features), N
-// is the tile's token rows (16/64/128), K runs over the contraction in groups of
-// 128.  A = MXFP4 weights (E2M1, loaded by TMA in the 16-byte-aligned unpacked
-// shared-memory form), B = activations as two E4M3 terms, each with its own E8M0
-// block scales; both scale sets are copied into tensor memory with tcgen05.cp and
-// consumed natively by the block-scaled MMA (kind::mxf8f6f4, one scale per 32 K).
-// Accumulators live in tensor memory.  Warp roles: warp 0 issues TMA loads into a
-// ring of shared-memory stages, warp 1 issues MMAs, warps 2-5 run the epilogue.
+// covers the tile's token rows, K runs over the contraction in groups of 128 (one
+// pipeline stage).  A = the MXFP4 weights exactly as stored (packed E2M1 codes,
+// TMA-loaded with the 64-byte swizzle); B = the activations, encoded as four
+// packed E2M1 terms with their own E8M0 block scales.  kind::mxf4 consumes both
+// codes and both scale sets natively (K = 64 per instruction, scales copied into
+// tensor memory with tcgen05.cp).  For 16-row decode tiles the four terms are
+// concatenated along N (one N = 64 MMA per K step and weight tile; the epilogue
+// adds the four column groups); larger tiles run one MMA per term into the same
+// accumulator.
+//
+// Persistent CTAs (one per SM) split the iterations (work unit x K group) of all
+// units evenly; a unit cut by a CTA boundary writes fp32 partials and an integer
+// arrival counter elects the CTA that sums them, in fixed order.  Warp roles: warp
+// 0 issues TMA loads into a ring of shared-memory stages, warp 1 issues MMAs into
+// one of two tensor-memory accumulators, warps 2-5 run the epilogue of one unit
+// while the MMAs of the next proceed.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
 #include "sm100_ptx.cuh"
@@ -28,64 +37,124 @@ namespace {
 
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitLimit = 1000000000ull;  // ns a bounded mbarrier wait may take (1 s)
+constexpr int kATileBytes = kMTile * 64;         // one 128-row x 128-code weight tile, packed
 
 template <int BM, bool GATEUP>
 struct GemmCfg {
-  static constexpr int kA = GATEUP ? 2 : 1;                 // weight tiles per stage
-  static constexpr int kNb = BM > 128 ? 2 : 1;              // scale atoms per activation term
-  static constexpr int kATileBytes = kMTile * 128;          // smem bytes of one A tile
-  static constexpr int kBTileBytes = BM * 128;              // smem bytes of one B tile
-  static constexpr int kSfBytes = (kA + 2 * kNb) * kSfAtomBytes;
-  static constexpr int kStageRaw = kA * kATileBytes + 2 * kBTileBytes + kSfBytes;
+  static constexpr int kA = GATEUP ? 2 : 1;                  // weight tiles per stage (gate, up)
+  static constexpr bool kConcat = kTerms * BM <= 64;         // all terms in one MMA along N
+  static constexpr int kN = kConcat ? kTerms * BM : BM;      // MMA N
+  static constexpr int kAccN = kN;                           // accumulator columns per weight tile
+  static constexpr int kAccCols = kA * kAccN;
+  static constexpr int kVals = kA * BM;                      // values per row after summing terms
+  static constexpr int kBRows = kTerms * BM;                 // B tile rows (terms x token rows)
+  static constexpr int kBBytes = kBRows * 64;
+  static constexpr int kBBoxRows = kBRows < 256 ? kBRows : 256;
+  static constexpr int kNbAtoms = (kBRows + 127) / 128;      // B scale atoms per stage
+  static constexpr int kSfBytes = (kA + kNbAtoms) * kSfAtomBytes;
+  static constexpr int kStageRaw = kA * kATileBytes + kBBytes + kSfBytes;
   static constexpr int kStageBytes = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kSmemBudget = 220 * 1024;
+  static constexpr int kEpiBytes = 16 * kMTile * 4 + 2 * 128 * 4;  // h transpose chunk + row metadata
+  static constexpr int kSmemBudget = 216 * 1024 - kEpiBytes;
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 1024 /*barriers*/;
-  // expected transaction bytes per stage: the FP4 tiles count their packed global bytes
-  static constexpr uint32_t kTxBytes = kA * kMTile * 64 + 2 * BM * 128 + kSfBytes;
-  // tensor memory columns: accumulators first, then one scale ring slot per stage
-  static constexpr int kAccCols = kA * BM;
-  static constexpr int kSfColsPerStage = 4 * kA + 2 * 4 * kNb;
-  static constexpr int kTmemNeed = kAccCols + kStages * kSfColsPerStage;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kBarBytes = 2048;
+  static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
+  static constexpr uint32_t kTxBytes = kA * kATileBytes + kBBytes + kSfBytes;
+  static constexpr int kSfColsPerStage = 4 * (kA + kNbAtoms);
+  static constexpr int kSfCols = kStages * kSfColsPerStage;
+  static constexpr int kNumAcc = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
+  static constexpr int kTmemNeed = kNumAcc * kAccCols + kSfCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
+  // the epilogue reads the whole accumulator into registers before releasing it
+  static constexpr bool kLoadAll = kAccCols <= 128;
   static_assert(kTmemNeed <= 512, "tensor memory budget");
   static_assert(kStages >= 2, "pipeline depth");
+  static_assert(kBRows % kBBoxRows == 0, "B tile = whole TMA boxes");
 };
 
-struct WorkUnit {
-  int tile, mt;
-};
-
-// Raster: units are grouped in blocks of `group` tiles; within a block, the M tile
-// varies slowest, so co-resident CTAs share weight tiles (same expert) and
+// Raster: units are grouped in blocks of `group` tiles; within a block the M tile
+// varies slowest, so neighbouring units share weight tiles (same expert) and
 // activation tiles through L2.
-__device__ __forceinline__ bool map_unit(int u, int num_tiles, int mt_count, int group, WorkUnit& w) {
-  if (u >= num_tiles * mt_count) return false;
+__device__ __forceinline__ void map_unit(int u, int num_tiles, int mt_count, int group, int& tile, int& mt) {
   const int g = u / (group * mt_count);
   const int first = g * group;
   const int gsize = min(group, num_tiles - first);
   const int within = u - first * mt_count;
-  w.mt = within / gsize;
-  w.tile = first + within % gsize;
-  return true;
+  mt = within / gsize;
+  tile = first + within % gsize;
 }
+
+// Even split of the W = units x K-groups iterations over G persistent CTAs: CTA c
+// owns iterations [begin(c), begin(c + 1)), never empty since G <= W.  A unit cut
+// by a CTA boundary is finished by whichever of its CTAs arrives last.
+struct SplitK {
+  long long W;
+  int G;
+  __device__ __forceinline__ int begin(int c) const { return (int)((W * c) / G); }
+  __device__ __forceinline__ int cta_of(int it) const {
+    int c = (int)(((long long)it * G) / W);
+    if (c > G - 1) c = G - 1;
+    while (c + 1 < G && begin(c + 1) <= it) ++c;
+    while (c > 0 && begin(c) > it) --c;
+    return c;
+  }
+  // partial-sum slot of CTA c for unit u: 2c for its first unit, 2c + 1 for its last
+  __device__ __forceinline__ int slot(int c, int u, int kg) const { return (u == begin(c) / kg) ? 2 * c : 2 * c + 1; }
+};
+
+// Work schedule of one CTA: D whole units dealt round-robin (unit c + w*G), then an
+// even split of the remaining units' K iterations (stream-K).  D leaves between G
+// and 2G units for the split so every CTA gets work and none gets more than one
+// unit's worth extra.
+struct Schedule {
+  int KG, G, D, u0;   // u0 = D * G: first unit of the split part
+  SplitK sk;          // over the split part's iterations
+  int c, b, e;        // this CTA and its split range [b, e)
+  int nseg;           // segments of this CTA: D whole units + split segments
+  __device__ void init(int U, int kg, int grid, int cta) {
+    KG = kg;
+    G = grid;
+    D = (U >= 2 * grid) ? U / grid - 1 : 0;
+    u0 = D * grid;
+    const long long Wr = (long long)(U - u0) * kg;
+    sk.W = Wr;
+    sk.G = (int)(Wr < (long long)grid ? Wr : (long long)grid);
+    c = cta;
+    if (cta < sk.G) {
+      b = sk.begin(cta);
+      e = sk.begin(cta + 1);
+      nseg = D + (e - 1) / kg - b / kg + 1;
+    } else {
+      b = e = 0;
+      nseg = D;
+    }
+  }
+  // segment i: unit, K-group range, whether the unit is whole here
+  __device__ void seg(int i, int& u, int& kk0, int& kk1, bool& whole) const {
+    if (i < D) {
+      u = c + i * G;
+      kk0 = 0;
+      kk1 = KG;
+      whole = true;
+      return;
+    }
+    const int ur = b / KG + (i - D);  // unit within the split part
+    const int s0 = max(b, ur * KG), s1 = min(e, (ur + 1) * KG);
+    u = u0 + ur;
+    kk0 = s0 - ur * KG;
+    kk1 = s1 - ur * KG;
+    whole = (kk0 == 0) && (kk1 == KG);
+  }
+};
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
 
-// Warp-wide two-term E4M3 encoding of one value per lane (the 32 lanes form one
-// MX block).  Returns the codes and the exponents of both terms.
-__device__ __forceinline__ void encode_two_term(float v, uint8_t& q1, uint8_t& q2, int& p1, int& p2) {
-  float a = fabsf(v);
-  a = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
-  p1 = mx_e4m3_exponent(a);
-  q1 = f32_to_e4m3(v * pow2_int(-p1));
-  const float r = v - e4m3_to_f32(q1) * pow2_int(p1);
-  float ar = fabsf(r);
-  ar = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(ar)));
-  p2 = mx_e4m3_exponent(ar);
-  q2 = f32_to_e4m3(r * pow2_int(-p2));
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ float warp_absmax(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
 }
 
 }  // namespace
@@ -97,31 +166,34 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
   uint64_t* empty_bar = full_bar + C::kStages;
-  uint64_t* accum_bar = empty_bar + C::kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
-  int* s_flags = reinterpret_cast<int*>(tmem_slot + 1);  // [0] error, [1..BM] combine finalisers
+  uint64_t* accf_bar = empty_bar + C::kStages;   // [2] accumulator ready
+  uint64_t* acce_bar = accf_bar + 2;             // [2] accumulator drained
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+  int* s_flags = reinterpret_cast<int*>(tmem_slot + 4);  // [0] error, [1] unit finisher, [2..] combine
+  float* s_xpose = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);  // [16][128]
+  int* s_rowa = reinterpret_cast<int*>(s_xpose + 16 * kMTile);   // [128] assignment of each tile row
+  float* s_roww = reinterpret_cast<float*>(s_rowa + 128);         // [128] its top-k weight
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  const int num_tiles = __ldg(p.num_tiles);
-  WorkUnit wu;
-  if (!map_unit(blockIdx.x, num_tiles, p.mt, p.group_tiles, wu)) return;
-  const TileEntry te = p.tiles[wu.tile];
-
+  // prologue that touches nothing the previous kernel writes: barriers, tensor
+  // memory, descriptor prefetch; it overlaps the previous kernel's tail
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(accum_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf_bar[b], 1);
+      mbar_init(&acce_bar[b], 128);
+    }
     s_flags[0] = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tm_w);
-    tma_prefetch_desc(&p.tm_act_hi);
-    tma_prefetch_desc(&p.tm_act_lo);
+    tma_prefetch_desc(&p.tm_act);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -131,194 +203,394 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_launch_dependents();
+  // the routing, the encoded activations and (for down) h come from the previous
+  // kernels: wait for them to complete
+  pdl_wait();
+
+  const int num_tiles = __ldg(p.num_tiles);
+  const int KG = p.kg;
+  const int U = num_tiles * p.mt;
+  const int grid = (long long)U * KG < (long long)gridDim.x ? U * KG : (int)gridDim.x;
+  Schedule sch;
+  sch.init(U, KG, grid > 0 ? grid : 1, blockIdx.x);
+  if (U == 0 || (int)blockIdx.x >= grid) sch.nseg = 0;  // no work: straight to teardown
 
   auto stage_ptr = [&](int s) { return smem + s * C::kStageBytes; };
-  // stage layout: [A tiles][B hi][B lo][SF A x kA][SF B hi x kNb][SF B lo x kNb]
-  auto a_tile = [&](int s, int j) { return stage_ptr(s) + j * C::kATileBytes; };
-  auto b_tile = [&](int s, int term) { return stage_ptr(s) + C::kA * C::kATileBytes + term * C::kBTileBytes; };
-  auto sf_a = [&](int s, int j) {
-    return stage_ptr(s) + C::kA * C::kATileBytes + 2 * C::kBTileBytes + j * kSfAtomBytes;
-  };
-  auto sf_b = [&](int s, int term) {
-    return stage_ptr(s) + C::kA * C::kATileBytes + 2 * C::kBTileBytes + (C::kA + term * C::kNb) * kSfAtomBytes;
-  };
+  // stage layout: [A tiles][B tile (terms x rows)][SF A x kA][SF B x kNbAtoms]
+  auto a_tile = [&](int s, int j) { return stage_ptr(s) + j * kATileBytes; };
+  auto b_tile = [&](int s) { return stage_ptr(s) + C::kA * kATileBytes; };
+  auto sf_a = [&](int s, int j) { return stage_ptr(s) + C::kA * kATileBytes + C::kBBytes + j * kSfAtomBytes; };
+  auto sf_b = [&](int s) { return stage_ptr(s) + C::kA * kATileBytes + C::kBBytes + C::kA * kSfAtomBytes; };
 
-  const int kblocks = p.K / kMxBlock;  // real MX blocks along K (padded blocks are skipped)
-  const int kg = p.kg;
+  const int kblocks = p.K / kMxBlock;  // real MX blocks along K; K steps past them are skipped
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint8_t* wsf_base = p.w_sf + ((size_t)te.expert * p.w_groups * p.mt + wu.mt) * (size_t)kg * kSfAtomBytes;
-      const size_t wsf_group_stride = (size_t)p.mt * kg * kSfAtomBytes;
-      const size_t asf_tile = (size_t)wu.tile * kg * (kSfAtomBytes * C::kNb);
+      const size_t wsf_group_stride = (size_t)p.mt * KG * kSfAtomBytes;
       int g = 0;
-      for (; g < kg; ++g) {
-        const int s = g % C::kStages;
-        const uint32_t ph = (g / C::kStages) & 1;
-        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1, kWaitLimit)) {
-          report_status(p.status, kStatusTimeoutProducer);
-          s_flags[0] = 1;
-          break;
+      bool err = false;
+      for (int si = 0; si < sch.nseg && !err; ++si) {
+        int u, kk0, kk1, tile, mt;
+        bool whole;
+        sch.seg(si, u, kk0, kk1, whole);
+        map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
+        const int expert = p.tiles[tile].expert;
+        const uint8_t* wsf_base = p.w_sf + ((size_t)expert * p.w_groups * p.mt + mt) * (size_t)KG * kSfAtomBytes;
+        for (int kk = kk0; kk < kk1; ++kk, ++g) {
+          const int s = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
+          if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1, kWaitLimit)) {
+            report_status(p.status, kStatusTimeoutProducer);
+            s_flags[0] = 1;
+            err = true;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[s], C::kTxBytes);
+          for (int j = 0; j < C::kA; ++j) {
+            tma_load_4d(a_tile(s, j), &p.tm_w, &full_bar[s], 0, mt * kMTile, kk, expert * p.w_groups + j);
+            bulk_load(sf_a(s, j), wsf_base + j * wsf_group_stride + (size_t)kk * kSfAtomBytes, kSfAtomBytes,
+                      &full_bar[s]);
+          }
+          for (int bx = 0; bx < C::kBRows / C::kBBoxRows; ++bx)
+            tma_load_3d(b_tile(s) + bx * C::kBBoxRows * 64, &p.tm_act, &full_bar[s], 0,
+                        tile * C::kBRows + bx * C::kBBoxRows, kk);
+          bulk_load(sf_b(s), p.act_sf + ((size_t)tile * KG + kk) * (kSfAtomBytes * C::kNbAtoms),
+                    kSfAtomBytes * C::kNbAtoms, &full_bar[s]);
         }
-        mbar_arrive_expect_tx(&full_bar[s], C::kTxBytes);
-        const int kc = g * kKGroup;
-        for (int j = 0; j < C::kA; ++j) {
-          tma_load_4d(a_tile(s, j), &p.tm_w, &full_bar[s], kc, wu.mt * kMTile, j, te.expert);
-          bulk_load(sf_a(s, j), wsf_base + j * wsf_group_stride + (size_t)g * kSfAtomBytes, kSfAtomBytes,
-                    &full_bar[s]);
-        }
-        tma_load_2d(b_tile(s, 0), &p.tm_act_hi, &full_bar[s], kc, te.pad_row);
-        tma_load_2d(b_tile(s, 1), &p.tm_act_lo, &full_bar[s], kc, te.pad_row);
-        bulk_load(sf_b(s, 0), p.act_sf_hi + asf_tile + (size_t)g * kSfAtomBytes * C::kNb, kSfAtomBytes * C::kNb,
-                  &full_bar[s]);
-        bulk_load(sf_b(s, 1), p.act_sf_lo + asf_tile + (size_t)g * kSfAtomBytes * C::kNb, kSfAtomBytes * C::kNb,
-                  &full_bar[s]);
       }
       // on an error, wait (bounded) for the copies already issued to land
-      if (s_flags[0]) {
-        for (int gg = max(0, g - C::kStages); gg < g; ++gg) {
+      if (err) {
+        for (int gg = max(0, g - C::kStages); gg < g; ++gg)
           mbar_wait_bounded(&full_bar[gg % C::kStages], (gg / C::kStages) & 1, kWaitLimit);
-        }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t sf_col0 = C::kAccCols;
-      for (int g = 0; g < kg; ++g) {
-        const int s = g % C::kStages;
-        const uint32_t ph = (g / C::kStages) & 1;
-        if (!mbar_wait_bounded(&full_bar[s], ph, kWaitLimit)) {
+      const uint32_t sf_col0 = C::kNumAcc * C::kAccCols;
+      int g = 0;
+      bool err = false;
+      for (int si = 0; si < sch.nseg && !err; ++si) {
+        int u, kk0, kk1;
+        bool whole;
+        sch.seg(si, u, kk0, kk1, whole);
+        const int b = si % C::kNumAcc;
+        if (!mbar_wait_bounded(&acce_bar[b], ((si / C::kNumAcc) & 1) ^ 1, kWaitLimit)) {
           report_status(p.status, kStatusTimeoutMain);
           s_flags[0] = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t sfc = tmem + sf_col0 + s * C::kSfColsPerStage;
-        // scale atoms -> tensor memory (32 rows x 16 bytes, replicated to 4 lane quarters)
-        for (int j = 0; j < C::kA; ++j) tmem_cp_32x128b_warpx4(sfc + 4 * j, smem_desc(smem_u32(sf_a(s, j)), 0, 128, 0));
-        for (int term = 0; term < 2; ++term)
-          for (int q = 0; q < C::kNb; ++q)
-            tmem_cp_32x128b_warpx4(sfc + 4 * C::kA + term * 4 * C::kNb + 4 * q,
-                                   smem_desc(smem_u32(sf_b(s, term)) + q * kSfAtomBytes, 0, 128, 0));
-        for (int kb = 0; kb < 4; ++kb) {
-          if (g * 4 + kb >= kblocks) break;
-          const uint32_t idesc = idesc_mx(kMTile, BM, kFmtE2M1, kFmtE4M3, kb, kb);
-          for (int term = 0; term < 2; ++term) {
-            const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(b_tile(s, term)) + 32 * kb);
-            const uint32_t sfb = sfc + 4 * C::kA + term * 4 * C::kNb;
-            const uint32_t acc = (g | kb | term) != 0;
-            for (int j = 0; j < C::kA; ++j) {
-              const uint64_t adesc = smem_desc_kmajor_sw128(smem_u32(a_tile(s, j)) + 32 * kb);
-              mma_mxf8f6f4(tmem + j * BM, adesc, bdesc, idesc, sfc + 4 * j, sfb, acc);
-            }
+        const uint32_t acc_base = tmem + b * C::kAccCols;
+        bool seg_first = true;
+        for (int kk = kk0; kk < kk1; ++kk, ++g) {
+          const int s = g % C::kStages;
+          const uint32_t ph = (g / C::kStages) & 1;
+          if (!mbar_wait_bounded(&full_bar[s], ph, kWaitLimit)) {
+            report_status(p.status, kStatusTimeoutMain);
+            s_flags[0] = 1;
+            err = true;
+            break;
           }
+          tc_fence_after();
+          const uint32_t sfc = tmem + sf_col0 + s * C::kSfColsPerStage;
+          const uint32_t sfb0 = sfc + 4 * C::kA;
+          // scale atoms -> tensor memory (32 rows x 16 bytes, replicated to 4 lane quarters)
+          for (int j = 0; j < C::kA; ++j)
+            tmem_cp_32x128b_warpx4(sfc + 4 * j, smem_desc(smem_u32(sf_a(s, j)), 0, 128, 0));
+          for (int q = 0; q < C::kNbAtoms; ++q)
+            tmem_cp_32x128b_warpx4(sfb0 + 4 * q, smem_desc(smem_u32(sf_b(s)) + q * kSfAtomBytes, 0, 128, 0));
+          for (int ks = 0; ks < 2; ++ks) {           // two K = 64 steps per 128-value K group
+            if (kk * 4 + 2 * ks >= kblocks) break;   // both MX blocks of this step are padding
+            const uint32_t idesc = idesc_mxf4(kMTile, C::kN, 2 * ks, 2 * ks);
+            if constexpr (C::kConcat) {
+              const uint64_t bdesc = smem_desc_kmajor_sw64(smem_u32(b_tile(s)) + 32 * ks);
+              const uint32_t acc = seg_first ? 0u : 1u;
+              for (int j = 0; j < C::kA; ++j) {
+                const uint64_t adesc = smem_desc_kmajor_sw64(smem_u32(a_tile(s, j)) + 32 * ks);
+                mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * j, sfb0, acc);
+              }
+            } else {
+              for (int t = 0; t < kTerms; ++t) {
+                const uint64_t bdesc = smem_desc_kmajor_sw64(smem_u32(b_tile(s)) + t * BM * 64 + 32 * ks);
+                const uint32_t sfb = sfb0 + (t * BM) / 32;
+                const uint32_t acc = (seg_first && t == 0) ? 0u : 1u;
+                for (int j = 0; j < C::kA; ++j) {
+                  const uint64_t adesc = smem_desc_kmajor_sw64(smem_u32(a_tile(s, j)) + 32 * ks);
+                  mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * j, sfb, acc);
+                }
+              }
+            }
+            seg_first = false;
+          }
+          mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
         }
-        mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+        if (!err) mma_commit(&accf_bar[b]);
       }
-      mma_commit(accum_bar);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                // tensor-memory lane quarter of this warp
     const int m = q * 32 + lane;           // row of the 128-row tile
-    const int feat = wu.mt * kMTile + m;   // output feature
-    const bool ok = mbar_wait_bounded(accum_bar, 0, kWaitLimit);
-    if (!ok) {
-      report_status(p.status, kStatusTimeoutEpi);
-      s_flags[0] = 1;
-    }
-    tc_fence_after();
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const int nrows = te.n_rows;
-    if (ok) {
-      if constexpr (GATEUP) {
-        const bool fvalid = feat < p.I;
-        uint8_t* sfh = p.h_sf_hi + ((size_t)wu.tile * p.kg_out + wu.mt) * (kSfAtomBytes * C::kNb);
-        uint8_t* sfl = p.h_sf_lo + ((size_t)wu.tile * p.kg_out + wu.mt) * (kSfAtomBytes * C::kNb);
-#pragma unroll 1
-        for (int c0 = 0; c0 < BM; c0 += 16) {
-          if (c0 >= nrows) break;
-          uint32_t rg[16], ru[16];
-          tmem_ld_32x32b_x16(lane_base + c0, rg);
-          tmem_ld_32x32b_x16(lane_base + BM + c0, ru);
-          tmem_wait_ld();
+    const int et = threadIdx.x - 64;       // 0..127 within the epilogue warps
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    const int i_pad = (p.I + 63) / 64 * 64;  // h features written (zeros past I)
+    for (int si = 0; si < sch.nseg; ++si) {
+      int u, kk0, kk1, tile, mt;
+      bool whole;
+      sch.seg(si, u, kk0, kk1, whole);
+      const int b = si % C::kNumAcc;
+      map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
+      const TileEntry te = p.tiles[tile];
+      const int nrows = te.n_rows;
+      const int feat = mt * kMTile + m;
+      if constexpr (!GATEUP) {
+        // row metadata of the tile, staged before the accumulator is ready
+        if (et < nrows) {
+          const int a = __ldg(p.perm + te.row_begin + et);
+          s_rowa[et] = a;
+          s_roww[et] = __ldg(p.topk_w + a);
+        }
+      }
+      const bool ok = mbar_wait_bounded(&accf_bar[b], (si / C::kNumAcc) & 1, kWaitLimit);
+      if (!ok) {
+        report_status(p.status, kStatusTimeoutEpi);
+        s_flags[0] = 1;
+        break;
+      }
+      tc_fence_after();
+      epi_bar();  // row metadata visible
+      const uint32_t acc_addr = tmem + lane_off + b * C::kAccCols;
+      const int ur = u - sch.u0;  // unit within the split part (when not whole)
+      float* my_slot = whole ? nullptr : p.partials + (size_t)sch.sk.slot(blockIdx.x, ur, KG) * (C::kVals * kMTile);
+
+      // the math of 16 token columns starting at c0, given g/u (gate/up) or y (down)
+      auto consume = [&](int c0, const float* va, const float* vb) {
+        if constexpr (GATEUP) {
+          // h = silu(g) * u -> shared memory, transposed so that one thread holds the 32
+          // features of one MX block of one token column
+          const bool fvalid = feat < p.I;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 16; ++j) s_xpose[j * kMTile + m] = fvalid ? silu_f(va[j]) * vb[j] : 0.f;
+          epi_bar();
+          const int j = et >> 2, qb = et & 3;  // column, MX block (threads 4j..4j+3 share a column)
+          if (et < 64) {
             const int r = c0 + j;
-            const float g = __uint_as_float(rg[j]);
-            const float u = __uint_as_float(ru[j]);
-            const float h = fvalid ? silu_f(g) * u : 0.f;
-            uint8_t q1, q2;
-            int p1, p2;
-            encode_two_term(h, q1, q2, p1, p2);
-            if (r < nrows) {
-              const size_t row = (size_t)(te.pad_row + r);
-              if (fvalid) {
-                p.h_hi[row * p.I + feat] = q1;
-                p.h_lo[row * p.I + feat] = q2;
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = s_xpose[j * kMTile + qb * 32 + i];
+            const int feat0 = mt * kMTile + qb * 32;
+            uint8_t* sf = p.h_sf + ((size_t)tile * p.kg_out + mt) * (kSfAtomBytes * act_sf_atoms(BM));
+#pragma unroll
+            for (int t = 0; t < kTerms; ++t) {
+              float amax = 0.f;
+#pragma unroll
+              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+              const int pe = mx_e2m1_exponent(amax);
+              const float inv = pow2_int(-pe), sc = pow2_int(pe);
+              uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const uint32_t pair = f32x2_to_e2m1x2(v[2 * i] * inv, v[2 * i + 1] * inv);
+                v[2 * i] -= e2m1_to_f32(pair & 15u) * sc;
+                v[2 * i + 1] -= e2m1_to_f32(pair >> 4) * sc;
+                w[i >> 2] |= pair << (8 * (i & 3));
               }
-              if (lane == 0) {
-                const int off = sf_atom_offset(r, q);
-                sfh[off] = static_cast<uint8_t>(p1 + 127);
-                sfl[off] = static_cast<uint8_t>(p2 + 127);
+              // the 4 MX blocks of a column sit in 4 adjacent lanes: pack their exponents
+              const uint32_t e8 = static_cast<uint32_t>(pe + 127);
+              const uint32_t word = __shfl_sync(0xffffffffu, e8, lane & ~3) | (__shfl_sync(0xffffffffu, e8, (lane & ~3) + 1) << 8) |
+                                    (__shfl_sync(0xffffffffu, e8, (lane & ~3) + 2) << 16) |
+                                    (__shfl_sync(0xffffffffu, e8, (lane & ~3) + 3) << 24);
+              if (r < nrows) {
+                if (feat0 < i_pad)
+                  *reinterpret_cast<uint4*>(p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM)) =
+                      make_uint4(w[0], w[1], w[2], w[3]);
+                if (qb == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(t * BM + r, 0)) = word;
               }
             }
           }
+          epi_bar();  // s_xpose reused by the next chunk
+        } else {
+          (void)vb;
+          if (feat < p.H) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int r = c0 + j;
+              if (r < nrows) p.slots[(size_t)s_rowa[r] * p.H + feat] = s_roww[r] * va[j];
+            }
+          }
+        }
+      };
+
+      // unit finisher election for a split unit (after this CTA's partials are stored)
+      auto elect_finisher = [&]() -> bool {
+        __threadfence();
+        epi_bar();
+        if (et == 0) {
+          const int cf = sch.sk.cta_of(ur * KG), cl = sch.sk.cta_of(ur * KG + KG - 1);
+          int* cnt = p.unit_cnt + u;
+          const int old = atomicAdd(cnt, 1);
+          const int fin = (old == cl - cf) ? 1 : 0;
+          if (fin) *cnt = 0;
+          s_flags[1] = fin;
+        }
+        epi_bar();
+        const bool fin = s_flags[1] != 0;
+        if (fin) __threadfence();
+        return fin;
+      };
+      auto slot_of = [&](int c) {
+        return p.partials + (size_t)sch.sk.slot(c, ur, KG) * (C::kVals * kMTile);
+      };
+
+      bool finished = whole;
+      if constexpr (C::kLoadAll) {
+        // whole accumulator -> registers, release it to the MMA warp, then compute
+        float acc[C::kAccCols];
+#pragma unroll
+        for (int c0 = 0; c0 < C::kAccCols; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld_32x32b_x16(acc_addr + c0, r);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) acc[c0 + j] = __uint_as_float(r[j]);
+        }
+        tmem_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&acce_bar[b]);
+        // values: add the term column groups when the terms share one MMA
+        float vals[C::kVals];
+#pragma unroll
+        for (int j = 0; j < C::kA; ++j)
+#pragma unroll
+          for (int c = 0; c < BM; ++c) {
+            float v = acc[j * C::kAccN + c];
+            if constexpr (C::kConcat) {
+#pragma unroll
+              for (int t = 1; t < kTerms; ++t) v += acc[j * C::kAccN + t * BM + c];
+            }
+            vals[j * BM + c] = v;
+          }
+        if (!whole) {
+#pragma unroll
+          for (int j = 0; j < C::kVals; ++j) my_slot[j * kMTile + m] = vals[j];
+          finished = elect_finisher();
+          if (finished) {
+            const int cf = sch.sk.cta_of(ur * KG), cl = sch.sk.cta_of(ur * KG + KG - 1);
+#pragma unroll
+            for (int j = 0; j < C::kVals; ++j) vals[j] = 0.f;
+            for (int c = cf; c <= cl; ++c) {
+              const float* sl = slot_of(c);
+#pragma unroll
+              for (int j = 0; j < C::kVals; ++j) vals[j] += __ldcg(sl + j * kMTile + m);
+            }
+          }
+        }
+        if (finished) {
+#pragma unroll
+          for (int c0 = 0; c0 < BM; c0 += 16)
+            if (c0 < nrows) consume(c0, vals + c0, GATEUP ? vals + BM + c0 : nullptr);
         }
       } else {
-        const bool fvalid = feat < p.H;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BM; c0 += 16) {
-          if (c0 >= nrows) break;
-          uint32_t rd[16];
-          tmem_ld_32x32b_x16(lane_base + c0, rd);
-          tmem_wait_ld();
+        // accumulator too large for registers (per-term MMAs): 16 columns at a time
+        if (whole) {
+          for (int c0 = 0; c0 < BM; c0 += 16) {
+            if (c0 >= nrows) break;
+            uint32_t rg[16], ru[16];
+            float va[16], vb[16];
+            tmem_ld_32x32b_x16(acc_addr + c0, rg);
+            if (C::kA > 1) tmem_ld_32x32b_x16(acc_addr + C::kAccN + c0, ru);
+            tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int r = c0 + j;
-            if (r < nrows && fvalid) {
-              const int a = __ldg(p.perm + te.row_begin + r);
-              const float wgt = __ldg(p.topk_w + a);
-              p.slots[(size_t)a * p.H + feat] = wgt * __uint_as_float(rd[j]);
+            for (int j = 0; j < 16; ++j) {
+              va[j] = __uint_as_float(rg[j]);
+              vb[j] = C::kA > 1 ? __uint_as_float(ru[j]) : 0.f;
+            }
+            consume(c0, va, vb);
+          }
+          tc_fence_before();
+          mbar_arrive(&acce_bar[b]);
+        } else {
+          for (int j0 = 0; j0 < C::kA; ++j0)
+            for (int c0 = 0; c0 < BM; c0 += 16) {
+              uint32_t r[16];
+              tmem_ld_32x32b_x16(acc_addr + j0 * C::kAccN + c0, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) my_slot[(j0 * BM + c0 + j) * kMTile + m] = __uint_as_float(r[j]);
+            }
+          tc_fence_before();
+          mbar_arrive(&acce_bar[b]);
+          finished = elect_finisher();
+          if (finished) {
+            const int cf = sch.sk.cta_of(ur * KG), cl = sch.sk.cta_of(ur * KG + KG - 1);
+            for (int c0 = 0; c0 < BM; c0 += 16) {
+              if (c0 >= nrows) break;
+              float va[16], vb[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) va[j] = vb[j] = 0.f;
+              for (int c = cf; c <= cl; ++c) {
+                const float* sl = slot_of(c);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                  va[j] += __ldcg(sl + (c0 + j) * kMTile + m);
+                  if (C::kA > 1) vb[j] += __ldcg(sl + (BM + c0 + j) * kMTile + m);
+                }
+              }
+              consume(c0, va, vb);
             }
           }
         }
       }
-    }
-    if constexpr (!GATEUP) {
-      // deterministic combine: the last CTA to finish a (token, output tile) sums the
-      // token's k weighted slots in ascending j and writes the bf16 output
-      __threadfence();
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      const int et = threadIdx.x - 64;  // 0..127
-      if (et < BM) {
-        int fin = 0;
-        if (et < nrows && ok) {
-          const int a = __ldg(p.perm + te.row_begin + et);
-          const int t = a / p.k;
-          int* cnt = p.combine_cnt + (size_t)t * p.mt + wu.mt;
-          const int old = atomicAdd(cnt, 1);
-          if (old == p.k - 1) {
-            fin = 1;
-            *cnt = 0;  // ready for the next call
+
+      if constexpr (!GATEUP) {
+        // deterministic combine: the last CTA to finish a (token, output tile) sums the
+        // token's k weighted slots in ascending j and writes the bf16 output
+        if (finished) {
+          __threadfence();
+          epi_bar();
+          if (et < BM) {
+            int fin = 0;
+            if (et < nrows) {
+              const int t = s_rowa[et] / p.k;
+              int* cnt = p.combine_cnt + (size_t)t * p.mt + mt;
+              const int old = atomicAdd(cnt, 1);
+              if (old == p.k - 1) {
+                fin = 1;
+                *cnt = 0;  // ready for the next call
+              }
+            }
+            s_flags[2 + et] = fin;
+          }
+          epi_bar();
+          __threadfence();
+          if (feat < p.H) {
+            // 8 rows at a time so their slot loads are in flight together
+            for (int r0 = 0; r0 < nrows; r0 += 8) {
+              int tt[8];
+              bool f[8];
+              float acc[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int r = r0 + i;
+                f[i] = (r < nrows) && s_flags[2 + r];
+                tt[i] = f[i] ? s_rowa[r] / p.k : 0;
+                acc[i] = 0.f;
+              }
+              for (int j = 0; j < p.k; ++j) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  if (f[i]) acc[i] += __ldcg(p.slots + ((size_t)tt[i] * p.k + j) * p.H + feat);
+              }
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                if (f[i]) p.out[(size_t)tt[i] * p.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i]));
+            }
           }
         }
-        s_flags[1 + et] = fin;
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      __threadfence();
-      if (ok && feat < p.H) {
-        for (int r = 0; r < nrows; ++r) {
-          if (!s_flags[1 + r]) continue;
-          const int a = __ldg(p.perm + te.row_begin + r);
-          const int t = a / p.k;
-          float acc = 0.f;
-          for (int j = 0; j < p.k; ++j) acc += __ldcg(p.slots + ((size_t)t * p.k + j) * p.H + feat);
-          p.out[(size_t)t * p.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(acc));
-        }
-      }
+      epi_bar();  // flags and row metadata are reused by the next segment
     }
   }
   tc_fence_before();
@@ -341,9 +613,7 @@ static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  const int units = p.max_tiles * p.mt;
-  kern<<<units, kGemmThreads, C::kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(p.grid), dim3(kGemmThreads), C::kSmemBytes, stream, p);
 }
 
 template <bool GATEUP>

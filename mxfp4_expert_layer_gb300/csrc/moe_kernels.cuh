@@ -7,6 +7,25 @@
 
 namespace moe {
 
+// Launches `kern` with programmatic stream serialization: it may begin while the
+// previous kernel on the stream finishes; the kernel itself waits (pdl_wait) before
+// it touches memory that kernel produced.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 struct RouteParams {
   const uint16_t* x;        // bf16 [T, H]
   const uint16_t* w_router; // bf16 [E, H]
@@ -37,8 +56,8 @@ struct QuantXParams {
   const TileEntry* tiles;
   const int32_t* num_tiles;
   int T, H, k, bm, max_tiles, kg;
-  uint8_t *q_hi, *q_lo;    // [pad_rows, H]
-  uint8_t *sf_hi, *sf_lo;  // [max_tiles][kg][512 * atoms]
+  uint8_t* q;              // [kg][max_tiles][kTerms][bm][64]: four E2M1 terms per row
+  uint8_t* sf;             // [max_tiles][kg][512 * act_sf_atoms(bm)]
   int32_t* zero_buf;       // combine counters to clear (or null)
   int zero_count;
 };
@@ -46,12 +65,10 @@ cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t stream);
 
 struct GemmParams {
   // operand tensor maps (TMA)
-  CUtensorMap tm_w;        // weights: 4-bit codes [E][groups][rows][Kp] (16U4_ALIGN16B)
-  CUtensorMap tm_act_hi;   // activations e4m3 [pad_rows][K]
-  CUtensorMap tm_act_lo;
+  CUtensorMap tm_w;        // weights: packed E2M1 [E*groups][KG][rows][64 B]
+  CUtensorMap tm_act;      // activations: packed E2M1 terms [KG][max_tiles*kTerms*bm][64 B]
   const uint8_t* w_sf;     // weight scale atoms [E][groups][mt][kg][512]
-  const uint8_t* act_sf_hi;// activation scale atoms [max_tiles][kg][512 * atoms]
-  const uint8_t* act_sf_lo;
+  const uint8_t* act_sf;   // activation scale atoms [max_tiles][kg][512 * act_sf_atoms]
   const TileEntry* tiles;
   const int32_t* num_tiles;
   const int32_t* perm;
@@ -62,14 +79,18 @@ struct GemmParams {
   int rows_out;            // output features (I for gate/up, H for down)
   int w_groups;            // 2 (gate, up) or 1 (down)
   int group_tiles;         // tiles per raster group
-  // gate/up epilogue outputs (two-term e4m3 h)
-  uint8_t *h_hi, *h_lo, *h_sf_hi, *h_sf_lo;
+  // gate/up epilogue outputs (four-term E2M1 h)
+  uint8_t *h_q, *h_sf;
   int kg_out;              // K groups of h along I
   // down epilogue
   const float* topk_w;
   float* slots;            // f32 [T*k, H]
   int32_t* combine_cnt;    // [T, mt]
   uint16_t* out;           // bf16 [T, H]
+  // split-K across persistent CTAs
+  int grid;                // persistent CTAs (<= kMaxCtas)
+  float* partials;         // [2 * grid][kA * bm * 128] partial accumulators
+  int32_t* unit_cnt;       // [max_tiles * mt] arrivals per work unit
   uint32_t* status;
 };
 cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream);
@@ -90,7 +111,7 @@ struct HiddenDequantParams {
   const TileEntry* tiles;
   const int32_t* num_tiles;
   int I, bm, max_tiles, kg;
-  const uint8_t *h_hi, *h_lo, *sf_hi, *sf_lo;
+  const uint8_t *h_q, *sf;
   float* out;              // [T*k, I]
 };
 cudaError_t launch_hidden_dequant(const HiddenDequantParams& p, cudaStream_t stream);

@@ -14,8 +14,11 @@
 // warp in a fixed order, so the outputs are bit-reproducible run to run.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
+#include "sm100_ptx.cuh"
 
 namespace moe {
+
+using namespace ptx;
 
 namespace {
 
@@ -200,6 +203,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   extern __shared__ __align__(16) uint8_t route_smem[];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the previous kernel on the stream may still read this call's outputs
+  pdl_wait();
+  pdl_launch_dependents();
   const int g = blockIdx.x;
   const int t0 = g * kTokensPerGroup;
   const int nt = min(kTokensPerGroup, p.T - t0);
@@ -207,9 +213,21 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     // stage the group's activations in shared memory (16-byte vectors)
     uint4* xs = reinterpret_cast<uint4*>(route_smem);
     const int vec_per_row = p.H / 8;
-    for (int i = tid; i < nt * vec_per_row; i += kRouteThreads) {
-      const int r = i / vec_per_row, c = i % vec_per_row;
-      xs[i] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(t0 + r) * p.H) + c);
+    // rows of one group are contiguous in x: issue four loads per thread at a time
+    const uint4* xg = reinterpret_cast<const uint4*>(p.x + (size_t)t0 * p.H);
+    const int nx = nt * vec_per_row;
+    for (int i0 = tid; i0 < nx; i0 += 4 * kRouteThreads) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kRouteThreads;
+        v[u] = i < nx ? __ldg(xg + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u * kRouteThreads;
+        if (i < nx) xs[i] = v[u];
+      }
     }
     __syncthreads();
     const int e_begin = blockIdx.y * p.experts_per_block;
@@ -219,24 +237,36 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
 #pragma unroll
       for (int r = 0; r < kTokensPerGroup; ++r) acc[r] = 0.f;
       const uint4* wr = reinterpret_cast<const uint4*>(p.w_router + (size_t)e * p.H);
-      for (int c = lane; c < vec_per_row; c += 32) {
-        const uint4 wv = __ldg(wr + c);
-        const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
-        const float w4 = bf16_lo(wv.z), w5 = bf16_hi(wv.z), w6 = bf16_lo(wv.w), w7 = bf16_hi(wv.w);
+      // four router-weight loads in flight per lane, then their FMAs in a fixed order
+      for (int c0 = lane; c0 < vec_per_row; c0 += 128) {
+        uint4 wv4[4];
 #pragma unroll
-        for (int r = 0; r < kTokensPerGroup; ++r) {
-          if (r < nt) {
-            const uint4 xv = xs[r * vec_per_row + c];
-            float a = acc[r];
-            a = fmaf(bf16_lo(xv.x), w0, a);
-            a = fmaf(bf16_hi(xv.x), w1, a);
-            a = fmaf(bf16_lo(xv.y), w2, a);
-            a = fmaf(bf16_hi(xv.y), w3, a);
-            a = fmaf(bf16_lo(xv.z), w4, a);
-            a = fmaf(bf16_hi(xv.z), w5, a);
-            a = fmaf(bf16_lo(xv.w), w6, a);
-            a = fmaf(bf16_hi(xv.w), w7, a);
-            acc[r] = a;
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 32 * u;
+          wv4[u] = c < vec_per_row ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = c0 + 32 * u;
+          if (c >= vec_per_row) break;
+          const uint4 wv = wv4[u];
+          const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
+          const float w4 = bf16_lo(wv.z), w5 = bf16_hi(wv.z), w6 = bf16_lo(wv.w), w7 = bf16_hi(wv.w);
+#pragma unroll
+          for (int r = 0; r < kTokensPerGroup; ++r) {
+            if (r < nt) {
+              const uint4 xv = xs[r * vec_per_row + c];
+              float a = acc[r];
+              a = fmaf(bf16_lo(xv.x), w0, a);
+              a = fmaf(bf16_hi(xv.x), w1, a);
+              a = fmaf(bf16_lo(xv.y), w2, a);
+              a = fmaf(bf16_hi(xv.y), w3, a);
+              a = fmaf(bf16_lo(xv.z), w4, a);
+              a = fmaf(bf16_hi(xv.z), w5, a);
+              a = fmaf(bf16_lo(xv.w), w6, a);
+              a = fmaf(bf16_hi(xv.w), w7, a);
+              acc[r] = a;
+            }
           }
         }
       }
@@ -306,8 +336,7 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured_smem[dev] = (int)smem;
   }
-  route_kernel<<<grid, kRouteThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(route_kernel, grid, dim3(kRouteThreads), smem, stream, p);
 }
 
 cudaError_t launch_tile_table(const int32_t* idx, int Tk, int E, int bm, int32_t* counts, int32_t* offsets,

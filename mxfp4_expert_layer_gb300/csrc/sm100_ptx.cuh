@@ -82,6 +82,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// ------------------------------------------------------------------ dependent launch
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of the stream still runs;
+// pdl_wait() blocks until that kernel has completed and its writes are visible, and
+// pdl_launch_dependents() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ------------------------------------------------------------------ fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -207,6 +215,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes
   return d;
 }
 
+// K-major operand tile whose rows are 64 bytes (128 packed FP4 values), stored with
+// the 64-byte swizzle (eight-row groups of 512 bytes).  Base 512-byte aligned; a K
+// offset inside the 64-byte row is added to the start address.
+__device__ __forceinline__ uint64_t smem_desc_kmajor_sw64(uint32_t saddr) {
+  return smem_desc(saddr, 16, 512, 4);
+}
+
 // K-major operand tile whose rows are 128 bytes, stored with the 128-byte swizzle
 // (eight-row groups of 1024 bytes).  The tile base must be 1024-byte aligned; a
 // K offset inside the 128-byte row is added to the start address.
@@ -234,6 +249,15 @@ __host__ __device__ constexpr uint32_t idesc_mx(uint32_t M, uint32_t N, uint32_t
 constexpr uint32_t kFmtE4M3 = 0;
 constexpr uint32_t kFmtE2M1 = 5;
 
+// Instruction descriptor of kind::mxf4 (E2M1 x E2M1, K = 64 per instruction, two
+// E8M0 scales per row: scale_vec::2X).  Same fields as above; the E2M1 format code
+// of this kind is 1.  Scale-factor id 0 reads bytes 0-1 of the scale word, id 2
+// reads bytes 2-3.
+__host__ __device__ constexpr uint32_t idesc_mxf4(uint32_t M, uint32_t N, uint32_t a_sf_id, uint32_t b_sf_id) {
+  return ((b_sf_id & 3u) << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
+         ((a_sf_id & 3u) << 29);
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
@@ -252,6 +276,19 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t adesc, ui
       "{\n\t.reg .pred P;\n\t"
       "setp.ne.b32 P, %6, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], P;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// D (+)= (A * scales) x (B * scales)^T over K = 64 with packed E2M1 operands, one
+// E8M0 scale per row and 32 K values (two per instruction), scales read from TMEM.
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "setp.ne.b32 P, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], P;\n\t}" ::"r"(
           d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");

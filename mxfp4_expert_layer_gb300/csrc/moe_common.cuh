@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "moe_mxfp4.h"
@@ -195,6 +196,15 @@ __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
 
 // Nearest E2M1 code of v as a 4-bit code.
 __device__ __forceinline__ uint32_t f32_to_e2m1(float v) { return f32x2_to_e2m1x2(v, 0.f) & 0xFu; }
+
+// Values of the two E2M1 codes of one byte (low nibble -> .x), through the hardware
+// E2M1 -> f16 conversion (exact: every E2M1 value is an f16).
+__device__ __forceinline__ float2 e2m1x2_to_f32x2(uint32_t byte) {
+  uint32_t h2;
+  const uint16_t b16 = static_cast<uint16_t>(byte & 0xFFu);
+  asm("{\n\t.reg .b8 t, z;\n\tmov.b16 {t, z}, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}" : "=r"(h2) : "h"(b16));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h2));
+}
 
 // Value of a 4-bit E2M1 code: sign bit 3, exponent bits 2-1 (bias 1), mantissa bit 0.
 __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {

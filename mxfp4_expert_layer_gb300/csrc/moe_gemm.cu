@@ -149,13 +149,12 @@ struct Schedule {
   }
 };
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.f + expf(-g)); }
+// silu(g) = g / (1 + e^-g) with the fast exponential and division (|error| well below
+// the E2M1 encoding error that follows)
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ float warp_absmax(float v) {
-  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
-}
 
 }  // namespace
 
@@ -375,40 +374,50 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
 #pragma unroll
           for (int j = 0; j < 16; ++j) s_xpose[j * kMTile + m] = fvalid ? silu_f(va[j]) * vb[j] : 0.f;
           epi_bar();
-          const int j = et >> 2, qb = et & 3;  // column, MX block (threads 4j..4j+3 share a column)
-          if (et < 64) {
-            const int r = c0 + j;
-            float v[32];
+          // 16 columns x 4 MX blocks, two threads per block (16 values each): threads
+          // 8j..8j+7 hold column j, the pair (2qb, 2qb+1) block qb
+          const int j = et >> 3, qb = (et >> 1) & 3, hf = et & 1;
+          const int r = c0 + j;
+          float vv[16];
+          const float4* src = reinterpret_cast<const float4*>(s_xpose + j * kMTile + qb * 32 + hf * 16);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = s_xpose[j * kMTile + qb * 32 + i];
-            const int feat0 = mt * kMTile + qb * 32;
-            uint8_t* sf = p.h_sf + ((size_t)tile * p.kg_out + mt) * (kSfAtomBytes * act_sf_atoms(BM));
+          for (int i = 0; i < 4; ++i) {
+            const float4 f4 = src[i];
+            vv[4 * i] = f4.x;
+            vv[4 * i + 1] = f4.y;
+            vv[4 * i + 2] = f4.z;
+            vv[4 * i + 3] = f4.w;
+          }
+          const int feat0 = mt * kMTile + qb * 32 + hf * 16;
+          uint8_t* sf = p.h_sf + ((size_t)tile * p.kg_out + mt) * (kSfAtomBytes * act_sf_atoms(BM));
 #pragma unroll
-            for (int t = 0; t < kTerms; ++t) {
-              float amax = 0.f;
+          for (int t = 0; t < kTerms; ++t) {
+            float amax = 0.f;
 #pragma unroll
-              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-              const int pe = mx_e2m1_exponent(amax);
-              const float inv = pow2_int(-pe), sc = pow2_int(pe);
-              uint32_t w[4] = {0, 0, 0, 0};
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(vv[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            const int pe = mx_e2m1_exponent(amax);
+            const float inv = pow2_int(-pe), sc = pow2_int(pe);
+            uint32_t w[2] = {0, 0};
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const uint32_t pair = f32x2_to_e2m1x2(v[2 * i] * inv, v[2 * i + 1] * inv);
-                v[2 * i] -= e2m1_to_f32(pair & 15u) * sc;
-                v[2 * i + 1] -= e2m1_to_f32(pair >> 4) * sc;
-                w[i >> 2] |= pair << (8 * (i & 3));
-              }
-              // the 4 MX blocks of a column sit in 4 adjacent lanes: pack their exponents
-              const uint32_t e8 = static_cast<uint32_t>(pe + 127);
-              const uint32_t word = __shfl_sync(0xffffffffu, e8, lane & ~3) | (__shfl_sync(0xffffffffu, e8, (lane & ~3) + 1) << 8) |
-                                    (__shfl_sync(0xffffffffu, e8, (lane & ~3) + 2) << 16) |
-                                    (__shfl_sync(0xffffffffu, e8, (lane & ~3) + 3) << 24);
-              if (r < nrows) {
-                if (feat0 < i_pad)
-                  *reinterpret_cast<uint4*>(p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM)) =
-                      make_uint4(w[0], w[1], w[2], w[3]);
-                if (qb == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(t * BM + r, 0)) = word;
-              }
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t pair = f32x2_to_e2m1x2(vv[2 * i] * inv, vv[2 * i + 1] * inv);
+              const float2 q = e2m1x2_to_f32x2(pair);
+              vv[2 * i] -= q.x * sc;
+              vv[2 * i + 1] -= q.y * sc;
+              w[i >> 2] |= pair << (8 * (i & 3));
+            }
+            // the 4 MX blocks of a column sit in lanes 8j'..8j'+7 (even lanes): pack exponents
+            const uint32_t e8 = static_cast<uint32_t>(pe + 127);
+            const int base = lane & ~7;
+            const uint32_t word = __shfl_sync(0xffffffffu, e8, base) | (__shfl_sync(0xffffffffu, e8, base + 2) << 8) |
+                                  (__shfl_sync(0xffffffffu, e8, base + 4) << 16) |
+                                  (__shfl_sync(0xffffffffu, e8, base + 6) << 24);
+            if (r < nrows) {
+              if (feat0 < i_pad)
+                *reinterpret_cast<uint2*>(p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM)) =
+                    make_uint2(w[0], w[1]);
+              if ((et & 7) == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(t * BM + r, 0)) = word;
             }
           }
           epi_bar();  // s_xpose reused by the next chunk
@@ -480,10 +489,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             const int cf = sch.sk.cta_of(ur * KG), cl = sch.sk.cta_of(ur * KG + KG - 1);
 #pragma unroll
             for (int j = 0; j < C::kVals; ++j) vals[j] = 0.f;
-            for (int c = cf; c <= cl; ++c) {
-              const float* sl = slot_of(c);
+            // up to three slots in flight at a time (one for wide tiles), summed in CTA (K) order
+            if constexpr (C::kVals > 32) {
+              for (int c = cf; c <= cl; ++c) {
+                const float* sl = slot_of(c);
 #pragma unroll
-              for (int j = 0; j < C::kVals; ++j) vals[j] += __ldcg(sl + j * kMTile + m);
+                for (int j = 0; j < C::kVals; ++j) vals[j] += __ldcg(sl + j * kMTile + m);
+              }
+            } else
+            for (int c = cf; c <= cl; c += 3) {
+              float t1[C::kVals], t2[C::kVals], t3[C::kVals];
+              const float* s1p = slot_of(c);
+              const float* s2p = c + 1 <= cl ? slot_of(c + 1) : nullptr;
+              const float* s3p = c + 2 <= cl ? slot_of(c + 2) : nullptr;
+#pragma unroll
+              for (int j = 0; j < C::kVals; ++j) {
+                t1[j] = __ldcg(s1p + j * kMTile + m);
+                t2[j] = s2p ? __ldcg(s2p + j * kMTile + m) : 0.f;
+                t3[j] = s3p ? __ldcg(s3p + j * kMTile + m) : 0.f;
+              }
+#pragma unroll
+              for (int j = 0; j < C::kVals; ++j) {
+                vals[j] += t1[j];
+                if (s2p) vals[j] += t2[j];
+                if (s3p) vals[j] += t3[j];
+              }
             }
           }
         }

@@ -203,10 +203,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
-  // the routing, the encoded activations and (for down) h come from the previous
-  // kernels: wait for them to complete
-  pdl_wait();
-
+  // The tile table was written by the routing launch, which has completed before
+  // this kernel can start (every launch in between waited for it), so it is read
+  // before the dependency wait; the encoded activations (and, for down, h) come from
+  // the immediately preceding kernel and are only touched after pdl_wait().
   const int num_tiles = __ldg(p.num_tiles);
   const int KG = p.kg;
   const int U = num_tiles * p.mt;
@@ -228,16 +228,55 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const size_t wsf_group_stride = (size_t)p.mt * KG * kSfAtomBytes;
-      int g = 0;
-      bool err = false;
-      for (int si = 0; si < sch.nseg && !err; ++si) {
-        int u, kk0, kk1, tile, mt;
+      // iterator over this CTA's (segment, K group) iterations
+      int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0;
+      const uint8_t* wsf_base = nullptr;
+      auto open_seg = [&]() {
+        int u, kk0;
         bool whole;
         sch.seg(si, u, kk0, kk1, whole);
+        kk = kk0;
         map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
-        const int expert = p.tiles[tile].expert;
-        const uint8_t* wsf_base = p.w_sf + ((size_t)expert * p.w_groups * p.mt + mt) * (size_t)KG * kSfAtomBytes;
-        for (int kk = kk0; kk < kk1; ++kk, ++g) {
+        expert = p.tiles[tile].expert;
+        wsf_base = p.w_sf + ((size_t)expert * p.w_groups * p.mt + mt) * (size_t)KG * kSfAtomBytes;
+      };
+      auto advance = [&]() {
+        if (++kk == kk1 && ++si < sch.nseg) open_seg();
+      };
+      auto load_a = [&](int s) {
+        for (int j = 0; j < C::kA; ++j) {
+          tma_load_4d(a_tile(s, j), &p.tm_w, &full_bar[s], 0, mt * kMTile, kk, expert * p.w_groups + j);
+          bulk_load(sf_a(s, j), wsf_base + j * wsf_group_stride + (size_t)kk * kSfAtomBytes, kSfAtomBytes,
+                    &full_bar[s]);
+        }
+      };
+      auto load_b = [&](int s, int b_tile_idx, int b_kk) {
+        for (int bx = 0; bx < C::kBRows / C::kBBoxRows; ++bx)
+          tma_load_3d(b_tile(s) + bx * C::kBBoxRows * 64, &p.tm_act, &full_bar[s], 0,
+                      b_tile_idx * C::kBRows + bx * C::kBBoxRows, b_kk);
+        bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * KG + b_kk) * (kSfAtomBytes * C::kNbAtoms),
+                  kSfAtomBytes * C::kNbAtoms, &full_bar[s]);
+      };
+      int g = 0;
+      bool err = false;
+      if (sch.nseg > 0) {
+        open_seg();
+        // weights of the first stages depend only on the routing: stream them while
+        // the previous kernel finishes
+        int pre_tile[C::kStages], pre_kk[C::kStages];
+        int npre = 0;
+        while (npre < C::kStages && si < sch.nseg) {
+          mbar_arrive_expect_tx(&full_bar[npre], C::kTxBytes);  // fresh stages: no wait
+          load_a(npre);
+          pre_tile[npre] = tile;
+          pre_kk[npre] = kk;
+          ++npre;
+          advance();
+        }
+        pdl_wait();
+        for (int i = 0; i < npre; ++i) load_b(i, pre_tile[i], pre_kk[i]);
+        g = npre;
+        for (; si < sch.nseg; ++g) {
           const int s = g % C::kStages;
           const uint32_t ph = (g / C::kStages) & 1;
           if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1, kWaitLimit)) {
@@ -247,26 +286,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             break;
           }
           mbar_arrive_expect_tx(&full_bar[s], C::kTxBytes);
-          for (int j = 0; j < C::kA; ++j) {
-            tma_load_4d(a_tile(s, j), &p.tm_w, &full_bar[s], 0, mt * kMTile, kk, expert * p.w_groups + j);
-            bulk_load(sf_a(s, j), wsf_base + j * wsf_group_stride + (size_t)kk * kSfAtomBytes, kSfAtomBytes,
-                      &full_bar[s]);
-          }
-          for (int bx = 0; bx < C::kBRows / C::kBBoxRows; ++bx)
-            tma_load_3d(b_tile(s) + bx * C::kBBoxRows * 64, &p.tm_act, &full_bar[s], 0,
-                        tile * C::kBRows + bx * C::kBBoxRows, kk);
-          bulk_load(sf_b(s), p.act_sf + ((size_t)tile * KG + kk) * (kSfAtomBytes * C::kNbAtoms),
-                    kSfAtomBytes * C::kNbAtoms, &full_bar[s]);
+          load_a(s);
+          load_b(s, tile, kk);
+          advance();
         }
+      } else {
+        pdl_wait();
       }
       // on an error, wait (bounded) for the copies already issued to land
       if (err) {
         for (int gg = max(0, g - C::kStages); gg < g; ++gg)
           mbar_wait_bounded(&full_bar[gg % C::kStages], (gg / C::kStages) & 1, kWaitLimit);
       }
+    } else {
+      pdl_wait();
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    pdl_wait();
     if (lane == 0) {
       const uint32_t sf_col0 = C::kNumAcc * C::kAccCols;
       int g = 0;
@@ -331,6 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();  // unit counters are cleared by the preceding launches
     const int q = warp & 3;                // tensor-memory lane quarter of this warp
     const int m = q * 32 + lane;           // row of the 128-row tile
     const int et = threadIdx.x - 64;       // 0..127 within the epilogue warps

@@ -60,9 +60,10 @@ const char* moe_error_string(int status);
 
 /* ------------------------------------------------------------------ weights
  * One-time re-layout of raw MXFP4 expert weights into the layout the tensor-core
- * kernels stream: rows are padded along K to a multiple of 128 codes (pad codes 0)
- * and the E8M0 scales are regrouped into 512-byte atoms of 128 rows x 4 MX blocks,
- * the order in which the block-scaled MMA reads them.  No value is re-quantised;
+ * kernels stream: codes K-group major, [E][groups][K/128][rows per group][64 B]
+ * (K padded to a multiple of 128 codes with code 0), and the E8M0 scales regrouped
+ * into 512-byte atoms of 128 rows x 4 MX blocks, the order in which the
+ * block-scaled MMA reads them (groups = 2 for gate/up: gate rows, up rows).  No value is re-quantised;
  * the bytes are only moved ("MXFP4 MoE on tensor cores": weights permuted once at
  * load).
  *   kind  MOE_WEIGHTS_GATEUP: rows = 2*I (gate then up), K = H.
@@ -143,10 +144,11 @@ int moe_build_tile_table(const int32_t* topk_idx, int T, int k, int E, int tile_
 
 /* moe_mxfp4_gateup_swiglu: for every tile (expert e, rows of perm) and every
  * hidden feature i: g = x_t . W_gate[e][i], u = x_t . W_up[e][i], h = silu(g) * u.
- * x rows are gathered by perm (the permute step) and encoded as two E4M3 terms
- * with E8M0 block scales; the weights stay MXFP4 and their scales feed the
- * block-scaled MMA directly.  h is left in the workspace (two-term E4M3 in tile
- * row order) for moe_mxfp4_down_combine.
+ * x rows are gathered by perm (the permute step) and encoded as a sum of four
+ * E2M1 terms, each with its own E8M0 scale per 32-value block; the weights stay
+ * MXFP4 and both operands' scales feed the block-scaled MMA (kind::mxf4) directly.
+ * h is left in the workspace, encoded the same way in tile row order, for
+ * moe_mxfp4_down_combine.
  *   x bf16 [T, H]; perm, tiles, num_tiles as written by moe_build_tile_table with
  *   the same tile_rows (0 = policy); w_gateup: moe_prepare_weights(MOE_WEIGHTS_GATEUP).
  * Source: "Where the time went", row "MoE gate/up + SwiGLU".                       */
@@ -164,7 +166,7 @@ int moe_mxfp4_down_combine(const int32_t* perm, const int32_t* tiles, const int3
                            const float* topk_w, const void* w_down, int T, int H, int I, int E, int k,
                            void* workspace, size_t workspace_bytes, uint16_t* out, moe_stream_t stream);
 
-/* moe_hidden_dequant: expand the workspace's two-term encoded h into f32
+/* moe_hidden_dequant: expand the workspace's four-term encoded h into f32
  * [T*k, I] rows in assignment order (t*k + j); a test and inspection aid.          */
 int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows, int T,
                        int H, int I, int E, int k, const void* workspace, size_t workspace_bytes, float* h_out,

@@ -1,6 +1,6 @@
 // Data movement kernels around the expert GEMMs:
 //  * quant_x: the permute step -- activation rows gathered into tile order and
-//    encoded as two E4M3 terms with E8M0 block scales (the tensor-core B operand);
+//    encoded as four E2M1 terms with E8M0 block scales (the tensor-core B operand);
 //  * prepare: one-time re-layout of raw MXFP4 expert weights ("MXFP4 MoE on tensor
 //    cores": weights permuted once at load; nothing is re-quantised);
 //  * hidden_dequant: expands the encoded SwiGLU output for inspection.

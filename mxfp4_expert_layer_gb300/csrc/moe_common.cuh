@@ -1,5 +1,5 @@
 // Shared definitions of the MXFP4 MoE layer kernels: shapes, workspace layout,
-// the two-term E4M3 activation encoding and device status reporting.
+// the four-term E2M1 activation encoding and device status reporting.
 #pragma once
 
 #include <cstddef>

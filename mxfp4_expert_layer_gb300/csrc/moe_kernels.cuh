@@ -49,7 +49,7 @@ cudaError_t launch_tile_table(const int32_t* idx, int Tk, int E, int bm, int32_t
                               int32_t* perm, int32_t* inv_perm, TileEntry* tiles, int32_t* num_tiles,
                               cudaStream_t stream);
 
-// Gather + two-term E4M3 encoding of the activation rows of every tile.
+// Gather + four-term E2M1 encoding of the activation rows of every tile.
 struct QuantXParams {
   const uint16_t* x;       // bf16 [T, H]
   const int32_t* perm;

@@ -159,7 +159,9 @@ int moe_mxfp4_gateup_swiglu(const uint16_t* x, const int32_t* perm, const int32_
 /* moe_mxfp4_down_combine: y_tj = h_tj . W_down[e_tj]^T for every assignment, then
  * out[t] = sum_{j=0..k-1} topk_w[t, j] * y_tj summed in fp32 in ascending j and
  * rounded once to bf16 -- deterministic run to run.  Reads h from the workspace
- * (written by moe_mxfp4_gateup_swiglu for the same routing).
+ * (written by moe_mxfp4_gateup_swiglu for the same routing).  Two launches: the
+ * down GEMM writes w_tj * y_tj into a per-assignment fp32 slot of the workspace,
+ * then a combine kernel sums each token's k slots.
  *   topk_w f32 [T, k]; w_down: moe_prepare_weights(MOE_WEIGHTS_DOWN); out bf16 [T, H].
  * Source: "Where the time went", row "MoE down + combine".                         */
 int moe_mxfp4_down_combine(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows,
@@ -183,17 +185,20 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* router
                 uint16_t* out, int32_t* topk_idx_out, float* topk_w_out, moe_stream_t stream);
 
 /* moe_forward_timed: moe_forward that also records caller-created CUDA events
- * (cudaEvent_t, passed as void*) on `stream`: events[i] just before launch i and
- * events[n] after the last one, n = moe_forward_launches(...); the launches are
- * route + tile table, gather + encode of x, gate/up + SwiGLU, down + combine.  It
- * gives the per-kernel time split ("Where the time went": per-section times of a
- * decode step).  events must hold n + 1 valid events.                             */
+ * (cudaEvent_t, passed as void*) on `stream` around its MOE_FORWARD_STAGES stages:
+ * events[i] just before stage i and events[MOE_FORWARD_STAGES] after the last one.
+ * The stages are route + tile table, gather + encode of x, gate/up + SwiGLU, and
+ * down + combine (two launches).  It gives the per-stage time split ("Where the
+ * time went": per-section times of a decode step).  events must hold
+ * MOE_FORWARD_STAGES + 1 valid events.                                            */
+#define MOE_FORWARD_STAGES 4
 int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
                       const void* w_down, int T, int H, int I, int E, int k, void* workspace,
                       size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
                       void* const* events, moe_stream_t stream);
 
-/* Number of kernels moe_forward launches for a shape (for launch accounting). */
+/* Number of kernels moe_forward launches for a shape (for launch accounting):
+ * route + table, gather + encode, gate/up, down, combine.                          */
 int moe_forward_launches(int T, int H, int I, int E, int k);
 
 /* Synchronises `stream`, reads the workspace's device status word into *status

@@ -171,7 +171,7 @@ int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, c
   q.T = T; q.H = H; q.k = k; q.bm = bm; q.max_tiles = L.max_tiles; q.kg = L.kg_h;
   q.q = ws_ptr<uint8_t>(ws, L.x_q);
   q.sf = ws_ptr<uint8_t>(ws, L.x_sf);
-  q.zero_buf = ws_ptr<int32_t>(ws, L.combine_cnt);
+  q.zero_buf = ws_ptr<int32_t>(ws, L.unit_cnt);
   q.zero_count = (int)(L.zero_bytes / sizeof(int32_t));
   cudaError_t e = launch_quant_x(q, stream);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -224,13 +224,17 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   g.group_tiles = bm >= 128 ? 32 : (bm >= 64 ? 16 : 1);
   g.topk_w = topk_w;
   g.slots = ws_ptr<float>(ws, L.slots);
-  g.combine_cnt = ws_ptr<int32_t>(ws, L.combine_cnt);
-  g.out = out;
   g.grid = persistent_ctas();
   g.partials = ws_ptr<float>(ws, L.partials);
   g.unit_cnt = ws_ptr<int32_t>(ws, L.unit_cnt);
   g.status = ws_ptr<uint32_t>(ws, L.status);
-  return cuda_status(launch_down(g, stream));
+  int st = cuda_status(launch_down(g, stream));
+  if (st != MOE_OK) return st;
+  CombineParams c{};
+  c.slots = g.slots;
+  c.T = T; c.H = H; c.k = k;
+  c.out = out;
+  return cuda_status(launch_combine(c, stream));
 }
 
 RouteParams route_params(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E, int k,
@@ -465,7 +469,7 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
 
 int moe_forward_launches(int T, int H, int I, int E, int k) {
   if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
-  return 4;  // route+table, gather+encode, gate/up, down+combine
+  return 5;  // route+table, gather+encode, gate/up, down, combine
 }
 
 int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream) {

@@ -106,6 +106,40 @@ cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t stream) {
   return launch_pdl(quant_x_kernel, dim3(blocks), dim3(kAuxThreads), 0, stream, p);
 }
 
+// Weighted top-k combine + unpermute ("Where the time went", row "MoE down +
+// combine"): out[t, f] = sum_{j<k} slot[t*k + j, f], each slot already holding
+// w_tj * y_tj, summed in fp32 in ascending j and rounded once to bf16 (RNE) -- the
+// same order every call.  One thread per 4 features of one token.
+__global__ void __launch_bounds__(kAuxThreads) combine_kernel(CombineParams p) {
+  ptx::pdl_wait();
+  ptx::pdl_launch_dependents();
+  const int nq = p.H / 4;
+  const long long i = (long long)blockIdx.x * kAuxThreads + threadIdx.x;
+  if (i >= (long long)p.T * nq) return;
+  const int t = (int)(i / nq), q = (int)(i - (long long)t * nq);
+  const float4* s = reinterpret_cast<const float4*>(p.slots + (size_t)t * p.k * p.H) + q;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int j = 0; j < p.k; ++j) {
+    const float4 v = __ldcg(s + (size_t)j * nq);
+    acc.x += v.x;
+    acc.y += v.y;
+    acc.z += v.z;
+    acc.w += v.w;
+  }
+  const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.x)) |
+                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
+  const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
+                      ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+  reinterpret_cast<uint2*>(p.out + (size_t)t * p.H)[q] = make_uint2(lo, hi);
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+  const long long threads = (long long)p.T * (p.H / 4);
+  const int blocks = (int)((threads + kAuxThreads - 1) / kAuxThreads);
+  return launch_pdl(combine_kernel, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
+}
+
 // Codes: 16-byte vectors moved into the K-group-major layout
 // [E][G][KG][rows per group][64 bytes]; vectors past K/2 bytes of a row are zero.
 __global__ void prepare_codes_kernel(PrepareParams p) {

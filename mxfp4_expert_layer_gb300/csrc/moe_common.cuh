@@ -80,9 +80,8 @@ struct WsLayout {
   size_t h_q;            // h encoded: [kg_i][max_tiles][kTerms][bm][64 bytes]
   size_t h_sf;           // [max_tiles][kg_i][512 * act_sf_atoms(bm)]
   size_t slots;          // f32 [T*k, H]: weighted expert outputs awaiting the combine
-  size_t combine_cnt;    // i32 [T, mt_h]: arrivals per (token, output tile)
   size_t unit_cnt;       // i32 [max_tiles * max(mt_h, mt_i)]: arrivals per GEMM work unit
-  size_t zero_bytes;     // bytes from combine_cnt cleared before each layer call
+  size_t zero_bytes;     // bytes from unit_cnt cleared before each layer call
   size_t partials;       // f32 [2 * kMaxCtas][2 * bm * 128]: split-K partial accumulators
   size_t total;
 };
@@ -121,9 +120,8 @@ inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   L.h_q = take((size_t)L.kg_i * L.pad_rows * kTerms * 64);
   L.h_sf = take((size_t)L.max_tiles * L.kg_i * sfa);
   L.slots = take(sizeof(float) * tk * H);
-  L.combine_cnt = take(sizeof(int32_t) * (size_t)T * L.mt_h);
   L.unit_cnt = take(sizeof(int32_t) * (size_t)L.max_tiles * (L.mt_h > L.mt_i ? L.mt_h : L.mt_i));
-  L.zero_bytes = o - L.combine_cnt;
+  L.zero_bytes = o - L.unit_cnt;
   L.partials = take(sizeof(float) * (size_t)2 * kMaxCtas * 2 * bm * kMTile);
   L.total = o;
   return L;

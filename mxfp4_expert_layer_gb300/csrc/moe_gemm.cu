@@ -1,6 +1,7 @@
 // Grouped MXFP4 expert GEMMs on the 5th-generation tensor cores (tcgen05):
 //   gate/up + SwiGLU   h = silu(x W_gate^T) * (x W_up^T)
-//   down + combine     out[t] = sum_j w_tj * (h_tj W_down^T)
+//   down               slot_tj = w_tj * (h_tj W_down^T), summed over j by the
+//                      combine launch that follows
 //
 // Sources: "A 297-line kernel file that decodes faster than vLLM", section "Where
 // the time went" (rows "MoE gate/up + SwiGLU" and "MoE down + combine") and
@@ -104,10 +105,11 @@ struct SplitK {
   __device__ __forceinline__ int slot(int c, int u, int kg) const { return (u == begin(c) / kg) ? 2 * c : 2 * c + 1; }
 };
 
-// Work schedule of one CTA: D whole units dealt round-robin (unit c + w*G), then an
-// even split of the remaining units' K iterations (stream-K).  D leaves between G
-// and 2G units for the split so every CTA gets work and none gets more than one
-// unit's worth extra.
+// Work schedule of one CTA.  With no more units than CTAs every CTA runs one whole
+// unit (grid = U): nothing is split, so no partials are exchanged.  Otherwise D
+// whole units are dealt round-robin (unit c + w*G), then the remaining units' K
+// iterations are split evenly (stream-K); D leaves between G and 2G units for the
+// split so every CTA gets work and none gets more than one unit's worth extra.
 struct Schedule {
   int KG, G, D, u0;   // u0 = D * G: first unit of the split part
   SplitK sk;          // over the split part's iterations
@@ -116,7 +118,7 @@ struct Schedule {
   __device__ void init(int U, int kg, int grid, int cta) {
     KG = kg;
     G = grid;
-    D = (U >= 2 * grid) ? U / grid - 1 : 0;
+    D = (U <= grid) ? 1 : (U >= 2 * grid) ? U / grid - 1 : 0;  // U <= grid: callers pass grid = U
     u0 = D * grid;
     const long long Wr = (long long)(U - u0) * kg;
     sk.W = Wr;
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   uint64_t* accf_bar = empty_bar + C::kStages;   // [2] accumulator ready
   uint64_t* acce_bar = accf_bar + 2;             // [2] accumulator drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
-  int* s_flags = reinterpret_cast<int*>(tmem_slot + 4);  // [0] error, [1] unit finisher, [2..] combine
+  int* s_flags = reinterpret_cast<int*>(tmem_slot + 4);  // [0] error, [1] unit finisher
   float* s_xpose = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);  // [16][128]
   int* s_rowa = reinterpret_cast<int*>(s_xpose + 16 * kMTile);   // [128] assignment of each tile row
   float* s_roww = reinterpret_cast<float*>(s_rowa + 128);         // [128] its top-k weight
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   const int num_tiles = __ldg(p.num_tiles);
   const int KG = p.kg;
   const int U = num_tiles * p.mt;
-  const int grid = (long long)U * KG < (long long)gridDim.x ? U * KG : (int)gridDim.x;
+  const int grid = U <= (int)gridDim.x ? U : (int)gridDim.x;
   Schedule sch;
   sch.init(U, KG, grid > 0 ? grid : 1, blockIdx.x);
   if (U == 0 || (int)blockIdx.x >= grid) sch.nseg = 0;  // no work: straight to teardown
@@ -612,53 +614,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         }
       }
 
-      if constexpr (!GATEUP) {
-        // deterministic combine: the last CTA to finish a (token, output tile) sums the
-        // token's k weighted slots in ascending j and writes the bf16 output
-        if (finished) {
-          __threadfence();
-          epi_bar();
-          if (et < BM) {
-            int fin = 0;
-            if (et < nrows) {
-              const int t = s_rowa[et] / p.k;
-              int* cnt = p.combine_cnt + (size_t)t * p.mt + mt;
-              const int old = atomicAdd(cnt, 1);
-              if (old == p.k - 1) {
-                fin = 1;
-                *cnt = 0;  // ready for the next call
-              }
-            }
-            s_flags[2 + et] = fin;
-          }
-          epi_bar();
-          __threadfence();
-          if (feat < p.H) {
-            // 8 rows at a time so their slot loads are in flight together
-            for (int r0 = 0; r0 < nrows; r0 += 8) {
-              int tt[8];
-              bool f[8];
-              float acc[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int r = r0 + i;
-                f[i] = (r < nrows) && s_flags[2 + r];
-                tt[i] = f[i] ? s_rowa[r] / p.k : 0;
-                acc[i] = 0.f;
-              }
-              for (int j = 0; j < p.k; ++j) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                  if (f[i]) acc[i] += __ldcg(p.slots + ((size_t)tt[i] * p.k + j) * p.H + feat);
-              }
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                if (f[i]) p.out[(size_t)tt[i] * p.H + feat] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[i]));
-            }
-          }
-        }
-      }
-      epi_bar();  // flags and row metadata are reused by the next segment
+      epi_bar();  // row metadata is reused by the next segment
     }
   }
   tc_fence_before();

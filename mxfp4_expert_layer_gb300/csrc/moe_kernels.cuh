@@ -58,7 +58,7 @@ struct QuantXParams {
   int T, H, k, bm, max_tiles, kg;
   uint8_t* q;              // [kg][max_tiles][kTerms][bm][64]: four E2M1 terms per row
   uint8_t* sf;             // [max_tiles][kg][512 * act_sf_atoms(bm)]
-  int32_t* zero_buf;       // combine counters to clear (or null)
+  int32_t* zero_buf;       // GEMM arrival counters to clear (or null)
   int zero_count;
 };
 cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t stream);
@@ -84,9 +84,7 @@ struct GemmParams {
   int kg_out;              // K groups of h along I
   // down epilogue
   const float* topk_w;
-  float* slots;            // f32 [T*k, H]
-  int32_t* combine_cnt;    // [T, mt]
-  uint16_t* out;           // bf16 [T, H]
+  float* slots;            // f32 [T*k, H]: w_tj * y_tj per assignment
   // split-K across persistent CTAs
   int grid;                // persistent CTAs (<= kMaxCtas)
   float* partials;         // [2 * grid][kA * bm * 128] partial accumulators
@@ -95,6 +93,14 @@ struct GemmParams {
 };
 cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_down(const GemmParams& p, cudaStream_t stream);
+
+// Weighted top-k combine + unpermute of the down GEMM's slots into bf16 rows.
+struct CombineParams {
+  const float* slots;      // f32 [T*k, H], slot t*k + j = w_tj * y_tj
+  int T, H, k;
+  uint16_t* out;           // bf16 [T, H]
+};
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 struct PrepareParams {
   const uint8_t* codes;    // [E][R][K/2]

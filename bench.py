@@ -285,7 +285,7 @@ def main():
     # one CUDA graph per weight copy: a replay is one step (the layer runs inside a
     # captured decode step in the pages' engine); --eager times plain launches
     nk = 4  # stages bracketed by moe_forward_timed's events (MOE_FORWARD_STAGES)
-    names = ["route_topk_table", "gather_encode_x", "gateup_swiglu", "down_combine"]
+    names = ["encode_x", "route_topk_table", "gateup_swiglu", "down_combine"]
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     graphs, tgraphs, tevents = [], [], []

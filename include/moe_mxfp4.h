@@ -144,9 +144,11 @@ int moe_build_tile_table(const int32_t* topk_idx, int T, int k, int E, int tile_
 
 /* moe_mxfp4_gateup_swiglu: for every tile (expert e, rows of perm) and every
  * hidden feature i: g = x_t . W_gate[e][i], u = x_t . W_up[e][i], h = silu(g) * u.
- * x rows are gathered by perm (the permute step) and encoded as a sum of four
- * E2M1 terms, each with its own E8M0 scale per 32-value block; the weights stay
- * MXFP4 and both operands' scales feed the block-scaled MMA (kind::mxf4) directly.
+ * Three launches: every token row of x is encoded once as a sum of four E2M1
+ * terms, each with its own E8M0 scale per 32-value block; the encoded rows are
+ * gathered by perm (the permute step) into tile order; the GEMM runs.  The
+ * weights stay MXFP4 and both operands' scales feed the block-scaled MMA
+ * (kind::mxf4) directly.
  * h is left in the workspace, encoded the same way in tile row order, for
  * moe_mxfp4_down_combine.
  *   x bf16 [T, H]; perm, tiles, num_tiles as written by moe_build_tile_table with
@@ -187,8 +189,9 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* router
 /* moe_forward_timed: moe_forward that also records caller-created CUDA events
  * (cudaEvent_t, passed as void*) on `stream` around its MOE_FORWARD_STAGES stages:
  * events[i] just before stage i and events[MOE_FORWARD_STAGES] after the last one.
- * The stages are route + tile table, gather + encode of x, gate/up + SwiGLU, and
- * down + combine (two launches).  It gives the per-stage time split ("Where the
+ * The stages are the per-token encoding of x, route + top-k + tile table, gate/up
+ * + SwiGLU (two launches: the gather of the encoded rows by perm, then the GEMM),
+ * and down + combine (two launches).  It gives the per-stage time split ("Where the
  * time went": per-section times of a decode step).  events must hold
  * MOE_FORWARD_STAGES + 1 valid events.                                            */
 #define MOE_FORWARD_STAGES 4
@@ -198,7 +201,7 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
                       void* const* events, moe_stream_t stream);
 
 /* Number of kernels moe_forward launches for a shape (for launch accounting):
- * route + table, gather + encode, gate/up, down, combine.                          */
+ * encode x, route + top-k + table, gather x, gate/up, down, combine.               */
 int moe_forward_launches(int T, int H, int I, int E, int k);
 
 /* Synchronises `stream`, reads the workspace's device status word into *status

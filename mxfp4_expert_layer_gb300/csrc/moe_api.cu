@@ -158,30 +158,39 @@ int persistent_ctas() {
 }
 
 // ------------------------------------------------------------------ stage bodies
-int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm,
-               const void* w_gateup, int T, int H, int I, int E, int k, void* ws, const WsLayout& L,
-               cudaStream_t stream, void* const* events = nullptr) {
-  // events (optional): [0] before the gather/encode launch, [1] before the GEMM
-  if (events) record_event(events[0], stream);
-  QuantXParams q{};
+// Per-token activation encoding; also clears the GEMMs' arrival counters.
+int run_encode_x(const uint16_t* x, int T, int H, void* ws, const WsLayout& L, cudaStream_t stream) {
+  EncodeXParams q{};
   q.x = x;
-  q.perm = perm;
-  q.tiles = tiles;
-  q.num_tiles = num_tiles;
-  q.T = T; q.H = H; q.k = k; q.bm = bm; q.max_tiles = L.max_tiles; q.kg = L.kg_h;
-  q.q = ws_ptr<uint8_t>(ws, L.x_q);
-  q.sf = ws_ptr<uint8_t>(ws, L.x_sf);
+  q.T = T; q.H = H;
+  q.q = ws_ptr<uint8_t>(ws, L.xt_q);
+  q.sf = ws_ptr<uint32_t>(ws, L.xt_sf);
   q.zero_buf = ws_ptr<int32_t>(ws, L.unit_cnt);
   q.zero_count = (int)(L.zero_bytes / sizeof(int32_t));
-  cudaError_t e = launch_quant_x(q, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_encode_x(q, stream));
+}
+
+// The permute (gather of the encoded rows into tile order) and the gate/up GEMM; x
+// must already be encoded in the workspace (run_encode_x).
+int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm, const void* w_gateup,
+               int T, int H, int I, int E, int k, void* ws, const WsLayout& L, cudaStream_t stream) {
+  GatherXParams gx{};
+  gx.xt_q = ws_ptr<uint8_t>(ws, L.xt_q);
+  gx.xt_sf = ws_ptr<uint32_t>(ws, L.xt_sf);
+  gx.perm = perm;
+  gx.tiles = tiles;
+  gx.num_tiles = num_tiles;
+  gx.T = T; gx.k = k; gx.bm = bm; gx.max_tiles = L.max_tiles; gx.kg = L.kg_h;
+  gx.q = ws_ptr<uint8_t>(ws, L.x_q);
+  gx.sf = ws_ptr<uint8_t>(ws, L.x_sf);
+  if (launch_gather_x(gx, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
   const PreparedLayout P = make_prepared_layout(E, 2 * I, H, 2);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_gateup, P)) return MOE_ERR_CUDA;
-  if (!act_map(&g.tm_act, q.q, H, L.max_tiles, bm)) return MOE_ERR_CUDA;
+  if (!act_map(&g.tm_act, gx.q, H, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_gateup) + P.scales_off;
-  g.act_sf = q.sf;
+  g.act_sf = gx.sf;
   g.tiles = tiles;
   g.num_tiles = num_tiles;
   g.perm = perm;
@@ -199,7 +208,6 @@ int run_gateup(const uint16_t* x, const int32_t* perm, const TileEntry* tiles, c
   g.partials = ws_ptr<float>(ws, L.partials);
   g.unit_cnt = ws_ptr<int32_t>(ws, L.unit_cnt);
   g.status = ws_ptr<uint32_t>(ws, L.status);
-  if (events) record_event(events[1], stream);
   return cuda_status(launch_gateup(g, stream));
 }
 
@@ -364,8 +372,11 @@ int moe_mxfp4_gateup_swiglu(const uint16_t* x, const int32_t* perm, const int32_
     return MOE_ERR_INVALID_ARG;
   const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  return run_gateup(x, perm, reinterpret_cast<const TileEntry*>(tiles), num_tiles, bm, w_gateup, T, H, I, E, k,
-                    workspace, L, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = run_encode_x(x, T, H, workspace, L, s);
+  if (st != MOE_OK) return st;
+  return run_gateup(perm, reinterpret_cast<const TileEntry*>(tiles), num_tiles, bm, w_gateup, T, H, I, E, k,
+                    workspace, L, s);
 }
 
 int moe_mxfp4_down_combine(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows,
@@ -440,10 +451,16 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   auto mark = [&](int i) {
     if (events && record_event(events[i], s) != cudaSuccess) ev_ok = false;
   };
+  r.wait_at_end = 1;  // the encoding launch before it waits for the previous call
+  // stages: [0] encode x, [1] route + top-k + tile table, [2] gate/up, [3] down + combine
   mark(0);
   if (!ev_ok) return MOE_ERR_INVALID_ARG;
+  st = run_encode_x(x, T, H, ws, L, s);
+  if (st != MOE_OK) return st;
+  mark(1);
   if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
-  st = run_gateup(x, perm, tiles, num_tiles, bm, w_gateup, T, H, I, E, k, ws, L, s, events ? events + 1 : nullptr);
+  mark(2);
+  st = run_gateup(perm, tiles, num_tiles, bm, w_gateup, T, H, I, E, k, ws, L, s);
   if (st != MOE_OK) return st;
   mark(3);
   st = run_down(perm, tiles, num_tiles, bm, w, w_down, T, H, I, E, k, ws, L, out, s);
@@ -469,7 +486,7 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
 
 int moe_forward_launches(int T, int H, int I, int E, int k) {
   if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
-  return 5;  // route+table, gather+encode, gate/up, down, combine
+  return 6;  // encode x, route + table, gather x, gate/up, down, combine
 }
 
 int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream) {

@@ -1,6 +1,6 @@
 // Data movement kernels around the expert GEMMs:
-//  * quant_x: the permute step -- activation rows gathered into tile order and
-//    encoded as four E2M1 terms with E8M0 block scales (the tensor-core B operand);
+//  * encode_x: activation rows encoded once per token as four E2M1 terms with E8M0
+//    block scales (the tensor-core B operand, gathered by the gate/up GEMM);
 //  * prepare: one-time re-layout of raw MXFP4 expert weights ("MXFP4 MoE on tensor
 //    cores": weights permuted once at load; nothing is re-quantised);
 //  * hidden_dequant: expands the encoded SwiGLU output for inspection.
@@ -22,14 +22,16 @@ __device__ __forceinline__ float quad_max(float v) {
   return v;
 }
 
-// Gather + encode: one warp per (tile row, 256-value chunk of x), so every load of a
-// call is in flight at once.  Each lane owns 8 consecutive values (one 16-byte
-// load); four lanes form one 32-value MX block, and the block is written as kTerms
-// E2M1 terms x ~ sum_t q_t * 2^p_t, each term with its own E8M0 exponent chosen
-// for the residual left by the terms before.  Values past H up to the next
-// multiple of 64 are encoded as zeros so every 64-value MMA step reads finite data.
-__global__ void __launch_bounds__(kAuxThreads) quant_x_kernel(QuantXParams p) {
-  ptx::pdl_wait();
+// Activation encoding, once per token: one warp per (token, 256-value chunk of x),
+// so every load of a call is in flight at once.  Each lane owns 8 consecutive
+// values (one 16-byte load); four lanes form one 32-value MX block, and the block
+// is written as kTerms E2M1 terms x ~ sum_t q_t * 2^p_t, each term with its own
+// E8M0 exponent chosen for the residual left by the terms before.  Values past H
+// up to the next multiple of 64 are encoded as zeros so every 64-value MMA step
+// reads finite data.  The gate/up GEMM gathers these rows by perm (the permute
+// step), so each token is encoded once however many experts it is routed to.
+__global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) {
+  ptx::pdl_wait();  // the previous layer call may still read this call's buffers
   ptx::pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
@@ -40,20 +42,14 @@ __global__ void __launch_bounds__(kAuxThreads) quant_x_kernel(QuantXParams p) {
   }
   const int nvec_pad = ((p.H + 63) / 64) * 8;  // 8-value vectors per row, padded to 64 values
   const int nchunks = (nvec_pad + 31) / 32;
-  const int row = (int)(gw / nchunks);
-  const int chunk = (int)(gw - (long long)row * nchunks);
-  const int num_tiles = __ldg(p.num_tiles);
-  const int tile = row / p.bm;
-  if (tile >= num_tiles) return;
-  const int r = row - tile * p.bm;
-  const TileEntry te = p.tiles[tile];
-  if (r >= te.n_rows) return;
-  const int a = __ldg(p.perm + te.row_begin + r);
+  const int t = (int)(gw / nchunks);
+  if (t >= p.T) return;
+  const int chunk = (int)(gw - (long long)t * nchunks);
   const int v = chunk * 32 + lane;
   const int nvec = p.H / 8;
   float f[8];
   if (v < nvec) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)(a / p.k) * p.H) + v);
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + v);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -64,10 +60,9 @@ __global__ void __launch_bounds__(kAuxThreads) quant_x_kernel(QuantXParams p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) f[i] = 0.f;
   }
-  const int natoms = act_sf_atoms(p.bm);
-  uint8_t* sf = p.sf + (size_t)tile * p.kg * (kSfAtomBytes * natoms);
+  const int kgroup = v >> 4;  // 16 vectors = 128 values per K group
 #pragma unroll
-  for (int t = 0; t < kTerms; ++t) {
+  for (int term = 0; term < kTerms; ++term) {
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(f[i]));
@@ -89,21 +84,57 @@ __global__ void __launch_bounds__(kAuxThreads) quant_x_kernel(QuantXParams p) {
                          (__shfl_sync(0xffffffffu, e8, base + 8) << 16) |
                          (__shfl_sync(0xffffffffu, e8, base + 12) << 24);
     if (v < nvec_pad) {
-      *reinterpret_cast<uint32_t*>(p.q + act_offset(tile, t, r, v * 8, p.max_tiles, p.bm)) = word;
-      if ((lane & 15) == 0) {
-        const int kgroup = v >> 4;  // 16 vectors = 128 values per K group
-        *reinterpret_cast<uint32_t*>(sf + (size_t)kgroup * (kSfAtomBytes * natoms) +
-                                     sf_atom_offset(t * p.bm + r, 0)) = sfw;
-      }
+      const size_t row = ((size_t)kgroup * p.T + t) * kTerms + term;
+      *reinterpret_cast<uint32_t*>(p.q + row * 64 + (v & 15) * 4) = word;
+      if ((lane & 15) == 0) p.sf[row] = sfw;
     }
   }
 }
 
-cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t stream) {
+cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream) {
   const int nvec_pad = ((p.H + 63) / 64) * 8;
-  const long long warps = (long long)p.max_tiles * p.bm * ((nvec_pad + 31) / 32);
+  const long long warps = (long long)p.T * ((nvec_pad + 31) / 32);
   const int blocks = (int)((warps * 32 + kAuxThreads - 1) / kAuxThreads);
-  return launch_pdl(quant_x_kernel, dim3(blocks), dim3(kAuxThreads), 0, stream, p);
+  return launch_pdl(encode_x_kernel, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
+}
+
+// The permute step: every (tile row, K group) copies its token's four encoded
+// 64-byte code runs and their exponent words from token order into the tile order
+// the gate/up GEMM loads by TMA.  Rows past a tile's last token are left as they
+// are (finite: zero-filled once, or earlier encodings) and their products are never
+// read.
+__global__ void __launch_bounds__(kAuxThreads) gather_x_kernel(GatherXParams p) {
+  ptx::pdl_wait();  // the routing launch (tile table) and the encoding before it
+  ptx::pdl_launch_dependents();
+  const long long i = (long long)blockIdx.x * kAuxThreads + threadIdx.x;
+  const int kg = (int)(i % p.kg);
+  const long long row = i / p.kg;
+  const int tile = (int)(row / p.bm), r = (int)(row - (long long)tile * p.bm);
+  if (tile >= p.max_tiles || tile >= __ldcg(p.num_tiles)) return;
+  const TileEntry te = load_tile(p.tiles + tile);
+  if (r >= te.n_rows) return;
+  const int tok = __ldcg(p.perm + te.row_begin + r) / p.k;
+  const size_t src_row = ((size_t)kg * p.T + tok) * kTerms;
+  const uint4* src = reinterpret_cast<const uint4*>(p.xt_q + src_row * 64);
+  uint4 v[kTerms * 4];
+#pragma unroll
+  for (int j = 0; j < kTerms * 4; ++j) v[j] = __ldcg(src + j);
+  const uint4 e = __ldcg(reinterpret_cast<const uint4*>(p.xt_sf + src_row));
+  const uint32_t ew[kTerms] = {e.x, e.y, e.z, e.w};
+  uint8_t* sf = p.sf + ((size_t)tile * p.kg + kg) * (kSfAtomBytes * act_sf_atoms(p.bm));
+#pragma unroll
+  for (int t = 0; t < kTerms; ++t) {
+    uint4* dst = reinterpret_cast<uint4*>(p.q + act_offset(tile, t, r, kg * kKGroup, p.max_tiles, p.bm));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = v[t * 4 + j];
+    *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(t * p.bm + r, 0)) = ew[t];
+  }
+}
+
+cudaError_t launch_gather_x(const GatherXParams& p, cudaStream_t stream) {
+  const long long threads = (long long)p.max_tiles * p.bm * p.kg;
+  const int blocks = (int)((threads + kAuxThreads - 1) / kAuxThreads);
+  return launch_pdl(gather_x_kernel, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
 }
 
 // Weighted top-k combine + unpermute ("Where the time went", row "MoE down +

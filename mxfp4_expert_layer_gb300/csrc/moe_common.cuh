@@ -58,6 +58,18 @@ struct TileEntry {
   int32_t pad_row;    // first row of the tile in the padded activation buffers (= tile * bm)
 };
 
+// One tile-table entry through L2 only (16-byte load): the table is produced by an
+// earlier kernel of the same call.
+__device__ __forceinline__ TileEntry load_tile(const TileEntry* t) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(t));
+  TileEntry e;
+  e.expert = v.x;
+  e.row_begin = v.y;
+  e.n_rows = v.z;
+  e.pad_row = v.w;
+  return e;
+}
+
 // ----------------------------------------------------------------- workspace
 // Byte offsets of every region inside the caller-allocated workspace.
 struct WsLayout {
@@ -75,7 +87,9 @@ struct WsLayout {
   size_t inv_perm;       // i32 [T*k]
   size_t tiles;          // TileEntry [max_tiles]
   size_t num_tiles;      // i32
-  size_t x_q;            // x encoded: [kg_h][max_tiles][kTerms][bm][64 bytes] packed E2M1
+  size_t xt_q;           // x encoded per token: [kg_h][T][kTerms][64 bytes] packed E2M1
+  size_t xt_sf;          // its E8M0 exponents: u32 [kg_h][T][kTerms] (4 MX blocks each)
+  size_t x_q;            // x gathered into tile order: [kg_h][max_tiles][kTerms][bm][64 bytes]
   size_t x_sf;           // its scale atoms [max_tiles][kg_h][512 * act_sf_atoms(bm)]
   size_t h_q;            // h encoded: [kg_i][max_tiles][kTerms][bm][64 bytes]
   size_t h_sf;           // [max_tiles][kg_i][512 * act_sf_atoms(bm)]
@@ -115,6 +129,8 @@ inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   L.inv_perm = take(sizeof(int32_t) * tk);
   L.tiles = take(sizeof(TileEntry) * (size_t)L.max_tiles);
   L.num_tiles = take(sizeof(int32_t));
+  L.xt_q = take((size_t)L.kg_h * T * kTerms * 64);
+  L.xt_sf = take((size_t)L.kg_h * T * kTerms * sizeof(uint32_t));
   L.x_q = take((size_t)L.kg_h * L.pad_rows * kTerms * 64);
   L.x_sf = take((size_t)L.max_tiles * L.kg_h * sfa);
   L.h_q = take((size_t)L.kg_i * L.pad_rows * kTerms * 64);

@@ -206,10 +206,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   const uint32_t tmem = *tmem_slot;
   pdl_launch_dependents();
   // The tile table was written by the routing launch, which has completed before
-  // this kernel can start (every launch in between waited for it), so it is read
-  // before the dependency wait; the encoded activations (and, for down, h) come from
-  // the immediately preceding kernel and are only touched after pdl_wait().
-  const int num_tiles = __ldg(p.num_tiles);
+  // this kernel can start: at least one launch lies between them, and every such
+  // launch signals its dependents only after its own dependency wait.  So the table
+  // is read before this kernel's wait; the B operand (gathered x, or h) comes from
+  // the immediately preceding kernel and is only touched after pdl_wait().  Routing
+  // outputs are read through L2 only (ld.global.cg): kernels overlap their
+  // neighbours, so nothing may come from an L1 line left by an earlier call.
+  const int num_tiles = __ldcg(p.num_tiles);
   const int KG = p.kg;
   const int U = num_tiles * p.mt;
   const int grid = U <= (int)gridDim.x ? U : (int)gridDim.x;
@@ -239,7 +242,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         sch.seg(si, u, kk0, kk1, whole);
         kk = kk0;
         map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
-        expert = p.tiles[tile].expert;
+        expert = __ldcg(&p.tiles[tile].expert);
         wsf_base = p.w_sf + ((size_t)expert * p.w_groups * p.mt + mt) * (size_t)KG * kSfAtomBytes;
       };
       auto advance = [&]() {
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    pdl_wait();  // unit counters are cleared by the preceding launches
+    pdl_wait();  // unit counters are cleared by the call's first launch
     const int q = warp & 3;                // tensor-memory lane quarter of this warp
     const int m = q * 32 + lane;           // row of the 128-row tile
     const int et = threadIdx.x - 64;       // 0..127 within the epilogue warps
@@ -382,15 +385,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       sch.seg(si, u, kk0, kk1, whole);
       const int b = si % C::kNumAcc;
       map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
-      const TileEntry te = p.tiles[tile];
+      const TileEntry te = load_tile(p.tiles + tile);
       const int nrows = te.n_rows;
       const int feat = mt * kMTile + m;
       if constexpr (!GATEUP) {
         // row metadata of the tile, staged before the accumulator is ready
         if (et < nrows) {
-          const int a = __ldg(p.perm + te.row_begin + et);
+          const int a = __ldcg(p.perm + te.row_begin + et);
           s_rowa[et] = a;
-          s_roww[et] = __ldg(p.topk_w + a);
+          s_roww[et] = __ldcg(p.topk_w + a);
         }
       }
       const bool ok = mbar_wait_bounded(&accf_bar[b], (si / C::kNumAcc) & 1, kWaitLimit);

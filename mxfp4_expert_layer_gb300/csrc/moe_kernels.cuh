@@ -38,6 +38,7 @@ struct RouteParams {
   float* topk_w;            // f32 [T, k]
   uint32_t* sync;           // arrival counters [ceil(T/8) + 1], zero between calls
   int build_table;          // also build the tile table (last block)
+  int wait_at_end;          // dependency wait in the table builder only (needs build_table)
   int bm;
   int32_t *counts, *offsets, *perm, *inv_perm, *num_tiles;
   TileEntry* tiles;
@@ -49,24 +50,35 @@ cudaError_t launch_tile_table(const int32_t* idx, int Tk, int E, int bm, int32_t
                               int32_t* perm, int32_t* inv_perm, TileEntry* tiles, int32_t* num_tiles,
                               cudaStream_t stream);
 
-// Gather + four-term E2M1 encoding of the activation rows of every tile.
-struct QuantXParams {
+// Four-term E2M1 encoding of every token's activation row, token major.
+struct EncodeXParams {
   const uint16_t* x;       // bf16 [T, H]
-  const int32_t* perm;
-  const TileEntry* tiles;
-  const int32_t* num_tiles;
-  int T, H, k, bm, max_tiles, kg;
-  uint8_t* q;              // [kg][max_tiles][kTerms][bm][64]: four E2M1 terms per row
-  uint8_t* sf;             // [max_tiles][kg][512 * act_sf_atoms(bm)]
+  int T, H;
+  uint8_t* q;              // [kg][T][kTerms][64 bytes]: packed E2M1 codes (low nibble first)
+  uint32_t* sf;            // [kg][T][kTerms]: E8M0 exponents of the 4 MX blocks of a K group
   int32_t* zero_buf;       // GEMM arrival counters to clear (or null)
   int zero_count;
 };
-cudaError_t launch_quant_x(const QuantXParams& p, cudaStream_t stream);
+cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream);
+
+// The permute step: encoded x rows copied from token order into the tile order of
+// the gate/up GEMM's B operand.
+struct GatherXParams {
+  const uint8_t* xt_q;     // [kg][T][kTerms][64 bytes] (EncodeXParams::q)
+  const uint32_t* xt_sf;   // [kg][T][kTerms]
+  const int32_t* perm;
+  const TileEntry* tiles;
+  const int32_t* num_tiles;
+  int T, k, bm, max_tiles, kg;
+  uint8_t* q;              // [kg][max_tiles][kTerms][bm][64 bytes]
+  uint8_t* sf;             // [max_tiles][kg][512 * act_sf_atoms(bm)]
+};
+cudaError_t launch_gather_x(const GatherXParams& p, cudaStream_t stream);
 
 struct GemmParams {
   // operand tensor maps (TMA)
   CUtensorMap tm_w;        // weights: packed E2M1 [E*groups][KG][rows][64 B]
-  CUtensorMap tm_act;      // activations: packed E2M1 terms [KG][max_tiles*kTerms*bm][64 B]
+  CUtensorMap tm_act;      // activations (x gathered, or h): packed E2M1 terms [KG][max_tiles*kTerms*bm][64 B]
   const uint8_t* w_sf;     // weight scale atoms [E][groups][mt][kg][512]
   const uint8_t* act_sf;   // activation scale atoms [max_tiles][kg][512 * act_sf_atoms]
   const TileEntry* tiles;

@@ -25,6 +25,7 @@ namespace {
 constexpr int kRouteThreads = 256;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kTokensPerGroup = 8;
+constexpr int kStageVecs = 12;   // 16-byte activation loads in flight per thread
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
@@ -198,56 +199,80 @@ __device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k
   }
 }
 
-// grid = (token groups of 8, expert slices); block = 256 threads.
+// grid = (token groups of 8, expert slices); block = 256 threads.  kRouterVecs:
+// 16-byte router-weight loads in flight per lane (more for few tokens, where the
+// loads' latency dominates; fewer for many, where registers bound the occupancy).
+template <int kRouterVecs>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   extern __shared__ __align__(16) uint8_t route_smem[];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // the previous kernel on the stream may still read this call's outputs
-  pdl_wait();
+  // The previous kernel on the stream may still read this call's outputs: wait for
+  // it first -- unless the launch before this one (the activation encoding of the
+  // same call) already waited for everything earlier; then only the table builder
+  // waits, at the end, so that this launch completes after that one.
+  if (!p.wait_at_end) pdl_wait();
   pdl_launch_dependents();
   const int g = blockIdx.x;
   const int t0 = g * kTokensPerGroup;
   const int nt = min(kTokensPerGroup, p.T - t0);
   if (!p.from_logits) {
-    // stage the group's activations in shared memory (16-byte vectors)
-    uint4* xs = reinterpret_cast<uint4*>(route_smem);
     const int vec_per_row = p.H / 8;
-    // rows of one group are contiguous in x: issue four loads per thread at a time
+    const int e_begin = blockIdx.y * p.experts_per_block;
+    const int e_end = min(p.E, e_begin + p.experts_per_block);
+    // the first chunk of this warp's router weights is requested before the
+    // activations are staged, so both latencies overlap
+    const int e_first = e_begin + warp;
+    uint4 wpre[kRouterVecs];
+    if (e_first < e_end) {
+      const uint4* wr = reinterpret_cast<const uint4*>(p.w_router + (size_t)e_first * p.H);
+#pragma unroll
+      for (int u = 0; u < kRouterVecs; ++u) {
+        const int c = lane + 32 * u;
+        wpre[u] = c < vec_per_row ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+      }
+    }
+    // stage the group's activations in shared memory (16-byte vectors); rows of one
+    // group are contiguous in x
+    uint4* xs = reinterpret_cast<uint4*>(route_smem);
     const uint4* xg = reinterpret_cast<const uint4*>(p.x + (size_t)t0 * p.H);
     const int nx = nt * vec_per_row;
-    for (int i0 = tid; i0 < nx; i0 += 4 * kRouteThreads) {
-      uint4 v[4];
+    for (int i0 = tid; i0 < nx; i0 += kStageVecs * kRouteThreads) {
+      uint4 v[kStageVecs];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kStageVecs; ++u) {
         const int i = i0 + u * kRouteThreads;
         v[u] = i < nx ? __ldg(xg + i) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kStageVecs; ++u) {
         const int i = i0 + u * kRouteThreads;
         if (i < nx) xs[i] = v[u];
       }
     }
     __syncthreads();
-    const int e_begin = blockIdx.y * p.experts_per_block;
-    const int e_end = min(p.E, e_begin + p.experts_per_block);
-    for (int e = e_begin + warp; e < e_end; e += kRouteWarps) {
+    for (int e = e_first; e < e_end; e += kRouteWarps) {
       float acc[kTokensPerGroup];
 #pragma unroll
       for (int r = 0; r < kTokensPerGroup; ++r) acc[r] = 0.f;
       const uint4* wr = reinterpret_cast<const uint4*>(p.w_router + (size_t)e * p.H);
-      // four router-weight loads in flight per lane, then their FMAs in a fixed order
-      for (int c0 = lane; c0 < vec_per_row; c0 += 128) {
-        uint4 wv4[4];
+      // kRouterVecs router-weight loads in flight per lane, then their FMAs in a
+      // fixed order (per lane: ascending vector index)
+      for (int c0 = 0; c0 < vec_per_row; c0 += 32 * kRouterVecs) {
+        uint4 wv4[kRouterVecs];
+        if (e == e_first && c0 == 0) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = c0 + 32 * u;
-          wv4[u] = c < vec_per_row ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+          for (int u = 0; u < kRouterVecs; ++u) wv4[u] = wpre[u];
+        } else {
+#pragma unroll
+          for (int u = 0; u < kRouterVecs; ++u) {
+            const int c = c0 + lane + 32 * u;
+            wv4[u] = c < vec_per_row ? __ldg(wr + c) : make_uint4(0, 0, 0, 0);
+          }
         }
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = c0 + 32 * u;
+        for (int u = 0; u < kRouterVecs; ++u) {
+          const int c = c0 + lane + 32 * u;
           if (c >= vec_per_row) break;
           const uint4 wv = wv4[u];
           const float w0 = bf16_lo(wv.x), w1 = bf16_hi(wv.x), w2 = bf16_lo(wv.y), w3 = bf16_hi(wv.y);
@@ -302,14 +327,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   if (!p.build_table) return;
   __threadfence();
   __syncthreads();
-  if (tid == 0) {
-    const unsigned old = atomicAdd(p.sync + gridDim.x, 1u);
-    s_last = (old == gridDim.x - 1) ? 1 : 0;
-    if (s_last) p.sync[gridDim.x] = 0;
+  if (gridDim.x > 1) {
+    // the last token group to finish builds the table
+    if (tid == 0) {
+      const unsigned old = atomicAdd(p.sync + gridDim.x, 1u);
+      s_last = (old == gridDim.x - 1) ? 1 : 0;
+      if (s_last) p.sync[gridDim.x] = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  if (p.wait_at_end) pdl_wait();
   build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
                          p.num_tiles, p.status);
 }
@@ -332,11 +361,13 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || configured_smem[dev] < (int)smem) {
-    e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(route_kernel<12>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(route_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured_smem[dev] = (int)smem;
   }
-  return launch_pdl(route_kernel, grid, dim3(kRouteThreads), smem, stream, p);
+  if (p.T <= 64) return launch_pdl(route_kernel<12>, grid, dim3(kRouteThreads), smem, stream, p);
+  return launch_pdl(route_kernel<4>, grid, dim3(kRouteThreads), smem, stream, p);
 }
 
 cudaError_t launch_tile_table(const int32_t* idx, int Tk, int E, int bm, int32_t* counts, int32_t* offsets,

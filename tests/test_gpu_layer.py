@@ -179,3 +179,29 @@ def test_layer_is_bit_reproducible():
     b = layer(x).clone()
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["gptoss20b_b1", "gptoss20b_b64"])
+def test_consecutive_calls_with_new_routing(name):
+    """Calls back to back on one workspace with different tokens (so a different
+    routing and tile table each time) each match the oracle: no launch may read a
+    routing result, an encoded row or a counter left over from the call before."""
+    import dataclasses
+    import torch
+    from synthetic.gen import bf16_bits_from_f32
+    base = make_config(name)
+    layer = build_layer(base)
+    outs, inps = [], []
+    for s in range(4):
+        rng = np.random.default_rng(100 + s)
+        x = bf16_bits_from_f32(rng.standard_normal((base.T, base.H), dtype=np.float32))
+        inp = dataclasses.replace(base, x=x)
+        inps.append(inp)
+        outs.append(layer(to_dev(x)).clone())
+    torch.cuda.synchronize()
+    assert layer.device_status(base.T) == 0
+    for inp, out in zip(inps, outs):
+        ref = oracle.moe_layer(inp)
+        keep = oracle.topk_margin(ref["logits"], inp.k) > 1e-4
+        rel, mx = errors(bf16_bits_to_f32(bf16_to_np(out))[keep], ref["out"][keep])
+        assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)

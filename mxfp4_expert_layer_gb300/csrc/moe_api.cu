@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -121,13 +122,20 @@ bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P)
 
 // Encoded activations {64 bytes, max_tiles * kTerms * bm rows, KG}: one tile's
 // kTerms * bm rows of a K group are contiguous (boxes of at most 256 rows).
-bool act_map(CUtensorMap* out, const void* base, int K, int max_tiles, int bm) {
+// Token-major tiles (at most 16 rows) get kActBoxes maps whose boxes hold the rows of
+// 1, 2, 4, 8 or 16 tokens, so a stage loads only its tile's real tokens.
+bool act_map(CUtensorMap (&out)[kActBoxes], const void* base, int K, int max_tiles, int bm) {
   const cuuint64_t rows = (cuuint64_t)max_tiles * kTerms * bm;
   cuuint64_t dims[3] = {64, rows, (cuuint64_t)ceil_div(K, kKGroup)};
   cuuint64_t strides[2] = {64, 64 * rows};
-  const int box_rows = kTerms * bm < 256 ? kTerms * bm : 256;
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  return make_map(out, base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+  for (int q = 0; q < kActBoxes; ++q) {
+    int box_rows = kTerms * bm < 256 ? kTerms * bm : 256;
+    if (act_token_major(bm)) box_rows = min(kTerms << q, kTerms * bm);
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    if (!make_map(&out[q], base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+      return false;
+  }
+  return true;
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -188,7 +196,7 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   const PreparedLayout P = make_prepared_layout(E, 2 * I, H, 2);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_gateup, P)) return MOE_ERR_CUDA;
-  if (!act_map(&g.tm_act, gx.q, H, L.max_tiles, bm)) return MOE_ERR_CUDA;
+  if (!act_map(g.tm_act, gx.q, H, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_gateup) + P.scales_off;
   g.act_sf = gx.sf;
   g.tiles = tiles;
@@ -200,6 +208,7 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   g.mt = L.mt_i;
   g.rows_out = I;
   g.w_groups = 2;
+  g.w_mt = P.mt;
   g.group_tiles = bm >= 128 ? 32 : (bm >= 64 ? 16 : 1);
   g.h_q = ws_ptr<uint8_t>(ws, L.h_q);
   g.h_sf = ws_ptr<uint8_t>(ws, L.h_sf);
@@ -217,7 +226,7 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   const PreparedLayout P = make_prepared_layout(E, H, I, 1);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_down, P)) return MOE_ERR_CUDA;
-  if (!act_map(&g.tm_act, ws_ptr<uint8_t>(ws, L.h_q), I, L.max_tiles, bm)) return MOE_ERR_CUDA;
+  if (!act_map(g.tm_act, ws_ptr<uint8_t>(ws, L.h_q), I, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_down) + P.scales_off;
   g.act_sf = ws_ptr<uint8_t>(ws, L.h_sf);
   g.tiles = tiles;
@@ -226,7 +235,10 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k; g.bm = bm; g.max_tiles = L.max_tiles;
   g.K = I;
   g.kg = P.kg;
-  g.mt = L.mt_h;
+  // pairs of M tiles per unit when there are units enough to keep every SM busy
+  g.m_pair = (long long)std::min(E, T * k) * ceil_div(L.mt_h, 2) >= 2LL * persistent_ctas() ? 1 : 0;
+  g.mt = g.m_pair ? ceil_div(L.mt_h, 2) : L.mt_h;
+  g.w_mt = P.mt;
   g.rows_out = H;
   g.w_groups = 1;
   g.group_tiles = bm >= 128 ? 32 : (bm >= 64 ? 16 : 1);

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kAuxThreads) gather_x_kernel(GatherXParams p) 
     uint4* dst = reinterpret_cast<uint4*>(p.q + act_offset(tile, t, r, kg * kKGroup, p.max_tiles, p.bm));
 #pragma unroll
     for (int j = 0; j < 4; ++j) dst[j] = v[t * 4 + j];
-    *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(t * p.bm + r, 0)) = ew[t];
+    *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(t, r, p.bm), 0)) = ew[t];
   }
 }
 
@@ -234,7 +234,7 @@ cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream) {
 
 // out[a][i] = sum_t e2m1(q_t) * 2^(s_t - 127) for every valid tile row.
 __global__ void hidden_dequant_kernel(HiddenDequantParams p) {
-  const int num_tiles = __ldg(p.num_tiles);
+  const int num_tiles = __ldcg(p.num_tiles);
   const long long total = (long long)num_tiles * p.bm * p.I;
   const int natoms = act_sf_atoms(p.bm);
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -243,15 +243,15 @@ __global__ void hidden_dequant_kernel(HiddenDequantParams p) {
     const int f = (int)(i - row * p.I);
     const int tile = (int)(row / p.bm);
     const int r = (int)(row - (long long)tile * p.bm);
-    const TileEntry te = p.tiles[tile];
+    const TileEntry te = load_tile(p.tiles + tile);
     if (r >= te.n_rows) continue;
-    const int a = p.perm[te.row_begin + r];
+    const int a = __ldcg(p.perm + te.row_begin + r);
     float v = 0.f;
     for (int t = 0; t < kTerms; ++t) {
       const uint8_t byte = p.h_q[act_offset(tile, t, r, f & ~1, p.max_tiles, p.bm)];
       const uint32_t code = (f & 1) ? (byte >> 4) : (byte & 15u);
       const size_t off = ((size_t)tile * p.kg + (f >> 7)) * (kSfAtomBytes * natoms) +
-                         sf_atom_offset(t * p.bm + r, (f >> 5) & 3);
+                         sf_atom_offset(act_row(t, r, p.bm), (f >> 5) & 3);
       v += e2m1_to_f32(code) * pow2_int((int)p.sf[off] - 127);
     }
     p.out[(size_t)a * p.I + f] = v;

@@ -21,6 +21,7 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxCtas = 160;        // persistent GEMM CTAs (one per SM; GB300 has 152)
 constexpr int kTerms = 4;            // E2M1 terms of the activation encoding
+constexpr int kActBoxes = 5;         // B box heights 4 x {1, 2, 4, 8, 16} rows for 16-row tiles
 
 // Device status word bits (read back with moe_get_device_status).
 constexpr uint32_t kStatusTimeoutMain = 1u << 0;
@@ -227,10 +228,18 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
   return (code & 8u) ? -mag : mag;
 }
 
+// Row of (term t, token row r) inside an activation tile's B operand.  Tiles of at
+// most 16 token rows (all terms in one MMA along N) are token major, so the rows of
+// the tile's real tokens come first and one TMA box of 4 x (tokens rounded up to a
+// power of two) rows covers them; larger tiles are term major (one MMA per term).
+__host__ __device__ inline bool act_token_major(int bm) { return kTerms * bm <= 64; }
+__host__ __device__ inline int act_row(int t, int r, int bm) {
+  return act_token_major(bm) ? r * kTerms + t : t * bm + r;
+}
 // Byte offset of the code byte holding values (k, k+1) (k even) of term t of row r
-// of tile `tile` in an encoded activation buffer [KG][max_tiles][kTerms][bm][64].
+// of tile `tile` in an encoded activation buffer [KG][max_tiles][kTerms * bm rows][64].
 __host__ __device__ inline size_t act_offset(int tile, int t, int r, int k, int max_tiles, int bm) {
-  return ((((size_t)(k >> 7) * max_tiles + tile) * kTerms + t) * bm + r) * 64 + ((k & 127) >> 1);
+  return (((size_t)(k >> 7) * max_tiles + tile) * (kTerms * bm) + act_row(t, r, bm)) * 64 + ((k & 127) >> 1);
 }
 
 // Scale atom byte offset of (row r within a tile, MX block b within a K group).

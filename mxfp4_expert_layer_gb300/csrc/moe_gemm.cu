@@ -40,9 +40,11 @@ constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitLimit = 1000000000ull;  // ns a bounded mbarrier wait may take (1 s)
 constexpr int kATileBytes = kMTile * 64;         // one 128-row x 128-code weight tile, packed
 
-template <int BM, bool GATEUP>
+// MPAIR (down only): two neighbouring 128-row M tiles per work unit, sharing each
+// stage's B tile, so a stage carries twice the weight bytes per activation byte.
+template <int BM, bool GATEUP, bool MPAIR>
 struct GemmCfg {
-  static constexpr int kA = GATEUP ? 2 : 1;                  // weight tiles per stage (gate, up)
+  static constexpr int kA = (GATEUP || MPAIR) ? 2 : 1;       // weight tiles per stage (gate/up, or 2 M tiles)
   static constexpr bool kConcat = kTerms * BM <= 64;         // all terms in one MMA along N
   static constexpr int kN = kConcat ? kTerms * BM : BM;      // MMA N
   static constexpr int kAccN = kN;                           // accumulator columns per weight tile
@@ -61,7 +63,8 @@ struct GemmCfg {
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kBarBytes = 2048;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
-  static constexpr uint32_t kTxBytes = kA * kATileBytes + kBBytes + kSfBytes;
+  static constexpr uint32_t kTxBytes = kA * kATileBytes + kBBytes + kSfBytes;  // full B box
+  static constexpr uint32_t kTxNoB = kA * kATileBytes + kSfBytes;                // all but the B codes
   static constexpr int kSfColsPerStage = 4 * (kA + kNbAtoms);
   static constexpr int kSfCols = kStages * kSfColsPerStage;
   static constexpr int kNumAcc = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
@@ -160,9 +163,9 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 
 }  // namespace
 
-template <int BM, bool GATEUP>
+template <int BM, bool GATEUP, bool MPAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<BM, GATEUP>;
+  using C = GemmCfg<BM, GATEUP, MPAIR>;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -194,7 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tm_w);
-    tma_prefetch_desc(&p.tm_act);
+    for (int q = 0; q < (C::kConcat ? kActBoxes : 1); ++q) tma_prefetch_desc(&p.tm_act[q]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -232,33 +235,47 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const size_t wsf_group_stride = (size_t)p.mt * KG * kSfAtomBytes;
       // iterator over this CTA's (segment, K group) iterations
-      int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0;
-      const uint8_t* wsf_base = nullptr;
+      int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0, boxq = 0;
       auto open_seg = [&]() {
         int u, kk0;
         bool whole;
         sch.seg(si, u, kk0, kk1, whole);
         kk = kk0;
         map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
-        expert = __ldcg(&p.tiles[tile].expert);
-        wsf_base = p.w_sf + ((size_t)expert * p.w_groups * p.mt + mt) * (size_t)KG * kSfAtomBytes;
+        const TileEntry te = load_tile(p.tiles + tile);
+        expert = te.expert;
+        // token-major tiles: the smallest box (4 x 2^q rows) holding the real tokens
+        boxq = 0;
+        while ((1 << boxq) < te.n_rows && boxq < kActBoxes - 1) ++boxq;
       };
       auto advance = [&]() {
         if (++kk == kk1 && ++si < sch.nseg) open_seg();
       };
+      // bytes the stage's barrier expects for the current tile
+      auto tx_bytes = [&]() -> uint32_t {
+        return C::kConcat ? C::kTxNoB + (uint32_t)(kTerms << boxq) * 64u : C::kTxBytes;
+      };
       auto load_a = [&](int s) {
         for (int j = 0; j < C::kA; ++j) {
-          tma_load_4d(a_tile(s, j), &p.tm_w, &full_bar[s], 0, mt * kMTile, kk, expert * p.w_groups + j);
-          bulk_load(sf_a(s, j), wsf_base + j * wsf_group_stride + (size_t)kk * kSfAtomBytes, kSfAtomBytes,
-                    &full_bar[s]);
+          // gate/up: group j of M tile mt; down: M tile mt (or 2 mt + j), group 0.  An M
+          // tile past the matrix reads zeros (TMA fill) and scales of the last tile.
+          const int mrow = GATEUP ? mt : (MPAIR ? 2 * mt + j : mt);
+          const int grp = GATEUP ? j : 0;
+          tma_load_4d(a_tile(s, j), &p.tm_w, &full_bar[s], 0, mrow * kMTile, kk, expert * p.w_groups + grp);
+          const int msf = min(mrow, p.w_mt - 1);
+          const uint8_t* wsf = p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)KG * kSfAtomBytes;
+          bulk_load(sf_a(s, j), wsf + (size_t)kk * kSfAtomBytes, kSfAtomBytes, &full_bar[s]);
         }
       };
-      auto load_b = [&](int s, int b_tile_idx, int b_kk) {
-        for (int bx = 0; bx < C::kBRows / C::kBBoxRows; ++bx)
-          tma_load_3d(b_tile(s) + bx * C::kBBoxRows * 64, &p.tm_act, &full_bar[s], 0,
-                      b_tile_idx * C::kBRows + bx * C::kBBoxRows, b_kk);
+      auto load_b = [&](int s, int b_tile_idx, int b_kk, int q) {
+        if constexpr (C::kConcat) {
+          tma_load_3d(b_tile(s), &p.tm_act[q], &full_bar[s], 0, b_tile_idx * C::kBRows, b_kk);
+        } else {
+          for (int bx = 0; bx < C::kBRows / C::kBBoxRows; ++bx)
+            tma_load_3d(b_tile(s) + bx * C::kBBoxRows * 64, &p.tm_act[0], &full_bar[s], 0,
+                        b_tile_idx * C::kBRows + bx * C::kBBoxRows, b_kk);
+        }
         bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * KG + b_kk) * (kSfAtomBytes * C::kNbAtoms),
                   kSfAtomBytes * C::kNbAtoms, &full_bar[s]);
       };
@@ -268,18 +285,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         open_seg();
         // weights of the first stages depend only on the routing: stream them while
         // the previous kernel finishes
-        int pre_tile[C::kStages], pre_kk[C::kStages];
+        int pre_tile[C::kStages], pre_kk[C::kStages], pre_q[C::kStages];
         int npre = 0;
         while (npre < C::kStages && si < sch.nseg) {
-          mbar_arrive_expect_tx(&full_bar[npre], C::kTxBytes);  // fresh stages: no wait
+          mbar_arrive_expect_tx(&full_bar[npre], tx_bytes());  // fresh stages: no wait
           load_a(npre);
           pre_tile[npre] = tile;
           pre_kk[npre] = kk;
+          pre_q[npre] = boxq;
           ++npre;
           advance();
         }
         pdl_wait();
-        for (int i = 0; i < npre; ++i) load_b(i, pre_tile[i], pre_kk[i]);
+        for (int i = 0; i < npre; ++i) load_b(i, pre_tile[i], pre_kk[i], pre_q[i]);
         g = npre;
         for (; si < sch.nseg; ++g) {
           const int s = g % C::kStages;
@@ -290,9 +308,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             err = true;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[s], C::kTxBytes);
+          mbar_arrive_expect_tx(&full_bar[s], tx_bytes());
           load_a(s);
-          load_b(s, tile, kk);
+          load_b(s, tile, kk, boxq);
           advance();
         }
       } else {
@@ -460,17 +478,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
               if (feat0 < i_pad)
                 *reinterpret_cast<uint2*>(p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM)) =
                     make_uint2(w[0], w[1]);
-              if ((et & 7) == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(t * BM + r, 0)) = word;
+              if ((et & 7) == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(t, r, BM), 0)) = word;
             }
           }
           epi_bar();  // s_xpose reused by the next chunk
         } else {
-          (void)vb;
-          if (feat < p.H) {
+          // output features: M tile mt, or the pair 2 mt, 2 mt + 1 (va, vb)
+          const int fa = (MPAIR ? 2 * mt : mt) * kMTile + m;
+          const int fb = fa + kMTile;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int r = c0 + j;
-              if (r < nrows) p.slots[(size_t)s_rowa[r] * p.H + feat] = s_roww[r] * va[j];
+          for (int j = 0; j < 16; ++j) {
+            const int r = c0 + j;
+            if (r < nrows) {
+              float* slot = p.slots + (size_t)s_rowa[r] * p.H;
+              if (fa < p.H) slot[fa] = s_roww[r] * va[j];
+              if (MPAIR && fb < p.H) slot[fb] = s_roww[r] * vb[j];
             }
           }
         }
@@ -511,16 +533,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         tmem_wait_ld();
         tc_fence_before();
         mbar_arrive(&acce_bar[b]);
-        // values: add the term column groups when the terms share one MMA
+        // values: add the term columns when the terms share one MMA (token-major
+        // columns: token c's terms are columns 4c .. 4c + 3)
         float vals[C::kVals];
 #pragma unroll
         for (int j = 0; j < C::kA; ++j)
 #pragma unroll
           for (int c = 0; c < BM; ++c) {
-            float v = acc[j * C::kAccN + c];
+            float v;
             if constexpr (C::kConcat) {
+              v = acc[j * C::kAccN + kTerms * c];
 #pragma unroll
-              for (int t = 1; t < kTerms; ++t) v += acc[j * C::kAccN + t * BM + c];
+              for (int t = 1; t < kTerms; ++t) v += acc[j * C::kAccN + kTerms * c + t];
+            } else {
+              v = acc[j * C::kAccN + c];
             }
             vals[j * BM + c] = v;
           }
@@ -563,7 +589,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         if (finished) {
 #pragma unroll
           for (int c0 = 0; c0 < BM; c0 += 16)
-            if (c0 < nrows) consume(c0, vals + c0, GATEUP ? vals + BM + c0 : nullptr);
+            if (c0 < nrows) consume(c0, vals + c0, C::kA > 1 ? vals + BM + c0 : nullptr);
         }
       } else {
         // accumulator too large for registers (per-term MMAs): 16 columns at a time
@@ -626,10 +652,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int BM, bool GATEUP>
+template <int BM, bool GATEUP, bool MPAIR>
 static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
-  using C = GemmCfg<BM, GATEUP>;
-  auto kern = moe_gemm_kernel<BM, GATEUP>;
+  using C = GemmCfg<BM, GATEUP, MPAIR>;
+  auto kern = moe_gemm_kernel<BM, GATEUP, MPAIR>;
   // the shared-memory opt-in is a per-device function attribute: set it once per device
   static bool configured[64] = {};
   int dev = 0;
@@ -643,17 +669,19 @@ static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
   return launch_pdl(kern, dim3(p.grid), dim3(kGemmThreads), C::kSmemBytes, stream, p);
 }
 
-template <bool GATEUP>
+template <bool GATEUP, bool MPAIR>
 static cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream) {
   switch (p.bm) {
-    case 16: return launch_gemm_t<16, GATEUP>(p, stream);
-    case 64: return launch_gemm_t<64, GATEUP>(p, stream);
-    case 128: return launch_gemm_t<128, GATEUP>(p, stream);
+    case 16: return launch_gemm_t<16, GATEUP, MPAIR>(p, stream);
+    case 64: return launch_gemm_t<64, GATEUP, MPAIR>(p, stream);
+    case 128: return launch_gemm_t<128, GATEUP, MPAIR>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream) { return launch_gemm<true>(p, stream); }
-cudaError_t launch_down(const GemmParams& p, cudaStream_t stream) { return launch_gemm<false>(p, stream); }
+cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream) { return launch_gemm<true, false>(p, stream); }
+cudaError_t launch_down(const GemmParams& p, cudaStream_t stream) {
+  return p.m_pair ? launch_gemm<false, true>(p, stream) : launch_gemm<false, false>(p, stream);
+}
 
 }  // namespace moe

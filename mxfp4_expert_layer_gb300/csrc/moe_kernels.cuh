@@ -78,7 +78,9 @@ cudaError_t launch_gather_x(const GatherXParams& p, cudaStream_t stream);
 struct GemmParams {
   // operand tensor maps (TMA)
   CUtensorMap tm_w;        // weights: packed E2M1 [E*groups][KG][rows][64 B]
-  CUtensorMap tm_act;      // activations (x gathered, or h): packed E2M1 terms [KG][max_tiles*kTerms*bm][64 B]
+  // activations (x gathered, or h): packed E2M1 terms [KG][max_tiles*kTerms*bm][64 B];
+  // tiles of at most 16 rows use box q = 4 * 2^q rows (q < kActBoxes), others box 0
+  CUtensorMap tm_act[kActBoxes];
   const uint8_t* w_sf;     // weight scale atoms [E][groups][mt][kg][512]
   const uint8_t* act_sf;   // activation scale atoms [max_tiles][kg][512 * act_sf_atoms]
   const TileEntry* tiles;
@@ -87,9 +89,11 @@ struct GemmParams {
   int T, H, I, E, k, bm, max_tiles;
   int K;                   // contraction length (H for gate/up, I for down)
   int kg;                  // K groups of 128
-  int mt;                  // M tiles of the output features
+  int mt;                  // M units of the output features (M tiles, or pairs of them)
   int rows_out;            // output features (I for gate/up, H for down)
   int w_groups;            // 2 (gate, up) or 1 (down)
+  int w_mt;                // 128-row M tiles per group of the prepared weights
+  int m_pair;              // down: a unit covers the M tiles 2 mt and 2 mt + 1
   int group_tiles;         // tiles per raster group
   // gate/up epilogue outputs (four-term E2M1 h)
   uint8_t *h_q, *h_sf;

@@ -7,14 +7,18 @@
 // kernel searching a tiles x experts grid); "triton-kernels" README, section
 // "Quick Start" (softmax gating + top-k, expert indices and weights returned).
 //
-// One launch does all three steps: blocks of (8 tokens x a slice of experts)
-// compute logits; the last block to finish a token group (an integer arrival
-// count, no spinning) selects the top-k of those tokens; the last token group to
-// finish builds the tile table.  Every result is computed by one fixed thread or
+// One launch does all three steps.  Many tokens: blocks of (8 tokens x a slice of
+// experts) compute logits; the last block to finish a token group (an integer
+// arrival count, no spinning) selects the top-k of those tokens; the last token
+// group to finish builds the tile table.  Few tokens (decode): one thread-block
+// cluster splits the hidden dimension, exchanges partial logits through
+// distributed shared memory and needs no global atomics.  Every result is computed by one fixed thread or
 // warp in a fixed order, so the outputs are bit-reproducible run to run.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
 #include "sm100_ptx.cuh"
+
+#include <cooperative_groups.h>
 
 namespace moe {
 
@@ -149,13 +153,15 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
 
 // Top-k of one token by one warp: each lane holds logits e = lane + 32*i; k rounds
 // of a warp arg-max on (value desc, index asc).  Softmax over the k selected.
+// kShared: the logits row is in shared memory (else global, read through L2).
+template <bool kShared = false>
 __device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out) {
   const int lane = threadIdx.x & 31;
   float v[kMaxExperts / 32];
 #pragma unroll
   for (int i = 0; i < kMaxExperts / 32; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldcg(lg_row + e) : -INFINITY;
+    v[i] = (e < E) ? (kShared ? lg_row[e] : __ldcg(lg_row + e)) : -INFINITY;
   }
   unsigned taken = 0;  // bit i: element e = lane + 32*i already selected
   float sel_v[kMaxTopK];
@@ -343,6 +349,156 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
                          p.num_tiles, p.status);
 }
 
+// ------------------------------------------------------------------ decode routing
+// Few tokens (T <= 64): one cluster of kClusterCtas CTAs does the whole routing with
+// no global atomics.  CTA r computes the partial logits of every token and expert
+// over its slice of the hidden dimension on the tensor cores (mma.sync bf16, fp32
+// accumulate); after a cluster barrier CTA r sums the kClusterCtas partials of
+// tokens 8r..8r+7 in rank order (reading its peers' shared memory), selects their
+// top-k, and after a second barrier CTA 0 builds the tile table.
+constexpr int kClusterCtas = 8;
+constexpr int kClusterMaxTokens = kClusterCtas * kTokensPerGroup;
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t (&r)[2], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// Shared-memory layout of the cluster routing kernel for (T, H, E).
+struct ClusterRouteSmem {
+  int mrows, erows, pitch;        // staged x rows (multiple of 16), router rows (multiple of 8), row bytes
+  size_t x_off, w_off, part_off, lg_off, total;
+};
+__host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int E) {
+  ClusterRouteSmem L;
+  const int ksteps = H / 16;
+  const int kmax = ((ksteps + kClusterCtas - 1) / kClusterCtas) * 16;  // largest slice, elements
+  L.mrows = ((T + 15) / 16) * 16;
+  L.erows = ((E + 7) / 8) * 8;
+  L.pitch = kmax * 2 + 16;  // +16 bytes: rows fall in different banks for ldmatrix
+  L.x_off = 0;
+  L.w_off = L.x_off + (size_t)L.mrows * L.pitch;
+  L.part_off = L.w_off + (size_t)L.erows * L.pitch;
+  L.lg_off = L.part_off + sizeof(float) * (size_t)L.mrows * L.erows;
+  L.total = L.lg_off + sizeof(float) * (size_t)kTokensPerGroup * L.erows;
+  return L;
+}
+
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThreads)
+    route_cluster_kernel(RouteParams p) {
+  extern __shared__ __align__(16) uint8_t rc_smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!p.wait_at_end) pdl_wait();
+  pdl_launch_dependents();
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E);
+  uint8_t* xs = rc_smem + L.x_off;
+  uint8_t* wsm = rc_smem + L.w_off;
+  float* part = reinterpret_cast<float*>(rc_smem + L.part_off);  // [mrows][erows]
+  float* lg = reinterpret_cast<float*>(rc_smem + L.lg_off);      // [8][erows]
+
+  // this CTA's slice of the hidden dimension, in steps of 16
+  const int ksteps = p.H / 16;
+  const int ks0 = rank * ksteps / kClusterCtas, ks1 = (rank + 1) * ksteps / kClusterCtas;
+  const int nvec = (ks1 - ks0) * 2;  // 16-byte vectors per row slice
+  // stage x rows (zeros past T) and router rows (zeros past E), all loads in flight
+  {
+    const int nx = L.mrows * nvec, nw = L.erows * nvec, ntot = nx + nw;
+    for (int i0 = tid; i0 < ntot; i0 += kStageVecs * kRouteThreads) {
+      uint4 v[kStageVecs];
+#pragma unroll
+      for (int u = 0; u < kStageVecs; ++u) {
+        const int i = i0 + u * kRouteThreads;
+        v[u] = make_uint4(0, 0, 0, 0);
+        if (i < nx) {
+          const int r = i / nvec, c = i - r * nvec;
+          if (r < p.T) v[u] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)r * p.H + ks0 * 16) + c);
+        } else if (i < ntot) {
+          const int r = (i - nx) / nvec, c = (i - nx) - r * nvec;
+          if (r < p.E) v[u] = __ldg(reinterpret_cast<const uint4*>(p.w_router + (size_t)r * p.H + ks0 * 16) + c);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kStageVecs; ++u) {
+        const int i = i0 + u * kRouteThreads;
+        if (i < nx) {
+          const int r = i / nvec, c = i - r * nvec;
+          *reinterpret_cast<uint4*>(xs + (size_t)r * L.pitch + c * 16) = v[u];
+        } else if (i < ntot) {
+          const int r = (i - nx) / nvec, c = (i - nx) - r * nvec;
+          *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = v[u];
+        }
+      }
+    }
+  }
+  __syncthreads();
+  // partial logits: (16-token, 8-expert) output tiles dealt to the warps
+  {
+    const int ntn = L.erows / 8, npairs = (L.mrows / 16) * ntn;
+    const uint32_t xs_u = smem_u32(xs), ws_u = smem_u32(wsm);
+    for (int pi = warp; pi < npairs; pi += kRouteWarps) {
+      const int mi = pi / ntn, ni = pi - mi * ntn;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      // ldmatrix row addresses: A rows mi*16 + lane%16, column half lane/16; B rows
+      // ni*8 + lane%8, column half (lane/8)%2
+      const uint32_t a_addr = xs_u + (uint32_t)((mi * 16 + (lane & 15)) * L.pitch + (lane >> 4) * 16);
+      const uint32_t b_addr = ws_u + (uint32_t)((ni * 8 + (lane & 7)) * L.pitch + ((lane >> 3) & 1) * 16);
+      for (int kk = 0; kk < ks1 - ks0; ++kk) {
+        uint32_t a[4], b[2];
+        ldmatrix_x4(a, a_addr + kk * 32);
+        ldmatrix_x2(b, b_addr + kk * 32);
+        mma_bf16_16816(c, a, b);
+      }
+      const int r0 = mi * 16 + (lane >> 2), c0 = ni * 8 + (lane & 3) * 2;
+      part[r0 * L.erows + c0] = c[0];
+      part[r0 * L.erows + c0 + 1] = c[1];
+      part[(r0 + 8) * L.erows + c0] = c[2];
+      part[(r0 + 8) * L.erows + c0 + 1] = c[3];
+    }
+  }
+  cluster.sync();  // every CTA's partials are complete and visible in the cluster
+  // logits of tokens 8*rank .. 8*rank+7: partials summed in rank order
+  const int t0 = rank * kTokensPerGroup;
+  for (int i = tid; i < kTokensPerGroup * p.E; i += kRouteThreads) {
+    const int r = i / p.E, e = i - r * p.E, t = t0 + r;
+    if (t < p.T) {
+      float sum = 0.f;
+#pragma unroll
+      for (int b = 0; b < kClusterCtas; ++b) {
+        const float* pb = cluster.map_shared_rank(part, b);
+        sum += pb[t * L.erows + e];
+      }
+      if (p.bias) sum += __ldg(p.bias + e);
+      lg[r * L.erows + e] = sum;
+      p.logits[(size_t)t * p.E + e] = sum;
+    }
+  }
+  __syncthreads();
+  if (warp < kTokensPerGroup && t0 + warp < p.T) {
+    const int t = t0 + warp;
+    topk_softmax_warp<true>(lg + warp * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k, p.topk_w + (size_t)t * p.k);
+  }
+  // every CTA is done reading its peers' shared memory and has written its top-k
+  cluster.sync();
+  if (rank != 0 || !p.build_table) return;
+  if (p.wait_at_end) pdl_wait();
+  build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
+                         p.num_tiles, p.status);
+}
+
 __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t* idx, int Tk, int E, int bm,
                                                                    int32_t* counts, int32_t* offsets, int32_t* perm,
                                                                    int32_t* inv_perm, TileEntry* tiles,
@@ -350,7 +506,37 @@ __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t
   build_tile_table_block(idx, Tk, E, bm, counts, offsets, perm, inv_perm, tiles, num_tiles, nullptr);
 }
 
+// The cluster kernel serves few tokens when its operands fit in shared memory and
+// the device can place one cluster of kClusterCtas CTAs with that much memory.
+static bool use_cluster_route(const RouteParams& p, size_t* smem_out) {
+  if (p.from_logits || p.T > kClusterMaxTokens) return false;
+  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E);
+  if (L.total > 200 * 1024) return false;
+  static int state[64] = {};  // 0 unknown, 1 usable, -1 not
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  if (state[dev] == 0) {
+    state[dev] = -1;
+    if (cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kClusterCtas);
+      cfg.blockDim = dim3(kRouteThreads);
+      cfg.dynamicSmemBytes = 200 * 1024;
+      int clusters = 0;
+      if (cudaOccupancyMaxActiveClusters(&clusters, route_cluster_kernel, &cfg) == cudaSuccess && clusters > 0)
+        state[dev] = 1;
+    }
+    cudaGetLastError();  // a refused query leaves no sticky error
+  }
+  *smem_out = L.total;
+  return state[dev] == 1;
+}
+
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
+  size_t csmem = 0;
+  if (use_cluster_route(p, &csmem))
+    return launch_pdl(route_cluster_kernel, dim3(kClusterCtas), dim3(kRouteThreads), csmem, stream, p);
   const int groups = ceil_div(p.T, kTokensPerGroup);
   dim3 grid(groups, p.from_logits ? 1 : ceil_div(p.E, p.experts_per_block));
   const size_t smem = p.from_logits ? 0 : (size_t)kTokensPerGroup * p.H * sizeof(uint16_t);

@@ -67,7 +67,9 @@ __device__ int block_exclusive_scan_256(int v, int* scratch /* >= 8 ints */, int
 // Deterministic counting sort of the assignments by expert, stable in t*k+j,
 // executed by one block of 256 threads.  Each warp owns a contiguous chunk of
 // assignments and a private histogram row; lanes with equal experts are grouped
-// with __match_any_sync, so no atomics are used anywhere.
+// with __match_any_sync, so no atomics are used anywhere.  kSharedIdx: the top-k
+// indices are in this block's shared memory (else global, read through L2).
+template <bool kSharedIdx = false>
 __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, int E, int bm, int32_t* counts,
                                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, TileEntry* tiles,
                                        int32_t* num_tiles, uint32_t* status) {
@@ -85,7 +87,7 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
     const int a = base + lane;
     int e = -1;
     if (a < a_end) {
-      e = __ldcg(idx + a);
+      e = kSharedIdx ? idx[a] : __ldcg(idx + a);
       if (e < 0 || e >= E) {
         report_status(status, kStatusBadIndex);
         e = -1;
@@ -119,7 +121,7 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
     const int a = base + lane;
     int e = -1;
     if (a < a_end) {
-      e = __ldcg(idx + a);
+      e = kSharedIdx ? idx[a] : __ldcg(idx + a);
       if (e < 0 || e >= E) e = -1;
     }
     const unsigned grp = __match_any_sync(0xffffffffu, e);
@@ -155,7 +157,8 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
 // of a warp arg-max on (value desc, index asc).  Softmax over the k selected.
 // kShared: the logits row is in shared memory (else global, read through L2).
 template <bool kShared = false>
-__device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out) {
+__device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out,
+                                  int32_t* idx_copy = nullptr) {
   const int lane = threadIdx.x & 31;
   float v[kMaxExperts / 32];
 #pragma unroll
@@ -164,8 +167,8 @@ __device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k
     v[i] = (e < E) ? (kShared ? lg_row[e] : __ldcg(lg_row + e)) : -INFINITY;
   }
   unsigned taken = 0;  // bit i: element e = lane + 32*i already selected
-  float sel_v[kMaxTopK];
-  int sel_i[kMaxTopK];
+  float my_v = -INFINITY;  // lane j keeps the j-th selection
+  int my_i = 0;
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
@@ -187,21 +190,21 @@ __device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k
       }
     }
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    sel_v[j] = bv;
-    sel_i[j] = bi;
+    if (lane == j) {
+      my_v = bv;
+      my_i = bi;
+    }
   }
-  if (lane == 0) {
-    const float m = sel_v[0];
-    float ex[kMaxTopK];
-    float s = 0.f;
-    for (int j = 0; j < k; ++j) {
-      ex[j] = expf(sel_v[j] - m);
-      s += ex[j];
-    }
-    for (int j = 0; j < k; ++j) {
-      idx_out[j] = sel_i[j];
-      w_out[j] = ex[j] / s;
-    }
+  // softmax over the k selected: exponentials relative to the largest (selection 0),
+  // summed in selection order by lane 0, one division per selection
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  const float ex = lane < k ? expf(my_v - m) : 0.f;
+  float s = 0.f;
+  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
+  if (lane < k) {
+    idx_out[lane] = my_i;
+    w_out[lane] = ex / s;
+    if (idx_copy) idx_copy[lane] = my_i;
   }
 }
 
@@ -378,9 +381,9 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
 // Shared-memory layout of the cluster routing kernel for (T, H, E).
 struct ClusterRouteSmem {
   int mrows, erows, pitch;        // staged x rows (multiple of 16), router rows (multiple of 8), row bytes
-  size_t x_off, w_off, part_off, lg_off, total;
+  size_t x_off, w_off, part_off, lg_off, idx_off, bar_off, total;
 };
-__host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int E) {
+__host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int E, int k) {
   ClusterRouteSmem L;
   const int ksteps = H / 16;
   const int kmax = ((ksteps + kClusterCtas - 1) / kClusterCtas) * 16;  // largest slice, elements
@@ -391,9 +394,14 @@ __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int
   L.w_off = L.x_off + (size_t)L.mrows * L.pitch;
   L.part_off = L.w_off + (size_t)L.erows * L.pitch;
   L.lg_off = L.part_off + sizeof(float) * (size_t)L.mrows * L.erows;
-  L.total = L.lg_off + sizeof(float) * (size_t)kTokensPerGroup * L.erows;
+  L.idx_off = L.lg_off + sizeof(float) * (size_t)kTokensPerGroup * L.erows;
+  L.bar_off = L.idx_off + ((sizeof(int32_t) * (size_t)T * k + 15) / 16) * 16;
+  L.total = L.bar_off + 16;
   return L;
 }
+
+constexpr uint64_t kRouteWaitLimit = 1000000000ull;  // ns a bounded wait may take (1 s)
+constexpr int kMmaIlp = 4;                            // independent output tiles per warp pass
 
 __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThreads)
     route_cluster_kernel(RouteParams p) {
@@ -404,69 +412,82 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   namespace cg = cooperative_groups;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
-  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E);
+  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k);
   uint8_t* xs = rc_smem + L.x_off;
   uint8_t* wsm = rc_smem + L.w_off;
   float* part = reinterpret_cast<float*>(rc_smem + L.part_off);  // [mrows][erows]
   float* lg = reinterpret_cast<float*>(rc_smem + L.lg_off);      // [8][erows]
+  int32_t* sidx = reinterpret_cast<int32_t*>(rc_smem + L.idx_off);  // [T*k], used in CTA 0
+  uint64_t* bar = reinterpret_cast<uint64_t*>(rc_smem + L.bar_off);
 
   // this CTA's slice of the hidden dimension, in steps of 16
   const int ksteps = p.H / 16;
   const int ks0 = rank * ksteps / kClusterCtas, ks1 = (rank + 1) * ksteps / kClusterCtas;
-  const int nvec = (ks1 - ks0) * 2;  // 16-byte vectors per row slice
-  // stage x rows (zeros past T) and router rows (zeros past E), all loads in flight
-  {
-    const int nx = L.mrows * nvec, nw = L.erows * nvec, ntot = nx + nw;
-    for (int i0 = tid; i0 < ntot; i0 += kStageVecs * kRouteThreads) {
-      uint4 v[kStageVecs];
-#pragma unroll
-      for (int u = 0; u < kStageVecs; ++u) {
-        const int i = i0 + u * kRouteThreads;
-        v[u] = make_uint4(0, 0, 0, 0);
-        if (i < nx) {
-          const int r = i / nvec, c = i - r * nvec;
-          if (r < p.T) v[u] = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)r * p.H + ks0 * 16) + c);
-        } else if (i < ntot) {
-          const int r = (i - nx) / nvec, c = (i - nx) - r * nvec;
-          if (r < p.E) v[u] = __ldg(reinterpret_cast<const uint4*>(p.w_router + (size_t)r * p.H + ks0 * 16) + c);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kStageVecs; ++u) {
-        const int i = i0 + u * kRouteThreads;
-        if (i < nx) {
-          const int r = i / nvec, c = i - r * nvec;
-          *reinterpret_cast<uint4*>(xs + (size_t)r * L.pitch + c * 16) = v[u];
-        } else if (i < ntot) {
-          const int r = (i - nx) / nvec, c = (i - nx) - r * nvec;
-          *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = v[u];
-        }
-      }
-    }
+  const uint32_t slice_bytes = (uint32_t)(ks1 - ks0) * 32;
+  // stage the slices of x rows and router rows with one bulk copy per row; rows past
+  // T (x) or E (router) are zero-filled
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  for (int i = tid; i < (L.mrows - p.T) * (L.pitch / 16); i += kRouteThreads) {
+    const int r = p.T + i / (L.pitch / 16), c = i % (L.pitch / 16);
+    *reinterpret_cast<uint4*>(xs + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
+  }
+  for (int i = tid; i < (L.erows - p.E) * (L.pitch / 16); i += kRouteThreads) {
+    const int r = p.E + i / (L.pitch / 16), c = i % (L.pitch / 16);
+    *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
   }
   __syncthreads();
-  // partial logits: (16-token, 8-expert) output tiles dealt to the warps
+  if (slice_bytes > 0) {
+    if (tid == 0) mbar_arrive_expect_tx(bar, slice_bytes * (uint32_t)(p.T + p.E));
+    for (int r = tid; r < p.T + p.E; r += kRouteThreads) {
+      if (r < p.T)
+        bulk_load(xs + (size_t)r * L.pitch, p.x + (size_t)r * p.H + ks0 * 16, slice_bytes, bar);
+      else
+        bulk_load(wsm + (size_t)(r - p.T) * L.pitch, p.w_router + (size_t)(r - p.T) * p.H + ks0 * 16, slice_bytes,
+                  bar);
+    }
+    if (!mbar_wait_bounded(bar, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
+  }
+  // partial logits: (16-token, 8-expert) output tiles dealt to the warps, kMmaIlp
+  // independent tiles per pass so the tensor-core latencies overlap
   {
     const int ntn = L.erows / 8, npairs = (L.mrows / 16) * ntn;
     const uint32_t xs_u = smem_u32(xs), ws_u = smem_u32(wsm);
-    for (int pi = warp; pi < npairs; pi += kRouteWarps) {
-      const int mi = pi / ntn, ni = pi - mi * ntn;
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
-      // ldmatrix row addresses: A rows mi*16 + lane%16, column half lane/16; B rows
-      // ni*8 + lane%8, column half (lane/8)%2
-      const uint32_t a_addr = xs_u + (uint32_t)((mi * 16 + (lane & 15)) * L.pitch + (lane >> 4) * 16);
-      const uint32_t b_addr = ws_u + (uint32_t)((ni * 8 + (lane & 7)) * L.pitch + ((lane >> 3) & 1) * 16);
-      for (int kk = 0; kk < ks1 - ks0; ++kk) {
-        uint32_t a[4], b[2];
-        ldmatrix_x4(a, a_addr + kk * 32);
-        ldmatrix_x2(b, b_addr + kk * 32);
-        mma_bf16_16816(c, a, b);
+    for (int base = warp; base < npairs; base += kRouteWarps * kMmaIlp) {
+      float c[kMmaIlp][4];
+      uint32_t a_addr[kMmaIlp], b_addr[kMmaIlp];
+#pragma unroll
+      for (int q = 0; q < kMmaIlp; ++q) {
+        const int pi = min(base + q * kRouteWarps, npairs - 1);
+        const int mi = pi / ntn, ni = pi - mi * ntn;
+        // ldmatrix row addresses: A rows mi*16 + lane%16, column half lane/16; B rows
+        // ni*8 + lane%8, column half (lane/8)%2
+        a_addr[q] = xs_u + (uint32_t)((mi * 16 + (lane & 15)) * L.pitch + (lane >> 4) * 16);
+        b_addr[q] = ws_u + (uint32_t)((ni * 8 + (lane & 7)) * L.pitch + ((lane >> 3) & 1) * 16);
+        c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
       }
-      const int r0 = mi * 16 + (lane >> 2), c0 = ni * 8 + (lane & 3) * 2;
-      part[r0 * L.erows + c0] = c[0];
-      part[r0 * L.erows + c0 + 1] = c[1];
-      part[(r0 + 8) * L.erows + c0] = c[2];
-      part[(r0 + 8) * L.erows + c0 + 1] = c[3];
+      for (int kk = 0; kk < ks1 - ks0; ++kk) {
+#pragma unroll
+        for (int q = 0; q < kMmaIlp; ++q) {
+          uint32_t a[4], b[2];
+          ldmatrix_x4(a, a_addr[q] + kk * 32);
+          ldmatrix_x2(b, b_addr[q] + kk * 32);
+          mma_bf16_16816(c[q], a, b);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < kMmaIlp; ++q) {
+        const int pi = base + q * kRouteWarps;
+        if (pi >= npairs) break;
+        const int mi = pi / ntn, ni = pi - mi * ntn;
+        const int r0 = mi * 16 + (lane >> 2), c0 = ni * 8 + (lane & 3) * 2;
+        part[r0 * L.erows + c0] = c[q][0];
+        part[r0 * L.erows + c0 + 1] = c[q][1];
+        part[(r0 + 8) * L.erows + c0] = c[q][2];
+        part[(r0 + 8) * L.erows + c0 + 1] = c[q][3];
+      }
     }
   }
   cluster.sync();  // every CTA's partials are complete and visible in the cluster
@@ -487,16 +508,20 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     }
   }
   __syncthreads();
+  // top-k of one token per warp; the indices also go to CTA 0's shared memory, where
+  // the tile table is built
   if (warp < kTokensPerGroup && t0 + warp < p.T) {
     const int t = t0 + warp;
-    topk_softmax_warp<true>(lg + warp * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k, p.topk_w + (size_t)t * p.k);
+    int32_t* idx_cta0 = cluster.map_shared_rank(sidx, 0) + (size_t)t * p.k;
+    topk_softmax_warp<true>(lg + warp * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k, p.topk_w + (size_t)t * p.k,
+                            p.build_table ? idx_cta0 : nullptr);
   }
-  // every CTA is done reading its peers' shared memory and has written its top-k
+  // every CTA is done with its peers' shared memory and has delivered its top-k
   cluster.sync();
   if (rank != 0 || !p.build_table) return;
   if (p.wait_at_end) pdl_wait();
-  build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                         p.num_tiles, p.status);
+  build_tile_table_block<true>(sidx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
+                               p.num_tiles, p.status);
 }
 
 __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t* idx, int Tk, int E, int bm,
@@ -510,7 +535,7 @@ __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t
 // the device can place one cluster of kClusterCtas CTAs with that much memory.
 static bool use_cluster_route(const RouteParams& p, size_t* smem_out) {
   if (p.from_logits || p.T > kClusterMaxTokens) return false;
-  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E);
+  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k);
   if (L.total > 200 * 1024) return false;
   static int state[64] = {};  // 0 unknown, 1 usable, -1 not
   int dev = 0;

@@ -60,10 +60,11 @@ const char* moe_error_string(int status);
 
 /* ------------------------------------------------------------------ weights
  * One-time re-layout of raw MXFP4 expert weights into the layout the tensor-core
- * kernels stream: codes K-group major, [E][groups][K/128][rows per group][64 B]
- * (K padded to a multiple of 128 codes with code 0), and the E8M0 scales regrouped
+ * kernels stream: the codes stay row major, [E][rows][K/2] (the TMA boxes of 128
+ * rows x 256 codes are cut from them directly), and the E8M0 scales are regrouped
  * into 512-byte atoms of 128 rows x 4 MX blocks, the order in which the
- * block-scaled MMA reads them (groups = 2 for gate/up: gate rows, up rows).  No value is re-quantised;
+ * block-scaled MMA reads them, [E][groups][rows/128][K groups of 128, rounded up to
+ * even][512] (groups = 2 for gate/up: gate rows, up rows).  No value is re-quantised;
  * the bytes are only moved ("MXFP4 MoE on tensor cores": weights permuted once at
  * load).
  *   kind  MOE_WEIGHTS_GATEUP: rows = 2*I (gate then up), K = H.

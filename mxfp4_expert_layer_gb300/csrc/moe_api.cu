@@ -109,30 +109,36 @@ bool make_map(CUtensorMap* out, const void* ptr, CUtensorMapDataType dtype, int 
   return true;
 }
 
-// MXFP4 codes of one prepared family as a 4-D byte map {64 bytes = 128 codes, rows
-// per group, KG, E * groups}: one box = 128 consecutive rows of one K group, a
-// contiguous 8 KB kept packed in shared memory with the 64-byte swizzle.  Rows past
-// the group (the last M tile) are outside the map and read as zero.
-bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P) {
-  cuuint64_t dims[4] = {64, (cuuint64_t)P.rows_per_group, (cuuint64_t)P.kg, (cuuint64_t)P.E * P.groups};
-  cuuint64_t strides[3] = {64, 64ull * P.rows_per_group, 64ull * P.rows_per_group * P.kg};
-  cuuint32_t box[4] = {64, (cuuint32_t)kMTile, 1, 1};
-  return make_map(out, prepared, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
+// MXFP4 codes of one prepared family, row major, as a 3-D byte map {K/2 bytes, rows
+// per group, E * groups}: one box = 128 rows x (one pipeline stage of K: 128 bytes =
+// 256 codes with the 128-byte swizzle, or 64 bytes with the 64-byte swizzle), kept
+// packed in shared memory.  Parts of a box past K or past the group's rows are
+// outside the map and read as zero without touching memory.
+bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P, int bm) {
+  const cuuint64_t row_bytes = (cuuint64_t)P.K / 2;
+  cuuint64_t dims[3] = {row_bytes, (cuuint64_t)P.rows_per_group, (cuuint64_t)P.E * P.groups};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * P.rows_per_group};
+  const int kb = gemm_kstage(bm) / 2;
+  cuuint32_t box[3] = {(cuuint32_t)kb, (cuuint32_t)kMTile, 1};
+  return make_map(out, prepared, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box,
+                  kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// Encoded activations {64 bytes, max_tiles * kTerms * bm rows, KG}: one tile's
-// kTerms * bm rows of a K group are contiguous (boxes of at most 256 rows).
+// Encoded activations {kstage/2 bytes, max_tiles * kTerms * bm rows, stages}: one
+// tile's kTerms * bm rows of a stage are contiguous (boxes of at most 256 rows).
 // Token-major tiles (at most 16 rows) get kActBoxes maps whose boxes hold the rows of
 // 1, 2, 4, 8 or 16 tokens, so a stage loads only its tile's real tokens.
 bool act_map(CUtensorMap (&out)[kActBoxes], const void* base, int K, int max_tiles, int bm) {
   const cuuint64_t rows = (cuuint64_t)max_tiles * kTerms * bm;
-  cuuint64_t dims[3] = {64, rows, (cuuint64_t)ceil_div(K, kKGroup)};
-  cuuint64_t strides[2] = {64, 64 * rows};
+  const int kb = gemm_kstage(bm) / 2;
+  cuuint64_t dims[3] = {(cuuint64_t)kb, rows, (cuuint64_t)ceil_div(K, gemm_kstage(bm))};
+  cuuint64_t strides[2] = {(cuuint64_t)kb, (cuuint64_t)kb * rows};
   for (int q = 0; q < kActBoxes; ++q) {
     int box_rows = kTerms * bm < 256 ? kTerms * bm : 256;
     if (act_token_major(bm)) box_rows = min(kTerms << q, kTerms * bm);
-    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-    if (!make_map(&out[q], base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B))
+    cuuint32_t box[3] = {(cuuint32_t)kb, (cuuint32_t)box_rows, 1};
+    if (!make_map(&out[q], base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box,
+                  kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
       return false;
   }
   return true;
@@ -195,7 +201,7 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
 
   const PreparedLayout P = make_prepared_layout(E, 2 * I, H, 2);
   GemmParams g{};
-  if (!weight_map(&g.tm_w, w_gateup, P)) return MOE_ERR_CUDA;
+  if (!weight_map(&g.tm_w, w_gateup, P, bm)) return MOE_ERR_CUDA;
   if (!act_map(g.tm_act, gx.q, H, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_gateup) + P.scales_off;
   g.act_sf = gx.sf;
@@ -204,7 +210,8 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   g.perm = perm;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k; g.bm = bm; g.max_tiles = L.max_tiles;
   g.K = H;
-  g.kg = P.kg;
+  g.kg = ceil_div(H, gemm_kstage(bm));
+  g.kg_sf = P.kg;
   g.mt = L.mt_i;
   g.rows_out = I;
   g.w_groups = 2;
@@ -225,7 +232,7 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
              cudaStream_t stream) {
   const PreparedLayout P = make_prepared_layout(E, H, I, 1);
   GemmParams g{};
-  if (!weight_map(&g.tm_w, w_down, P)) return MOE_ERR_CUDA;
+  if (!weight_map(&g.tm_w, w_down, P, bm)) return MOE_ERR_CUDA;
   if (!act_map(g.tm_act, ws_ptr<uint8_t>(ws, L.h_q), I, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_down) + P.scales_off;
   g.act_sf = ws_ptr<uint8_t>(ws, L.h_sf);
@@ -234,7 +241,8 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   g.perm = perm;
   g.T = T; g.H = H; g.I = I; g.E = E; g.k = k; g.bm = bm; g.max_tiles = L.max_tiles;
   g.K = I;
-  g.kg = P.kg;
+  g.kg = ceil_div(I, gemm_kstage(bm));
+  g.kg_sf = P.kg;
   // pairs of M tiles per unit when there are units enough to keep every SM busy
   g.m_pair = (long long)std::min(E, T * k) * ceil_div(L.mt_h, 2) >= 2LL * persistent_ctas() ? 1 : 0;
   g.mt = g.m_pair ? ceil_div(L.mt_h, 2) : L.mt_h;
@@ -312,7 +320,7 @@ int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E, int 
   PrepareParams pp{};
   pp.codes = codes;
   pp.scales = scales;
-  pp.E = E; pp.R = rows; pp.K = K; pp.Kp = P.Kp; pp.groups = groups; pp.rows_per_group = P.rows_per_group;
+  pp.E = E; pp.R = rows; pp.K = K; pp.groups = groups; pp.rows_per_group = P.rows_per_group;
   pp.mt = P.mt; pp.kg = P.kg;
   pp.dst_codes = static_cast<uint8_t*>(dst);
   pp.dst_scales = static_cast<uint8_t*>(dst) + P.scales_off;

@@ -1,8 +1,9 @@
 // Data movement kernels around the expert GEMMs:
 //  * encode_x: activation rows encoded once per token as four E2M1 terms with E8M0
 //    block scales (the tensor-core B operand, gathered by the gate/up GEMM);
-//  * prepare: one-time re-layout of raw MXFP4 expert weights ("MXFP4 MoE on tensor
-//    cores": weights permuted once at load; nothing is re-quantised);
+//  * prepare: one-time re-layout of the E8M0 scales of raw MXFP4 expert weights into
+//    the tensor-memory atom order ("MXFP4 MoE on tensor cores": weights permuted once
+//    at load; nothing is re-quantised; the codes stay row major);
 //  * hidden_dequant: expands the encoded SwiGLU output for inspection.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
@@ -171,32 +172,6 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
   return launch_pdl(combine_kernel, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
 }
 
-// Codes: 16-byte vectors moved into the K-group-major layout
-// [E][G][KG][rows per group][64 bytes]; vectors past K/2 bytes of a row are zero.
-__global__ void prepare_codes_kernel(PrepareParams p) {
-  const int src_bytes = p.K / 2;
-  const long long total = (long long)p.E * p.R * p.kg * 4;  // 4 vectors of 16 B per 64-byte run
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    long long t = i;
-    const int v = (int)(t & 3);
-    t >>= 2;
-    const int row = (int)(t % p.rows_per_group);
-    t /= p.rows_per_group;
-    const int kgi = (int)(t % p.kg);
-    t /= p.kg;
-    const int grp = (int)(t % p.groups);
-    const int e = (int)(t / p.groups);
-    const int byte0 = kgi * 64 + v * 16;
-    uint4 val = make_uint4(0, 0, 0, 0);
-    if (byte0 < src_bytes) {
-      const size_t src_row = (size_t)e * p.R + (size_t)grp * p.rows_per_group + row;
-      val = __ldg(reinterpret_cast<const uint4*>(p.codes + src_row * src_bytes + byte0));
-    }
-    reinterpret_cast<uint4*>(p.dst_codes)[i] = val;
-  }
-}
-
 // Scales: one thread per atom byte; rows past the group and blocks past K get 127.
 __global__ void prepare_scales_kernel(PrepareParams p) {
   const long long atoms = (long long)p.E * p.groups * p.mt * p.kg;
@@ -225,8 +200,8 @@ __global__ void prepare_scales_kernel(PrepareParams p) {
 }
 
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream) {
-  prepare_codes_kernel<<<1184, 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // the codes keep their row-major layout
+  cudaError_t e = cudaMemcpyAsync(p.dst_codes, p.codes, (size_t)p.E * p.R * (p.K / 2), cudaMemcpyDeviceToDevice, stream);
   if (e != cudaSuccess) return e;
   prepare_scales_kernel<<<1184, 256, 0, stream>>>(p);
   return cudaGetLastError();

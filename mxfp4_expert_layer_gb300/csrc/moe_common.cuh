@@ -34,7 +34,9 @@ __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a -
 
 // K rounded up to whole pipeline stages (the prepared weight rows carry this many
 // 4-bit codes; codes past the real K are zero).
-__host__ __device__ inline int padded_k(int K) { return ceil_div(K, kKGroup) * kKGroup; }
+// K groups of 128 values (one scale atom each) over K, rounded up to an even count so
+// that a 256-value pipeline stage always finds two atoms
+__host__ __device__ inline int kgroups_even(int K) { return ceil_div(K, 2 * kKGroup) * 2; }
 
 // Token rows per tile from the mean tokens per expert ("token tile follows tokens
 // per expert"): 16 for decode-sized loads, 64 for medium, 128 for prefill.
@@ -75,7 +77,7 @@ __device__ __forceinline__ TileEntry load_tile(const TileEntry* t) {
 // Byte offsets of every region inside the caller-allocated workspace.
 struct WsLayout {
   int T, H, I, E, k, bm, max_tiles, pad_rows;
-  int kg_h, kg_i;        // K groups (of 128) over H and over I
+  int kg_h, kg_i;        // K groups of 128 over H and over I, rounded up to even
   int mt_h, mt_i;        // M tiles (of 128) over H and over I
   size_t status;         // uint32 device status word (+ padding)
   size_t route_sync;     // uint32 [ceil(T/8) + 1] arrival counters of the routing kernel
@@ -90,9 +92,9 @@ struct WsLayout {
   size_t num_tiles;      // i32
   size_t xt_q;           // x encoded per token: [kg_h][T][kTerms][64 bytes] packed E2M1
   size_t xt_sf;          // its E8M0 exponents: u32 [kg_h][T][kTerms] (4 MX blocks each)
-  size_t x_q;            // x gathered into tile order: [kg_h][max_tiles][kTerms][bm][64 bytes]
+  size_t x_q;            // x gathered into tile order (act_offset): kg_h * 128 values per row
   size_t x_sf;           // its scale atoms [max_tiles][kg_h][512 * act_sf_atoms(bm)]
-  size_t h_q;            // h encoded: [kg_i][max_tiles][kTerms][bm][64 bytes]
+  size_t h_q;            // h encoded, tile order (act_offset): kg_i * 128 values per row
   size_t h_sf;           // [max_tiles][kg_i][512 * act_sf_atoms(bm)]
   size_t slots;          // f32 [T*k, H]: weighted expert outputs awaiting the combine
   size_t unit_cnt;       // i32 [max_tiles * max(mt_h, mt_i)]: arrivals per GEMM work unit
@@ -110,8 +112,8 @@ inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   L.T = T; L.H = H; L.I = I; L.E = E; L.k = k; L.bm = bm;
   L.max_tiles = max_tiles_bound(T, k, E, bm);
   L.pad_rows = L.max_tiles * bm;
-  L.kg_h = ceil_div(H, kKGroup);
-  L.kg_i = ceil_div(I, kKGroup);
+  L.kg_h = kgroups_even(H);
+  L.kg_i = kgroups_even(I);
   L.mt_h = ceil_div(H, kMTile);
   L.mt_i = ceil_div(I, kMTile);
   const size_t A = 256;
@@ -151,19 +153,19 @@ __host__ __device__ inline P* ws_ptr(void* ws, size_t off) {
 
 // ----------------------------------------------------------------- MXFP4 weights
 // Prepared weight layout of one matrix family (gate/up or down) for E experts:
-//   codes  [E][G][KG][rows per group][64]  K-group major: for every 128-code K group
-//                         the 64-byte code runs of all rows of a group are adjacent,
-//                         so a 128-row TMA box is one contiguous 8 KB read.  G = 2
-//                         for gate/up (gate rows, up rows), 1 for down; KG = Kp / 128,
-//                         Kp = K padded to a multiple of 128 (pad codes are zero)
-//   scales [E][G][MT][KG][512]  MT = ceil(rows per group / 128); each 512-byte
-//                         atom holds the E8M0 scales of 128 rows x 4 MX blocks:
-//                         byte (l*16 + c*4 + b) = scale of row 32c + l, block b.
+//   codes  [E][G][rows per group][K / 2]  the raw row-major codes, unchanged: a TMA box
+//                         of 128 rows x 128 bytes (or 64) is one 256-code (128-code)
+//                         K step of an M tile; the box past K reads zeros (TMA fill).
+//                         G = 2 for gate/up (gate rows, up rows), 1 for down.
+//   scales [E][G][MT][KG][512]  MT = ceil(rows per group / 128), KG = K groups of 128
+//                         rounded up to even; each 512-byte atom holds the E8M0 scales
+//                         of 128 rows x 4 MX blocks: byte (l*16 + c*4 + b) = scale of
+//                         row 32c + l, block b (127 outside the matrix).
 //   trailer (256 bytes): a status word the preparing kernel sets when it meets
 //                         an E8M0 scale of 255 (NaN).
 struct PreparedLayout {
-  int E, R, K, Kp, groups, rows_per_group, mt, kg;
-  size_t codes_bytes;   // E * R * Kp / 2
+  int E, R, K, groups, rows_per_group, mt, kg;
+  size_t codes_bytes;   // E * R * K / 2
   size_t scales_off;    // aligned start of the scale atoms
   size_t flag_off;      // status trailer
   size_t total;
@@ -171,11 +173,11 @@ struct PreparedLayout {
 
 inline PreparedLayout make_prepared_layout(int E, int R, int K, int groups) {
   PreparedLayout P{};
-  P.E = E; P.R = R; P.K = K; P.Kp = padded_k(K); P.groups = groups;
+  P.E = E; P.R = R; P.K = K; P.groups = groups;
   P.rows_per_group = R / groups;
   P.mt = ceil_div(P.rows_per_group, kMTile);
-  P.kg = P.Kp / kKGroup;
-  P.codes_bytes = (size_t)E * R * (P.Kp / 2);
+  P.kg = kgroups_even(K);
+  P.codes_bytes = (size_t)E * R * (K / 2);
   P.scales_off = align_up(P.codes_bytes, 256);
   P.flag_off = align_up(P.scales_off + (size_t)E * groups * P.mt * P.kg * kSfAtomBytes, 256);
   P.total = P.flag_off + 256;
@@ -232,14 +234,20 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
 // most 16 token rows (all terms in one MMA along N) are token major, so the rows of
 // the tile's real tokens come first and one TMA box of 4 x (tokens rounded up to a
 // power of two) rows covers them; larger tiles are term major (one MMA per term).
-__host__ __device__ inline bool act_token_major(int bm) { return kTerms * bm <= 64; }
+__host__ __device__ constexpr bool act_token_major(int bm) { return kTerms * bm <= 64; }
+// K values per pipeline stage of the expert GEMMs: 256 (128-byte rows, 128-byte
+// swizzle) for 16-row decode tiles, whose weights stream at the HBM rate; 128
+// (64-byte rows) for larger tiles, whose bigger B tiles would leave too few stages.
+__host__ __device__ constexpr int gemm_kstage(int bm) { return act_token_major(bm) ? 256 : 128; }
 __host__ __device__ inline int act_row(int t, int r, int bm) {
   return act_token_major(bm) ? r * kTerms + t : t * bm + r;
 }
 // Byte offset of the code byte holding values (k, k+1) (k even) of term t of row r
-// of tile `tile` in an encoded activation buffer [KG][max_tiles][kTerms * bm rows][64].
+// of tile `tile` in an encoded activation buffer
+// [K / kstage][max_tiles][kTerms * bm rows][kstage / 2 bytes], kstage = gemm_kstage(bm).
 __host__ __device__ inline size_t act_offset(int tile, int t, int r, int k, int max_tiles, int bm) {
-  return (((size_t)(k >> 7) * max_tiles + tile) * (kTerms * bm) + act_row(t, r, bm)) * 64 + ((k & 127) >> 1);
+  const int ks = gemm_kstage(bm);
+  return (((size_t)(k / ks) * max_tiles + tile) * (kTerms * bm) + act_row(t, r, bm)) * (ks / 2) + ((k % ks) >> 1);
 }
 
 // Scale atom byte offset of (row r within a tile, MX block b within a K group).

@@ -38,23 +38,27 @@ namespace {
 
 constexpr int kGemmThreads = 192;
 constexpr uint64_t kWaitLimit = 1000000000ull;  // ns a bounded mbarrier wait may take (1 s)
-constexpr int kATileBytes = kMTile * 64;         // one 128-row x 128-code weight tile, packed
 
 // MPAIR (down only): two neighbouring 128-row M tiles per work unit, sharing each
 // stage's B tile, so a stage carries twice the weight bytes per activation byte.
 template <int BM, bool GATEUP, bool MPAIR>
 struct GemmCfg {
   static constexpr int kA = (GATEUP || MPAIR) ? 2 : 1;       // weight tiles per stage (gate/up, or 2 M tiles)
+  static constexpr int kKStage = gemm_kstage(BM);            // K values per stage
+  static constexpr int kKBytes = kKStage / 2;                // bytes per operand row per stage
+  static constexpr int kAtoms = kKStage / kKGroup;           // scale atoms per 128 rows per stage
+  static constexpr int kKSteps = kKStage / 64;               // K = 64 MMA steps per stage
+  static constexpr int kATileBytes = kMTile * kKBytes;       // one 128-row weight tile of a stage
   static constexpr bool kConcat = kTerms * BM <= 64;         // all terms in one MMA along N
   static constexpr int kN = kConcat ? kTerms * BM : BM;      // MMA N
   static constexpr int kAccN = kN;                           // accumulator columns per weight tile
   static constexpr int kAccCols = kA * kAccN;
   static constexpr int kVals = kA * BM;                      // values per row after summing terms
   static constexpr int kBRows = kTerms * BM;                 // B tile rows (terms x token rows)
-  static constexpr int kBBytes = kBRows * 64;
+  static constexpr int kBBytes = kBRows * kKBytes;
   static constexpr int kBBoxRows = kBRows < 256 ? kBRows : 256;
   static constexpr int kNbAtoms = (kBRows + 127) / 128;      // B scale atoms per stage
-  static constexpr int kSfBytes = (kA + kNbAtoms) * kSfAtomBytes;
+  static constexpr int kSfBytes = (kA + kNbAtoms) * kAtoms * kSfAtomBytes;
   static constexpr int kStageRaw = kA * kATileBytes + kBBytes + kSfBytes;
   static constexpr int kStageBytes = (kStageRaw + 1023) / 1024 * 1024;
   static constexpr int kEpiBytes = 16 * kMTile * 4 + 2 * 128 * 4;  // h transpose chunk + row metadata
@@ -65,7 +69,7 @@ struct GemmCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
   static constexpr uint32_t kTxBytes = kA * kATileBytes + kBBytes + kSfBytes;  // full B box
   static constexpr uint32_t kTxNoB = kA * kATileBytes + kSfBytes;                // all but the B codes
-  static constexpr int kSfColsPerStage = 4 * (kA + kNbAtoms);
+  static constexpr int kSfColsPerStage = 4 * (kA + kNbAtoms) * kAtoms;
   static constexpr int kSfCols = kStages * kSfColsPerStage;
   static constexpr int kNumAcc = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
   static constexpr int kTmemNeed = kNumAcc * kAccCols + kSfCols;
@@ -224,11 +228,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   if (U == 0 || (int)blockIdx.x >= grid) sch.nseg = 0;  // no work: straight to teardown
 
   auto stage_ptr = [&](int s) { return smem + s * C::kStageBytes; };
-  // stage layout: [A tiles][B tile (terms x rows)][SF A x kA][SF B x kNbAtoms]
-  auto a_tile = [&](int s, int j) { return stage_ptr(s) + j * kATileBytes; };
-  auto b_tile = [&](int s) { return stage_ptr(s) + C::kA * kATileBytes; };
-  auto sf_a = [&](int s, int j) { return stage_ptr(s) + C::kA * kATileBytes + C::kBBytes + j * kSfAtomBytes; };
-  auto sf_b = [&](int s) { return stage_ptr(s) + C::kA * kATileBytes + C::kBBytes + C::kA * kSfAtomBytes; };
+  // stage layout: [A tiles][B tile (terms x rows)][SF A: kA x kAtoms atoms][SF B: kAtoms x kNbAtoms atoms]
+  auto a_tile = [&](int s, int j) { return stage_ptr(s) + j * C::kATileBytes; };
+  auto b_tile = [&](int s) { return stage_ptr(s) + C::kA * C::kATileBytes; };
+  auto sf_a = [&](int s, int j) {
+    return stage_ptr(s) + C::kA * C::kATileBytes + C::kBBytes + j * C::kAtoms * kSfAtomBytes;
+  };
+  auto sf_b = [&](int s) { return stage_ptr(s) + C::kA * C::kATileBytes + C::kBBytes + C::kA * C::kAtoms * kSfAtomBytes; };
 
   const int kblocks = p.K / kMxBlock;  // real MX blocks along K; K steps past them are skipped
 
@@ -254,7 +260,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       };
       // bytes the stage's barrier expects for the current tile
       auto tx_bytes = [&]() -> uint32_t {
-        return C::kConcat ? C::kTxNoB + (uint32_t)(kTerms << boxq) * 64u : C::kTxBytes;
+        return C::kConcat ? C::kTxNoB + (uint32_t)(kTerms << boxq) * (uint32_t)C::kKBytes : C::kTxBytes;
       };
       auto load_a = [&](int s) {
         for (int j = 0; j < C::kA; ++j) {
@@ -262,10 +268,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           // tile past the matrix reads zeros (TMA fill) and scales of the last tile.
           const int mrow = GATEUP ? mt : (MPAIR ? 2 * mt + j : mt);
           const int grp = GATEUP ? j : 0;
-          tma_load_4d(a_tile(s, j), &p.tm_w, &full_bar[s], 0, mrow * kMTile, kk, expert * p.w_groups + grp);
+          tma_load_3d(a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile, expert * p.w_groups + grp);
           const int msf = min(mrow, p.w_mt - 1);
-          const uint8_t* wsf = p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)KG * kSfAtomBytes;
-          bulk_load(sf_a(s, j), wsf + (size_t)kk * kSfAtomBytes, kSfAtomBytes, &full_bar[s]);
+          const uint8_t* wsf =
+              p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)p.kg_sf * kSfAtomBytes;
+          bulk_load(sf_a(s, j), wsf + (size_t)kk * C::kAtoms * kSfAtomBytes, C::kAtoms * kSfAtomBytes, &full_bar[s]);
         }
       };
       auto load_b = [&](int s, int b_tile_idx, int b_kk, int q) {
@@ -273,11 +280,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           tma_load_3d(b_tile(s), &p.tm_act[q], &full_bar[s], 0, b_tile_idx * C::kBRows, b_kk);
         } else {
           for (int bx = 0; bx < C::kBRows / C::kBBoxRows; ++bx)
-            tma_load_3d(b_tile(s) + bx * C::kBBoxRows * 64, &p.tm_act[0], &full_bar[s], 0,
+            tma_load_3d(b_tile(s) + bx * C::kBBoxRows * C::kKBytes, &p.tm_act[0], &full_bar[s], 0,
                         b_tile_idx * C::kBRows + bx * C::kBBoxRows, b_kk);
         }
-        bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * KG + b_kk) * (kSfAtomBytes * C::kNbAtoms),
-                  kSfAtomBytes * C::kNbAtoms, &full_bar[s]);
+        // the stage's kAtoms K groups of scale atoms are adjacent
+        bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * p.kg_sf + (size_t)b_kk * C::kAtoms) * (kSfAtomBytes * C::kNbAtoms),
+                  C::kAtoms * C::kNbAtoms * kSfAtomBytes, &full_bar[s]);
       };
       int g = 0;
       bool err = false;
@@ -355,30 +363,37 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           }
           tc_fence_after();
           const uint32_t sfc = tmem + sf_col0 + s * C::kSfColsPerStage;
-          const uint32_t sfb0 = sfc + 4 * C::kA;
-          // scale atoms -> tensor memory (32 rows x 16 bytes, replicated to 4 lane quarters)
-          for (int j = 0; j < C::kA; ++j)
-            tmem_cp_32x128b_warpx4(sfc + 4 * j, smem_desc(smem_u32(sf_a(s, j)), 0, 128, 0));
-          for (int q = 0; q < C::kNbAtoms; ++q)
-            tmem_cp_32x128b_warpx4(sfb0 + 4 * q, smem_desc(smem_u32(sf_b(s)) + q * kSfAtomBytes, 0, 128, 0));
-          for (int ks = 0; ks < 2; ++ks) {           // two K = 64 steps per 128-value K group
-            if (kk * 4 + 2 * ks >= kblocks) break;   // both MX blocks of this step are padding
-            const uint32_t idesc = idesc_mxf4(kMTile, C::kN, 2 * ks, 2 * ks);
+          const uint32_t sfb0 = sfc + 4 * C::kA * C::kAtoms;
+          // scale atoms -> tensor memory (32 rows x 16 bytes, replicated to 4 lane quarters):
+          // A tile j, K group a at columns 4 (j kAtoms + a); B atom (a, q) at 4 (a kNbAtoms + q)
+          for (int i = 0; i < C::kA * C::kAtoms; ++i)
+            tmem_cp_32x128b_warpx4(sfc + 4 * i, smem_desc(smem_u32(sf_a(s, 0)) + i * kSfAtomBytes, 0, 128, 0));
+          for (int i = 0; i < C::kAtoms * C::kNbAtoms; ++i)
+            tmem_cp_32x128b_warpx4(sfb0 + 4 * i, smem_desc(smem_u32(sf_b(s)) + i * kSfAtomBytes, 0, 128, 0));
+          // operand rows are kKBytes long (64-byte swizzle for 64, 128-byte for 128)
+          auto kdesc = [&](uint32_t saddr) {
+            return C::kKBytes == 128 ? smem_desc_kmajor_sw128(saddr) : smem_desc_kmajor_sw64(saddr);
+          };
+          for (int ks = 0; ks < C::kKSteps; ++ks) {  // K = 64 steps: 32 bytes of every operand row
+            if (kk * (C::kKStage / kMxBlock) + 2 * ks >= kblocks) break;  // both MX blocks are padding
+            const int a = ks >> 1;                    // K group (scale atom) of this step
+            const uint32_t idesc = idesc_mxf4(kMTile, C::kN, 2 * (ks & 1), 2 * (ks & 1));
             if constexpr (C::kConcat) {
-              const uint64_t bdesc = smem_desc_kmajor_sw64(smem_u32(b_tile(s)) + 32 * ks);
+              const uint64_t bdesc = kdesc(smem_u32(b_tile(s)) + 32 * ks);
               const uint32_t acc = seg_first ? 0u : 1u;
               for (int j = 0; j < C::kA; ++j) {
-                const uint64_t adesc = smem_desc_kmajor_sw64(smem_u32(a_tile(s, j)) + 32 * ks);
-                mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * j, sfb0, acc);
+                const uint64_t adesc = kdesc(smem_u32(a_tile(s, j)) + 32 * ks);
+                mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
+                         sfb0 + 4 * a * C::kNbAtoms, acc);
               }
             } else {
               for (int t = 0; t < kTerms; ++t) {
-                const uint64_t bdesc = smem_desc_kmajor_sw64(smem_u32(b_tile(s)) + t * BM * 64 + 32 * ks);
-                const uint32_t sfb = sfb0 + (t * BM) / 32;
+                const uint64_t bdesc = kdesc(smem_u32(b_tile(s)) + t * BM * C::kKBytes + 32 * ks);
+                const uint32_t sfb = sfb0 + 4 * a * C::kNbAtoms + (t * BM) / 32;
                 const uint32_t acc = (seg_first && t == 0) ? 0u : 1u;
                 for (int j = 0; j < C::kA; ++j) {
-                  const uint64_t adesc = smem_desc_kmajor_sw64(smem_u32(a_tile(s, j)) + 32 * ks);
-                  mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * j, sfb, acc);
+                  const uint64_t adesc = kdesc(smem_u32(a_tile(s, j)) + 32 * ks);
+                  mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a), sfb, acc);
                 }
               }
             }

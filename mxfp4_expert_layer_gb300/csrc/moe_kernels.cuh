@@ -77,18 +77,20 @@ cudaError_t launch_gather_x(const GatherXParams& p, cudaStream_t stream);
 
 struct GemmParams {
   // operand tensor maps (TMA)
-  CUtensorMap tm_w;        // weights: packed E2M1 [E*groups][KG][rows][64 B]
-  // activations (x gathered, or h): packed E2M1 terms [KG][max_tiles*kTerms*bm][64 B];
-  // tiles of at most 16 rows use box q = 4 * 2^q rows (q < kActBoxes), others box 0
+  CUtensorMap tm_w;        // weights: packed E2M1 codes, row major [E*groups][rows][K/2 B]
+  // activations (x gathered, or h): packed E2M1 terms
+  // [stages][max_tiles*kTerms*bm][kstage/2 bytes]; tiles of at most 16 rows use box
+  // q = 4 * 2^q rows (q < kActBoxes), others box 0
   CUtensorMap tm_act[kActBoxes];
-  const uint8_t* w_sf;     // weight scale atoms [E][groups][mt][kg][512]
-  const uint8_t* act_sf;   // activation scale atoms [max_tiles][kg][512 * act_sf_atoms]
+  const uint8_t* w_sf;     // weight scale atoms [E][groups][mt][kg_sf][512]
+  const uint8_t* act_sf;   // activation scale atoms [max_tiles][kg_sf][512 * act_sf_atoms]
   const TileEntry* tiles;
   const int32_t* num_tiles;
   const int32_t* perm;
   int T, H, I, E, k, bm, max_tiles;
   int K;                   // contraction length (H for gate/up, I for down)
-  int kg;                  // K groups of 128
+  int kg;                  // pipeline stages along K (K / gemm_kstage(bm), rounded up)
+  int kg_sf;               // K groups of 128 (scale atoms) along K, rounded up to even
   int mt;                  // M units of the output features (M tiles, or pairs of them)
   int rows_out;            // output features (I for gate/up, H for down)
   int w_groups;            // 2 (gate, up) or 1 (down)
@@ -97,7 +99,7 @@ struct GemmParams {
   int group_tiles;         // tiles per raster group
   // gate/up epilogue outputs (four-term E2M1 h)
   uint8_t *h_q, *h_sf;
-  int kg_out;              // K groups of h along I
+  int kg_out;              // K groups of 128 of h along I, rounded up to even
   // down epilogue
   const float* topk_w;
   float* slots;            // f32 [T*k, H]: w_tj * y_tj per assignment
@@ -121,7 +123,7 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 struct PrepareParams {
   const uint8_t* codes;    // [E][R][K/2]
   const uint8_t* scales;   // [E][R][K/32]
-  int E, R, K, Kp, groups, rows_per_group, mt, kg;
+  int E, R, K, groups, rows_per_group, mt, kg;
   uint8_t* dst_codes;
   uint8_t* dst_scales;
   uint32_t* flag;          // set to 1 when a scale byte is 255

@@ -53,11 +53,12 @@ def test_sizes_and_policy(lib):
         assert L.moe_tile_rows(T, k, E) == oracle.tile_rows_policy(T, k, E)
         for bm in (16, 64, 128):
             assert L.moe_max_tiles(T, k, E, bm) == oracle.max_tiles_bound(T, k, E, bm)
-    # prepared bytes: codes padded to 128 K values, 512-byte scale atoms, trailer
+    # prepared bytes: the row-major codes, 512-byte scale atoms over an even number of
+    # 128-value K groups (2880 -> 24), a trailer
     E, I, H = 32, 2880, 2880
     n = L.moe_prepared_weight_bytes(E, 2 * I, H, L.MOE_WEIGHTS_GATEUP)
-    codes = E * 2 * I * 2944 // 2
-    atoms = E * 2 * 23 * 23 * 512
+    codes = E * 2 * I * H // 2
+    atoms = E * 2 * 23 * 24 * 512
     assert n == ((codes + 255) // 256 * 256 + atoms + 255) // 256 * 256 + 256
     assert L.moe_prepared_weight_bytes(E, 2 * I + 1, H, L.MOE_WEIGHTS_GATEUP) == 0
     assert L.moe_forward_launches(64, 2880, 2880, 32, 4) == 6

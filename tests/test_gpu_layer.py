@@ -15,20 +15,17 @@ pytestmark = pytest.mark.gpu
 
 
 def expected_prepared(codes: np.ndarray, scales: np.ndarray, groups: int) -> np.ndarray:
-    """The documented prepared layout, restated: codes K-group major
-    [E][G][KG][rows per group][64 bytes] (zero past K), then (256-aligned) scale atoms
+    """The documented prepared layout, restated: the codes unchanged (row major
+    [E][G * rows per group][K/2]), then (256-aligned) scale atoms
     [E][G][MT][KG][32 l][4 c][4 b] = scale of row 32c + l of the M tile, MX block
-    4*kg + b (127 outside the matrix), then a 256-byte status trailer."""
+    4*kg + b (127 outside the matrix), KG = K groups of 128 rounded up to even, then a
+    256-byte status trailer."""
     E, R, half = codes.shape
     K = half * 2
-    Kp = math.ceil(K / 128) * 128
     rpg = R // groups
     MT = math.ceil(rpg / 128)
-    KG = Kp // 128
-    padded = np.zeros((E, R, Kp // 2), np.uint8)
-    padded[:, :, :half] = codes
-    # [E][G*rpg][KG*64] -> [E][G][KG][rpg][64]
-    cp = padded.reshape(E, groups, rpg, Kp // 128, 64).transpose(0, 1, 3, 2, 4)
+    KG = math.ceil(K / 256) * 2
+    cp = codes
     sc = np.full((E, groups, MT, KG, 32, 4, 4), 127, np.uint8)
     blocks = K // 32
     for mt in range(MT):

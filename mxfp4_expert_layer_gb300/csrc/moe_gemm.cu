@@ -36,7 +36,10 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kGemmThreads = 192;
+// warps: 0 TMA producer, 1 MMA issuer, 2-5 epilogue (one per tensor-memory lane
+// quarter), 6 second MMA issuer (used when a stage carries two weight tiles)
+constexpr int kGemmThreads = 224;
+constexpr int kSecondIssuerWarp = 6;
 constexpr uint64_t kWaitLimit = 1000000000ull;  // ns a bounded mbarrier wait may take (1 s)
 
 // MPAIR (down only): two neighbouring 128-row M tiles per work unit, sharing each
@@ -69,7 +72,10 @@ struct GemmCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
   static constexpr uint32_t kTxBytes = kA * kATileBytes + kBBytes + kSfBytes;  // full B box
   static constexpr uint32_t kTxNoB = kA * kATileBytes + kSfBytes;                // all but the B codes
-  static constexpr int kSfColsPerStage = 4 * (kA + kNbAtoms) * kAtoms;
+  // MMA issuers: with two weight tiles per stage each of two threads issues one
+  // tile's MMAs (its own accumulator, scale copies and B scale columns)
+  static constexpr int kIssuers = kA;
+  static constexpr int kSfColsPerStage = 4 * (kA + kIssuers * kNbAtoms) * kAtoms;
   static constexpr int kSfCols = kStages * kSfColsPerStage;
   static constexpr int kNumAcc = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
   static constexpr int kTmemNeed = kNumAcc * kAccCols + kSfCols;
@@ -190,10 +196,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], C::kIssuers);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf_bar[b], 1);
+      mbar_init(&accf_bar[b], C::kIssuers);
       mbar_init(&acce_bar[b], 128);
     }
     s_flags[0] = 0;
@@ -332,10 +338,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     } else {
       pdl_wait();
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kSecondIssuerWarp) {
+    // ------------------------------------------------------------ MMA issuers
     pdl_wait();
-    if (lane == 0) {
+    const int issuer = warp == 1 ? 0 : 1;
+    if (lane == 0 && issuer < C::kIssuers) {
+      // this thread's weight tiles j in [j0, j1)
+      const int j0 = C::kIssuers == 2 ? issuer : 0, j1 = C::kIssuers == 2 ? issuer + 1 : C::kA;
       const uint32_t sf_col0 = C::kNumAcc * C::kAccCols;
       int g = 0;
       bool err = false;
@@ -363,10 +372,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           }
           tc_fence_after();
           const uint32_t sfc = tmem + sf_col0 + s * C::kSfColsPerStage;
-          const uint32_t sfb0 = sfc + 4 * C::kA * C::kAtoms;
+          // this issuer's copy of the B scale atoms
+          const uint32_t sfb0 = sfc + 4 * C::kA * C::kAtoms + issuer * 4 * C::kNbAtoms * C::kAtoms;
           // scale atoms -> tensor memory (32 rows x 16 bytes, replicated to 4 lane quarters):
           // A tile j, K group a at columns 4 (j kAtoms + a); B atom (a, q) at 4 (a kNbAtoms + q)
-          for (int i = 0; i < C::kA * C::kAtoms; ++i)
+          for (int i = j0 * C::kAtoms; i < j1 * C::kAtoms; ++i)
             tmem_cp_32x128b_warpx4(sfc + 4 * i, smem_desc(smem_u32(sf_a(s, 0)) + i * kSfAtomBytes, 0, 128, 0));
           for (int i = 0; i < C::kAtoms * C::kNbAtoms; ++i)
             tmem_cp_32x128b_warpx4(sfb0 + 4 * i, smem_desc(smem_u32(sf_b(s)) + i * kSfAtomBytes, 0, 128, 0));
@@ -381,7 +391,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             if constexpr (C::kConcat) {
               const uint64_t bdesc = kdesc(smem_u32(b_tile(s)) + 32 * ks);
               const uint32_t acc = seg_first ? 0u : 1u;
-              for (int j = 0; j < C::kA; ++j) {
+              for (int j = j0; j < j1; ++j) {
                 const uint64_t adesc = kdesc(smem_u32(a_tile(s, j)) + 32 * ks);
                 mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
                          sfb0 + 4 * a * C::kNbAtoms, acc);
@@ -391,7 +401,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                 const uint64_t bdesc = kdesc(smem_u32(b_tile(s)) + t * BM * C::kKBytes + 32 * ks);
                 const uint32_t sfb = sfb0 + 4 * a * C::kNbAtoms + (t * BM) / 32;
                 const uint32_t acc = (seg_first && t == 0) ? 0u : 1u;
-                for (int j = 0; j < C::kA; ++j) {
+                for (int j = j0; j < j1; ++j) {
                   const uint64_t adesc = kdesc(smem_u32(a_tile(s, j)) + 32 * ks);
                   mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a), sfb, acc);
                 }
@@ -399,12 +409,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             }
             seg_first = false;
           }
-          mma_commit(&empty_bar[s]);  // frees the stage once these MMAs have read it
+          mma_commit(&empty_bar[s]);  // frees the stage once both issuers' MMAs have read it
         }
         if (!err) mma_commit(&accf_bar[b]);
       }
     }
-  } else {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // unit counters are cleared by the call's first launch
     const int q = warp & 3;                // tensor-memory lane quarter of this warp

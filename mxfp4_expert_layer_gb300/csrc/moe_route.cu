@@ -34,6 +34,13 @@ constexpr int kStageVecs = 12;   // 16-byte activation loads in flight per threa
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// Unsigned key with the order of the float it encodes (larger float -> larger key).
+__device__ __forceinline__ uint32_t sortable_key(float v) {
+  if (v == 0.f) v = 0.f;  // -0 and +0 compare equal
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // (value, index) order used by top-k: larger value first, then smaller index.
 __device__ __forceinline__ bool topk_better(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
@@ -170,6 +177,7 @@ __device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k
   float my_v = -INFINITY;  // lane j keeps the j-th selection
   int my_i = 0;
   for (int j = 0; j < k; ++j) {
+    // this lane's best remaining element (larger value, then smaller index)
     float bv = -INFINITY;
     int bi = 0x7fffffff;
 #pragma unroll
@@ -180,15 +188,12 @@ __device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k
         bi = e;
       }
     }
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-      if (topk_better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
+    // warp arg-max in two reductions: the largest value (as an order-preserving
+    // unsigned key), then the smallest index among the lanes holding it
+    const uint32_t key = sortable_key(bv);
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+    bi = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)bi : 0xffffffffu);
+    bv = __shfl_sync(0xffffffffu, bv, bi & 31);
     if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
     if (lane == j) {
       my_v = bv;
@@ -430,15 +435,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     mbar_init(bar, 1);
     fence_mbar_init();
   }
-  for (int i = tid; i < (L.mrows - p.T) * (L.pitch / 16); i += kRouteThreads) {
-    const int r = p.T + i / (L.pitch / 16), c = i % (L.pitch / 16);
-    *reinterpret_cast<uint4*>(xs + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
-  }
-  for (int i = tid; i < (L.erows - p.E) * (L.pitch / 16); i += kRouteThreads) {
-    const int r = p.E + i / (L.pitch / 16), c = i % (L.pitch / 16);
-    *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
-  }
   __syncthreads();
+  // the copies first (their latency is the long pole), then the zero rows they never touch
   if (slice_bytes > 0) {
     if (tid == 0) mbar_arrive_expect_tx(bar, slice_bytes * (uint32_t)(p.T + p.E));
     for (int r = tid; r < p.T + p.E; r += kRouteThreads) {
@@ -448,8 +446,17 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
         bulk_load(wsm + (size_t)(r - p.T) * L.pitch, p.w_router + (size_t)(r - p.T) * p.H + ks0 * 16, slice_bytes,
                   bar);
     }
-    if (!mbar_wait_bounded(bar, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
   }
+  for (int i = tid; i < (L.mrows - p.T) * (L.pitch / 16); i += kRouteThreads) {
+    const int r = p.T + i / (L.pitch / 16), c = i % (L.pitch / 16);
+    *reinterpret_cast<uint4*>(xs + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
+  }
+  for (int i = tid; i < (L.erows - p.E) * (L.pitch / 16); i += kRouteThreads) {
+    const int r = p.E + i / (L.pitch / 16), c = i % (L.pitch / 16);
+    *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
+  }
+  if (slice_bytes > 0 && !mbar_wait_bounded(bar, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
+  __syncthreads();  // zero rows written by other threads
   // partial logits: (16-token, 8-expert) output tiles dealt to the warps, kMmaIlp
   // independent tiles per pass so the tensor-core latencies overlap
   {

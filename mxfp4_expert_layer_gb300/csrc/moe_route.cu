@@ -457,38 +457,40 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   }
   if (slice_bytes > 0 && !mbar_wait_bounded(bar, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
   __syncthreads();  // zero rows written by other threads
-  // partial logits: (16-token, 8-expert) output tiles dealt to the warps, kMmaIlp
-  // independent tiles per pass so the tensor-core latencies overlap
+  // partial logits: a warp takes one 16-token row block and kMmaIlp consecutive
+  // 8-expert column blocks, so each A fragment loaded from shared memory serves
+  // kMmaIlp MMAs (shared-memory bandwidth, not the tensor pipe, bounds this phase)
   {
-    const int ntn = L.erows / 8, npairs = (L.mrows / 16) * ntn;
+    const int ntn = L.erows / 8;
+    const int ngroups = (ntn + kMmaIlp - 1) / kMmaIlp, nitems = (L.mrows / 16) * ngroups;
     const uint32_t xs_u = smem_u32(xs), ws_u = smem_u32(wsm);
-    for (int base = warp; base < npairs; base += kRouteWarps * kMmaIlp) {
+    for (int item = warp; item < nitems; item += kRouteWarps) {
+      const int mi = item / ngroups, n0 = (item - mi * ngroups) * kMmaIlp;
       float c[kMmaIlp][4];
-      uint32_t a_addr[kMmaIlp], b_addr[kMmaIlp];
+      uint32_t b_addr[kMmaIlp];
+      // ldmatrix row addresses: A rows mi*16 + lane%16, column half lane/16; B rows
+      // ni*8 + lane%8, column half (lane/8)%2 (a column block past E repeats the last)
+      const uint32_t a_addr = xs_u + (uint32_t)((mi * 16 + (lane & 15)) * L.pitch + (lane >> 4) * 16);
 #pragma unroll
       for (int q = 0; q < kMmaIlp; ++q) {
-        const int pi = min(base + q * kRouteWarps, npairs - 1);
-        const int mi = pi / ntn, ni = pi - mi * ntn;
-        // ldmatrix row addresses: A rows mi*16 + lane%16, column half lane/16; B rows
-        // ni*8 + lane%8, column half (lane/8)%2
-        a_addr[q] = xs_u + (uint32_t)((mi * 16 + (lane & 15)) * L.pitch + (lane >> 4) * 16);
+        const int ni = min(n0 + q, ntn - 1);
         b_addr[q] = ws_u + (uint32_t)((ni * 8 + (lane & 7)) * L.pitch + ((lane >> 3) & 1) * 16);
         c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
       }
       for (int kk = 0; kk < ks1 - ks0; ++kk) {
+        uint32_t a[4];
+        ldmatrix_x4(a, a_addr + kk * 32);
 #pragma unroll
         for (int q = 0; q < kMmaIlp; ++q) {
-          uint32_t a[4], b[2];
-          ldmatrix_x4(a, a_addr[q] + kk * 32);
+          uint32_t b[2];
           ldmatrix_x2(b, b_addr[q] + kk * 32);
           mma_bf16_16816(c[q], a, b);
         }
       }
 #pragma unroll
       for (int q = 0; q < kMmaIlp; ++q) {
-        const int pi = base + q * kRouteWarps;
-        if (pi >= npairs) break;
-        const int mi = pi / ntn, ni = pi - mi * ntn;
+        const int ni = n0 + q;
+        if (ni >= ntn) break;
         const int r0 = mi * 16 + (lane >> 2), c0 = ni * 8 + (lane & 3) * 2;
         part[r0 * L.erows + c0] = c[q][0];
         part[r0 * L.erows + c0 + 1] = c[q][1];

@@ -172,15 +172,13 @@ int persistent_ctas() {
 }
 
 // ------------------------------------------------------------------ stage bodies
-// Per-token activation encoding; also clears the GEMMs' arrival counters.
+// Per-token activation encoding.
 int run_encode_x(const uint16_t* x, int T, int H, void* ws, const WsLayout& L, cudaStream_t stream) {
   EncodeXParams q{};
   q.x = x;
   q.T = T; q.H = H;
   q.q = ws_ptr<uint8_t>(ws, L.xt_q);
   q.sf = ws_ptr<uint32_t>(ws, L.xt_sf);
-  q.zero_buf = ws_ptr<int32_t>(ws, L.unit_cnt);
-  q.zero_count = (int)(L.zero_bytes / sizeof(int32_t));
   return cuda_status(launch_encode_x(q, stream));
 }
 
@@ -221,8 +219,6 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   g.h_sf = ws_ptr<uint8_t>(ws, L.h_sf);
   g.kg_out = L.kg_i;
   g.grid = persistent_ctas();
-  g.partials = ws_ptr<float>(ws, L.partials);
-  g.unit_cnt = ws_ptr<int32_t>(ws, L.unit_cnt);
   g.status = ws_ptr<uint32_t>(ws, L.status);
   return cuda_status(launch_gateup(g, stream));
 }
@@ -253,8 +249,6 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   g.topk_w = topk_w;
   g.slots = ws_ptr<float>(ws, L.slots);
   g.grid = persistent_ctas();
-  g.partials = ws_ptr<float>(ws, L.partials);
-  g.unit_cnt = ws_ptr<int32_t>(ws, L.unit_cnt);
   g.status = ws_ptr<uint32_t>(ws, L.status);
   int st = cuda_status(launch_down(g, stream));
   if (st != MOE_OK) return st;

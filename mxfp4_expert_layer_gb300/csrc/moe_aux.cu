@@ -36,11 +36,6 @@ __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) 
   ptx::pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
-  // clear the arrival counters of the GEMM kernels (grid-stride)
-  if (p.zero_buf) {
-    for (int i = blockIdx.x * kAuxThreads + threadIdx.x; i < p.zero_count; i += gridDim.x * kAuxThreads)
-      p.zero_buf[i] = 0;
-  }
   const int nvec_pad = ((p.H + 63) / 64) * 8;  // 8-value vectors per row, padded to 64 values
   const int nchunks = (nvec_pad + 31) / 32;
   const int t = (int)(gw / nchunks);

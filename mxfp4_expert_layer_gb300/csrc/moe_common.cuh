@@ -97,9 +97,6 @@ struct WsLayout {
   size_t h_q;            // h encoded, tile order (act_offset): kg_i * 128 values per row
   size_t h_sf;           // [max_tiles][kg_i][512 * act_sf_atoms(bm)]
   size_t slots;          // f32 [T*k, H]: weighted expert outputs awaiting the combine
-  size_t unit_cnt;       // i32 [max_tiles * max(mt_h, mt_i)]: arrivals per GEMM work unit
-  size_t zero_bytes;     // bytes from unit_cnt cleared before each layer call
-  size_t partials;       // f32 [2 * kMaxCtas][2 * bm * 128]: split-K partial accumulators
   size_t total;
 };
 
@@ -139,9 +136,6 @@ inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   L.h_q = take((size_t)L.kg_i * L.pad_rows * kTerms * 64);
   L.h_sf = take((size_t)L.max_tiles * L.kg_i * sfa);
   L.slots = take(sizeof(float) * tk * H);
-  L.unit_cnt = take(sizeof(int32_t) * (size_t)L.max_tiles * (L.mt_h > L.mt_i ? L.mt_h : L.mt_i));
-  L.zero_bytes = o - L.unit_cnt;
-  L.partials = take(sizeof(float) * (size_t)2 * kMaxCtas * 2 * bm * kMTile);
   L.total = o;
   return L;
 }

@@ -20,12 +20,10 @@
 // adds the four column groups); larger tiles run one MMA per term into the same
 // accumulator.
 //
-// Persistent CTAs (one per SM) split the iterations (work unit x K group) of all
-// units evenly; a unit cut by a CTA boundary writes fp32 partials and an integer
-// arrival counter elects the CTA that sums them, in fixed order.  Warp roles: warp
-// 0 issues TMA loads into a ring of shared-memory stages, warp 1 issues MMAs into
-// one of two tensor-memory accumulators, warps 2-5 run the epilogue of one unit
-// while the MMAs of the next proceed.
+// Persistent CTAs (one per SM) take whole work units (expert tile x M tile)
+// round-robin.  Warp roles: warp 0 issues TMA loads into a ring of shared-memory
+// stages, warps 1 and 6 issue MMAs into one of two tensor-memory accumulators,
+// warps 2-5 run the epilogue of one unit while the MMAs of the next proceed.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
 #include "sm100_ptx.cuh"
@@ -100,67 +98,24 @@ __device__ __forceinline__ void map_unit(int u, int num_tiles, int mt_count, int
   tile = first + within % gsize;
 }
 
-// Even split of the W = units x K-groups iterations over G persistent CTAs: CTA c
-// owns iterations [begin(c), begin(c + 1)), never empty since G <= W.  A unit cut
-// by a CTA boundary is finished by whichever of its CTAs arrives last.
-struct SplitK {
-  long long W;
-  int G;
-  __device__ __forceinline__ int begin(int c) const { return (int)((W * c) / G); }
-  __device__ __forceinline__ int cta_of(int it) const {
-    int c = (int)(((long long)it * G) / W);
-    if (c > G - 1) c = G - 1;
-    while (c + 1 < G && begin(c + 1) <= it) ++c;
-    while (c > 0 && begin(c) > it) --c;
-    return c;
-  }
-  // partial-sum slot of CTA c for unit u: 2c for its first unit, 2c + 1 for its last
-  __device__ __forceinline__ int slot(int c, int u, int kg) const { return (u == begin(c) / kg) ? 2 * c : 2 * c + 1; }
-};
-
-// Work schedule of one CTA.  With no more units than CTAs every CTA runs one whole
-// unit (grid = U): nothing is split, so no partials are exchanged.  Otherwise D
-// whole units are dealt round-robin (unit c + w*G), then the remaining units' K
-// iterations are split evenly (stream-K); D leaves between G and 2G units for the
-// split so every CTA gets work and none gets more than one unit's worth extra.
+// Work schedule of one CTA: whole units dealt round-robin (unit c + i*G).  With no
+// more units than CTAs every CTA runs one unit (grid = U).  No unit is ever split
+// along K: measured on the decode shapes, exchanging fp32 partials between CTAs for
+// the last wave costs more than the last wave's imbalance.
 struct Schedule {
-  int KG, G, D, u0;   // u0 = D * G: first unit of the split part
-  SplitK sk;          // over the split part's iterations
-  int c, b, e;        // this CTA and its split range [b, e)
-  int nseg;           // segments of this CTA: D whole units + split segments
+  int KG, G, c, nseg;
   __device__ void init(int U, int kg, int grid, int cta) {
     KG = kg;
     G = grid;
-    D = (U <= grid) ? 1 : (U >= 2 * grid) ? U / grid - 1 : 0;  // U <= grid: callers pass grid = U
-    u0 = D * grid;
-    const long long Wr = (long long)(U - u0) * kg;
-    sk.W = Wr;
-    sk.G = (int)(Wr < (long long)grid ? Wr : (long long)grid);
     c = cta;
-    if (cta < sk.G) {
-      b = sk.begin(cta);
-      e = sk.begin(cta + 1);
-      nseg = D + (e - 1) / kg - b / kg + 1;
-    } else {
-      b = e = 0;
-      nseg = D;
-    }
+    nseg = (U > cta) ? (U - cta + grid - 1) / grid : 0;  // units cta, cta + G, ... below U
   }
-  // segment i: unit, K-group range, whether the unit is whole here
+  // segment i: its unit and K-group range (always the whole K)
   __device__ void seg(int i, int& u, int& kk0, int& kk1, bool& whole) const {
-    if (i < D) {
-      u = c + i * G;
-      kk0 = 0;
-      kk1 = KG;
-      whole = true;
-      return;
-    }
-    const int ur = b / KG + (i - D);  // unit within the split part
-    const int s0 = max(b, ur * KG), s1 = min(e, (ur + 1) * KG);
-    u = u0 + ur;
-    kk0 = s0 - ur * KG;
-    kk1 = s1 - ur * KG;
-    whole = (kk0 == 0) && (kk1 == KG);
+    u = c + i * G;
+    kk0 = 0;
+    kk1 = KG;
+    whole = true;
   }
 };
 
@@ -416,7 +371,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
-    pdl_wait();  // unit counters are cleared by the call's first launch
+    pdl_wait();  // h (down) comes from the immediately preceding kernel
     const int q = warp & 3;                // tensor-memory lane quarter of this warp
     const int m = q * 32 + lane;           // row of the 128-row tile
     const int et = threadIdx.x - 64;       // 0..127 within the epilogue warps
@@ -448,8 +403,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       tc_fence_after();
       epi_bar();  // row metadata visible
       const uint32_t acc_addr = tmem + lane_off + b * C::kAccCols;
-      const int ur = u - sch.u0;  // unit within the split part (when not whole)
-      float* my_slot = whole ? nullptr : p.partials + (size_t)sch.sk.slot(blockIdx.x, ur, KG) * (C::kVals * kMTile);
 
       // the math of 16 token columns starting at c0, given g/u (gate/up) or y (down)
       auto consume = [&](int c0, const float* va, const float* vb) {
@@ -523,28 +476,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         }
       };
 
-      // unit finisher election for a split unit (after this CTA's partials are stored)
-      auto elect_finisher = [&]() -> bool {
-        __threadfence();
-        epi_bar();
-        if (et == 0) {
-          const int cf = sch.sk.cta_of(ur * KG), cl = sch.sk.cta_of(ur * KG + KG - 1);
-          int* cnt = p.unit_cnt + u;
-          const int old = atomicAdd(cnt, 1);
-          const int fin = (old == cl - cf) ? 1 : 0;
-          if (fin) *cnt = 0;
-          s_flags[1] = fin;
-        }
-        epi_bar();
-        const bool fin = s_flags[1] != 0;
-        if (fin) __threadfence();
-        return fin;
-      };
-      auto slot_of = [&](int c) {
-        return p.partials + (size_t)sch.sk.slot(c, ur, KG) * (C::kVals * kMTile);
-      };
-
-      bool finished = whole;
       if constexpr (C::kLoadAll) {
         // whole accumulator -> registers, release it to the MMA warp, then compute
         float acc[C::kAccCols];
@@ -575,97 +506,27 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
             }
             vals[j * BM + c] = v;
           }
-        if (!whole) {
 #pragma unroll
-          for (int j = 0; j < C::kVals; ++j) my_slot[j * kMTile + m] = vals[j];
-          finished = elect_finisher();
-          if (finished) {
-            const int cf = sch.sk.cta_of(ur * KG), cl = sch.sk.cta_of(ur * KG + KG - 1);
-#pragma unroll
-            for (int j = 0; j < C::kVals; ++j) vals[j] = 0.f;
-            // up to three slots in flight at a time (one for wide tiles), summed in CTA (K) order
-            if constexpr (C::kVals > 32) {
-              for (int c = cf; c <= cl; ++c) {
-                const float* sl = slot_of(c);
-#pragma unroll
-                for (int j = 0; j < C::kVals; ++j) vals[j] += __ldcg(sl + j * kMTile + m);
-              }
-            } else
-            for (int c = cf; c <= cl; c += 3) {
-              float t1[C::kVals], t2[C::kVals], t3[C::kVals];
-              const float* s1p = slot_of(c);
-              const float* s2p = c + 1 <= cl ? slot_of(c + 1) : nullptr;
-              const float* s3p = c + 2 <= cl ? slot_of(c + 2) : nullptr;
-#pragma unroll
-              for (int j = 0; j < C::kVals; ++j) {
-                t1[j] = __ldcg(s1p + j * kMTile + m);
-                t2[j] = s2p ? __ldcg(s2p + j * kMTile + m) : 0.f;
-                t3[j] = s3p ? __ldcg(s3p + j * kMTile + m) : 0.f;
-              }
-#pragma unroll
-              for (int j = 0; j < C::kVals; ++j) {
-                vals[j] += t1[j];
-                if (s2p) vals[j] += t2[j];
-                if (s3p) vals[j] += t3[j];
-              }
-            }
-          }
-        }
-        if (finished) {
-#pragma unroll
-          for (int c0 = 0; c0 < BM; c0 += 16)
-            if (c0 < nrows) consume(c0, vals + c0, C::kA > 1 ? vals + BM + c0 : nullptr);
-        }
+        for (int c0 = 0; c0 < BM; c0 += 16)
+          if (c0 < nrows) consume(c0, vals + c0, C::kA > 1 ? vals + BM + c0 : nullptr);
       } else {
         // accumulator too large for registers (per-term MMAs): 16 columns at a time
-        if (whole) {
-          for (int c0 = 0; c0 < BM; c0 += 16) {
-            if (c0 >= nrows) break;
-            uint32_t rg[16], ru[16];
-            float va[16], vb[16];
-            tmem_ld_32x32b_x16(acc_addr + c0, rg);
-            if (C::kA > 1) tmem_ld_32x32b_x16(acc_addr + C::kAccN + c0, ru);
-            tmem_wait_ld();
+        for (int c0 = 0; c0 < BM; c0 += 16) {
+          if (c0 >= nrows) break;
+          uint32_t rg[16], ru[16];
+          float va[16], vb[16];
+          tmem_ld_32x32b_x16(acc_addr + c0, rg);
+          if (C::kA > 1) tmem_ld_32x32b_x16(acc_addr + C::kAccN + c0, ru);
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              va[j] = __uint_as_float(rg[j]);
-              vb[j] = C::kA > 1 ? __uint_as_float(ru[j]) : 0.f;
-            }
-            consume(c0, va, vb);
+          for (int j = 0; j < 16; ++j) {
+            va[j] = __uint_as_float(rg[j]);
+            vb[j] = C::kA > 1 ? __uint_as_float(ru[j]) : 0.f;
           }
-          tc_fence_before();
-          mbar_arrive(&acce_bar[b]);
-        } else {
-          for (int j0 = 0; j0 < C::kA; ++j0)
-            for (int c0 = 0; c0 < BM; c0 += 16) {
-              uint32_t r[16];
-              tmem_ld_32x32b_x16(acc_addr + j0 * C::kAccN + c0, r);
-              tmem_wait_ld();
-#pragma unroll
-              for (int j = 0; j < 16; ++j) my_slot[(j0 * BM + c0 + j) * kMTile + m] = __uint_as_float(r[j]);
-            }
-          tc_fence_before();
-          mbar_arrive(&acce_bar[b]);
-          finished = elect_finisher();
-          if (finished) {
-            const int cf = sch.sk.cta_of(ur * KG), cl = sch.sk.cta_of(ur * KG + KG - 1);
-            for (int c0 = 0; c0 < BM; c0 += 16) {
-              if (c0 >= nrows) break;
-              float va[16], vb[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) va[j] = vb[j] = 0.f;
-              for (int c = cf; c <= cl; ++c) {
-                const float* sl = slot_of(c);
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                  va[j] += __ldcg(sl + (c0 + j) * kMTile + m);
-                  if (C::kA > 1) vb[j] += __ldcg(sl + (BM + c0 + j) * kMTile + m);
-                }
-              }
-              consume(c0, va, vb);
-            }
-          }
+          consume(c0, va, vb);
         }
+        tc_fence_before();
+        mbar_arrive(&acce_bar[b]);
       }
 
       epi_bar();  // row metadata is reused by the next segment

@@ -56,8 +56,6 @@ struct EncodeXParams {
   int T, H;
   uint8_t* q;              // [kg][T][kTerms][64 bytes]: packed E2M1 codes (low nibble first)
   uint32_t* sf;            // [kg][T][kTerms]: E8M0 exponents of the 4 MX blocks of a K group
-  int32_t* zero_buf;       // GEMM arrival counters to clear (or null)
-  int zero_count;
 };
 cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream);
 
@@ -103,10 +101,7 @@ struct GemmParams {
   // down epilogue
   const float* topk_w;
   float* slots;            // f32 [T*k, H]: w_tj * y_tj per assignment
-  // split-K across persistent CTAs
   int grid;                // persistent CTAs (<= kMaxCtas)
-  float* partials;         // [2 * grid][kA * bm * 128] partial accumulators
-  int32_t* unit_cnt;       // [max_tiles * mt] arrivals per work unit
   uint32_t* status;
 };
 cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream);

@@ -254,22 +254,24 @@ def main():
     dn_bytes = touched * DOWN_BYTES_PER_EXPERT(H, I)
     alg_bytes = gu_bytes + dn_bytes
 
-    # rotate weight copies so the touched experts of every call come from HBM
+    # rotate copies of the whole layer input (expert weights, router weight, x) so the
+    # touched experts of every call come from HBM and nothing a real model would not
+    # find in L2 (another layer's router, another step's activations) is found there
     copies = max(1, min(16, math.ceil(4 * L2_BYTES / max(alg_bytes, 1))))
-    wsets = [(layer.w_gateup, layer.w_down)] + [(layer.w_gateup.clone(), layer.w_down.clone())
-                                               for _ in range(copies - 1)]
+    wsets = [(layer.w_gateup, layer.w_down, wr, x)] + [
+        (layer.w_gateup.clone(), layer.w_down.clone(), wr.clone(), x.clone()) for _ in range(copies - 1)]
     ws = layer.workspace(T)
 
     def call(i, events=None):
-        wgu, wd = wsets[i % copies]
+        wgu, wd, wr_i, x_i = wsets[i % copies]
         b = None if bias is None else bias.data_ptr()
         cs = torch.cuda.current_stream().cuda_stream
         if events is None:
-            st = L.moe_forward(x.data_ptr(), wr.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
+            st = L.moe_forward(x_i.data_ptr(), wr_i.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
                                ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, cs)
         else:
-            st = L.moe_forward_timed(x.data_ptr(), wr.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
-                                     ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, events, cs)
+            st = L.moe_forward_timed(x_i.data_ptr(), wr_i.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E,
+                                     k, ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, events, cs)
         if st != 0:
             raise RuntimeError(f"moe_forward failed: {L.moe_error_string(st).decode()}")
 
@@ -285,7 +287,7 @@ def main():
     # one CUDA graph per weight copy: a replay is one step (the layer runs inside a
     # captured decode step in the pages' engine); --eager times plain launches
     nk = 4  # stages bracketed by moe_forward_timed's events (MOE_FORWARD_STAGES)
-    names = ["encode_x", "route_topk_table", "gateup_swiglu", "down_combine"]
+    names = ["route_topk_table", "encode_x", "gateup_swiglu", "down_combine"]
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     graphs, tgraphs, tevents = [], [], []
@@ -312,7 +314,7 @@ def main():
             tevents.append(evs)
             eg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(eg, stream=side):
-                x.copy_(hx, non_blocking=True)
+                wsets[j][3].copy_(hx, non_blocking=True)
                 call(j)
                 hout.copy_(out, non_blocking=True)
             e2e_graphs.append(eg)
@@ -421,8 +423,9 @@ def main():
         "data": "synthetic",
         "config": {"workload": inp.name, "T": T, "H": H, "I": I, "E": E, "k": k,
                    "tile_rows": L.moe_tile_rows(T, k, E), "touched_experts": touched,
-                   "l2": f"{copies} rotating weight copies ({copies * alg_bytes / 1e6:.0f} MB touched per "
-                         f"rotation > 4x L2)", "parallelism": f"replicas x{world}"},
+                   "l2": f"{copies} rotating copies of weights, router weight and x "
+                         f"({copies * alg_bytes / 1e6:.0f} MB of experts touched per rotation > 4x L2)",
+                   "parallelism": f"replicas x{world}"},
         "us_per_call": us,
         "timing": "eager launches" if args.eager else "CUDA graph replay per step",
         "eager_us_per_call": eager_ms * 1e3,

@@ -173,10 +173,12 @@ int persistent_ctas() {
 
 // ------------------------------------------------------------------ stage bodies
 // Per-token activation encoding.
-int run_encode_x(const uint16_t* x, int T, int H, void* ws, const WsLayout& L, cudaStream_t stream) {
+int run_encode_x(const uint16_t* x, int T, int H, void* ws, const WsLayout& L, cudaStream_t stream,
+                 bool wait_at_end = false) {
   EncodeXParams q{};
   q.x = x;
   q.T = T; q.H = H;
+  q.wait_at_end = wait_at_end ? 1 : 0;
   q.q = ws_ptr<uint8_t>(ws, L.xt_q);
   q.sf = ws_ptr<uint32_t>(ws, L.xt_sf);
   return cuda_status(launch_encode_x(q, stream));
@@ -465,14 +467,15 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   auto mark = [&](int i) {
     if (events && record_event(events[i], s) != cudaSuccess) ev_ok = false;
   };
-  r.wait_at_end = 1;  // the encoding launch before it waits for the previous call
-  // stages: [0] encode x, [1] route + top-k + tile table, [2] gate/up, [3] down + combine
+  // stages: [0] route + top-k + tile table, [1] encode x, [2] gate/up, [3] down + combine.
+  // Routing goes first (it waits for the previous kernel); the encoding overlaps it
+  // and waits for it at its end, so that the gather after the encoding sees both.
   mark(0);
   if (!ev_ok) return MOE_ERR_INVALID_ARG;
-  st = run_encode_x(x, T, H, ws, L, s);
-  if (st != MOE_OK) return st;
-  mark(1);
   if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(1);
+  st = run_encode_x(x, T, H, ws, L, s, /*wait_at_end=*/true);
+  if (st != MOE_OK) return st;
   mark(2);
   st = run_gateup(perm, tiles, num_tiles, bm, w_gateup, T, H, I, E, k, ws, L, s);
   if (st != MOE_OK) return st;
@@ -500,7 +503,7 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
 
 int moe_forward_launches(int T, int H, int I, int E, int k) {
   if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
-  return 6;  // encode x, route + table, gather x, gate/up, down, combine
+  return 6;  // route + table, encode x, gather x, gate/up, down, combine
 }
 
 int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream) {

@@ -32,14 +32,19 @@ __device__ __forceinline__ float quad_max(float v) {
 // reads finite data.  The gate/up GEMM gathers these rows by perm (the permute
 // step), so each token is encoded once however many experts it is routed to.
 __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) {
-  ptx::pdl_wait();  // the previous layer call may still read this call's buffers
+  // the previous kernel may still write x or read this call's buffers, unless the
+  // launch before this one already waited for it
+  if (!p.wait_at_end) ptx::pdl_wait();
   ptx::pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
   const int nvec_pad = ((p.H + 63) / 64) * 8;  // 8-value vectors per row, padded to 64 values
   const int nchunks = (nvec_pad + 31) / 32;
   const int t = (int)(gw / nchunks);
-  if (t >= p.T) return;
+  if (t >= p.T) {
+    if (p.wait_at_end) ptx::pdl_wait();
+    return;
+  }
   const int chunk = (int)(gw - (long long)t * nchunks);
   const int v = chunk * 32 + lane;
   const int nvec = p.H / 8;
@@ -85,6 +90,7 @@ __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) 
       if ((lane & 15) == 0) p.sf[row] = sfw;
     }
   }
+  if (p.wait_at_end) ptx::pdl_wait();
 }
 
 cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream) {

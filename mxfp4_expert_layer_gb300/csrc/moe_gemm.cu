@@ -223,17 +223,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
       auto tx_bytes = [&]() -> uint32_t {
         return C::kConcat ? C::kTxNoB + (uint32_t)(kTerms << boxq) * (uint32_t)C::kKBytes : C::kTxBytes;
       };
+      // Weights are read once per call.  When more units than CTAs stream them, mark
+      // them evict-first so that the activation tiles every unit of a tile re-reads
+      // stay in L2; a single wave keeps the normal policy (faster there).
+      const uint64_t w_policy = U > grid ? l2_policy_evict_first() : l2_policy_evict_normal();
       auto load_a = [&](int s) {
         for (int j = 0; j < C::kA; ++j) {
           // gate/up: group j of M tile mt; down: M tile mt (or 2 mt + j), group 0.  An M
           // tile past the matrix reads zeros (TMA fill) and scales of the last tile.
           const int mrow = GATEUP ? mt : (MPAIR ? 2 * mt + j : mt);
           const int grp = GATEUP ? j : 0;
-          tma_load_3d(a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile, expert * p.w_groups + grp);
+          tma_load_3d_hint(a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile,
+                           expert * p.w_groups + grp, w_policy);
           const int msf = min(mrow, p.w_mt - 1);
           const uint8_t* wsf =
               p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)p.kg_sf * kSfAtomBytes;
-          bulk_load(sf_a(s, j), wsf + (size_t)kk * C::kAtoms * kSfAtomBytes, C::kAtoms * kSfAtomBytes, &full_bar[s]);
+          bulk_load_hint(sf_a(s, j), wsf + (size_t)kk * C::kAtoms * kSfAtomBytes, C::kAtoms * kSfAtomBytes,
+                         &full_bar[s], w_policy);
         }
       };
       auto load_b = [&](int s, int b_tile_idx, int b_kk, int q) {

@@ -38,7 +38,6 @@ struct RouteParams {
   float* topk_w;            // f32 [T, k]
   uint32_t* sync;           // arrival counters [ceil(T/8) + 1], zero between calls
   int build_table;          // also build the tile table (last block)
-  int wait_at_end;          // dependency wait in the table builder only (needs build_table)
   int bm;
   int32_t *counts, *offsets, *perm, *inv_perm, *num_tiles;
   TileEntry* tiles;
@@ -56,6 +55,8 @@ struct EncodeXParams {
   int T, H;
   uint8_t* q;              // [kg][T][kTerms][64 bytes]: packed E2M1 codes (low nibble first)
   uint32_t* sf;            // [kg][T][kTerms]: E8M0 exponents of the 4 MX blocks of a K group
+  int wait_at_end;         // dependency wait after the encoding (the launch before it already
+                           // waited for earlier work), so this launch completes after that one
 };
 cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream);
 

@@ -46,44 +46,26 @@ __device__ __forceinline__ bool topk_better(float v1, int i1, float v2, int i2) 
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
-// Block-wide exclusive scan of one int per thread (blockDim.x == 256).
-__device__ int block_exclusive_scan_256(int v, int* scratch /* >= 8 ints */, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    int o = __shfl_up_sync(0xffffffffu, incl, d);
-    if (lane >= d) incl += o;
-  }
-  if (lane == 31) scratch[warp] = incl;
-  __syncthreads();
-  int warp_off = 0, sum = 0;
-#pragma unroll
-  for (int w = 0; w < kRouteWarps; ++w) {
-    int s = scratch[w];
-    if (w < warp) warp_off += s;
-    sum += s;
-  }
-  __syncthreads();
-  if (total) *total = sum;
-  return warp_off + incl - v;
-}
-
 }  // namespace
 
 // Deterministic counting sort of the assignments by expert, stable in t*k+j,
 // executed by one block of 256 threads.  Each warp owns a contiguous chunk of
 // assignments and a private histogram row; lanes with equal experts are grouped
-// with __match_any_sync, so no atomics are used anywhere.  kSharedIdx: the top-k
-// indices are in this block's shared memory (else global, read through L2).
+// with __match_any_sync, so no atomics are used anywhere.  One warp turns the
+// histograms into counts, row offsets, tile entries and per-warp bases (both
+// scans over experts in one pass), so the whole build takes three block barriers.
+// kSharedIdx: the top-k indices are in this block's shared memory (else global,
+// read through L2).
 template <bool kSharedIdx = false>
 __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, int E, int bm, int32_t* counts,
                                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, TileEntry* tiles,
                                        int32_t* num_tiles, uint32_t* status) {
   __shared__ int hist[kRouteWarps][kMaxExperts];
-  __shared__ int scan_scratch[kRouteWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kRouteWarps * kMaxExperts; i += kRouteThreads) (&hist[0][0])[i] = 0;
+  if (tid < E) {
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; ++w) hist[w][tid] = 0;
+  }
   __syncthreads();
   const int chunk = ceil_div(Tk, kRouteWarps);
   const int a_begin = warp * chunk;
@@ -104,24 +86,62 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
     if (e >= 0 && (grp & lt_mask) == 0) hist[warp][e] += __popc(grp);
   }
   __syncthreads();
-  // phase 2: counts, offsets (exclusive scan over experts), per-warp bases
-  int cnt = 0;
-  if (tid < E) {
-    for (int w = 0; w < kRouteWarps; ++w) cnt += hist[w][tid];
-  }
-  int total = 0;
-  const int off = block_exclusive_scan_256(tid < E ? cnt : 0, scan_scratch, &total);
-  if (tid < E) {
-    counts[tid] = cnt;
-    offsets[tid] = off;
-    int run = off;
-    for (int w = 0; w < kRouteWarps; ++w) {
-      const int h = hist[w][tid];
-      hist[w][tid] = run;  // becomes the next free sorted row of (warp, expert)
-      run += h;
+  // phase 2 (warp 0): lane l owns experts [l*per, l*per + per); counts, then one
+  // warp scan of (rows, tiles) gives each expert's first sorted row and first tile
+  if (warp == 0) {
+    const int per = ceil_div(E, 32);
+    const int e0 = lane * per, e1 = min(E, e0 + per);
+    int rows = 0, ntl = 0;
+    for (int e = e0; e < e1; ++e) {
+      int c = 0;
+#pragma unroll
+      for (int w = 0; w < kRouteWarps; ++w) c += hist[w][e];
+      rows += c;
+      ntl += ceil_div(c, bm);
+    }
+    int rows_incl = rows, ntl_incl = ntl;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int ro = __shfl_up_sync(0xffffffffu, rows_incl, d);
+      const int to = __shfl_up_sync(0xffffffffu, ntl_incl, d);
+      if (lane >= d) {
+        rows_incl += ro;
+        ntl_incl += to;
+      }
+    }
+    int off = rows_incl - rows, t0 = ntl_incl - ntl;
+    for (int e = e0; e < e1; ++e) {
+      int h[kRouteWarps], c = 0;
+#pragma unroll
+      for (int w = 0; w < kRouteWarps; ++w) {
+        h[w] = hist[w][e];
+        c += h[w];
+      }
+      counts[e] = c;
+      offsets[e] = off;
+      int run = off;
+#pragma unroll
+      for (int w = 0; w < kRouteWarps; ++w) {
+        hist[w][e] = run;  // becomes the next free sorted row of (warp, expert)
+        run += h[w];
+      }
+      const int nt = ceil_div(c, bm);
+      for (int q = 0; q < nt; ++q) {
+        TileEntry te;
+        te.expert = e;
+        te.row_begin = off + q * bm;
+        te.n_rows = min(bm, c - q * bm);
+        te.pad_row = (t0 + q) * bm;
+        tiles[t0 + q] = te;
+      }
+      off += c;
+      t0 += nt;
+    }
+    if (lane == 31) {
+      offsets[E] = rows_incl;
+      *num_tiles = ntl_incl;
     }
   }
-  if (tid == 0) offsets[E] = total;
   __syncthreads();
   // phase 3: scatter assignments to their sorted rows (stable in a)
   for (int base = a_begin; base < a_end; base += 32) {
@@ -142,30 +162,14 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
     }
     __syncwarp();
   }
-  __syncthreads();
-  // phase 4: tiles, experts ascending
-  const int nt = tid < E ? ceil_div(cnt, bm) : 0;
-  int ntotal = 0;
-  const int t0 = block_exclusive_scan_256(nt, scan_scratch, &ntotal);
-  if (tid < E) {
-    for (int q = 0; q < nt; ++q) {
-      TileEntry te;
-      te.expert = tid;
-      te.row_begin = off + q * bm;
-      te.n_rows = min(bm, cnt - q * bm);
-      te.pad_row = (t0 + q) * bm;
-      tiles[t0 + q] = te;
-    }
-  }
-  if (tid == 0) *num_tiles = ntotal;
 }
 
 // Top-k of one token by one warp: each lane holds logits e = lane + 32*i; k rounds
 // of a warp arg-max on (value desc, index asc).  Softmax over the k selected.
 // kShared: the logits row is in shared memory (else global, read through L2).
+// Returns the j-th selected expert in lane j < k.
 template <bool kShared = false>
-__device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out,
-                                  int32_t* idx_copy = nullptr) {
+__device__ int topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out) {
   const int lane = threadIdx.x & 31;
   float v[kMaxExperts / 32];
 #pragma unroll
@@ -209,8 +213,8 @@ __device__ void topk_softmax_warp(const float* __restrict__ lg_row, int E, int k
   if (lane < k) {
     idx_out[lane] = my_i;
     w_out[lane] = ex / s;
-    if (idx_copy) idx_copy[lane] = my_i;
   }
+  return my_i;
 }
 
 // grid = (token groups of 8, expert slices); block = 256 threads.  kRouterVecs:
@@ -221,11 +225,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   extern __shared__ __align__(16) uint8_t route_smem[];
   __shared__ int s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // The previous kernel on the stream may still read this call's outputs: wait for
-  // it first -- unless the launch before this one (the activation encoding of the
-  // same call) already waited for everything earlier; then only the table builder
-  // waits, at the end, so that this launch completes after that one.
-  if (!p.wait_at_end) pdl_wait();
+  // The previous kernel on the stream may still write x or read this call's outputs
+  pdl_wait();
   pdl_launch_dependents();
   const int g = blockIdx.x;
   const int t0 = g * kTokensPerGroup;
@@ -352,18 +353,20 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     if (!s_last) return;
     __threadfence();
   }
-  if (p.wait_at_end) pdl_wait();
   build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
                          p.num_tiles, p.status);
 }
 
 // ------------------------------------------------------------------ decode routing
 // Few tokens (T <= 64): one cluster of kClusterCtas CTAs does the whole routing with
-// no global atomics.  CTA r computes the partial logits of every token and expert
-// over its slice of the hidden dimension on the tensor cores (mma.sync bf16, fp32
-// accumulate); after a cluster barrier CTA r sums the kClusterCtas partials of
-// tokens 8r..8r+7 in rank order (reading its peers' shared memory), selects their
-// top-k, and after a second barrier CTA 0 builds the tile table.
+// no global atomics and no full cluster barrier after the start.  CTA r computes
+// the partial logits of every token and expert over its slice of the hidden
+// dimension on the tensor cores (mma.sync bf16, fp32 accumulate) and pushes the
+// partials of tokens 8q..8q+7 into CTA q's shared memory (st.async, counted on
+// CTA q's mbarrier).  CTA q sums the kClusterCtas partials in rank order, selects
+// the top-k of its tokens and pushes the indices to CTA 0, which builds the tile
+// table.  A CTA's shared memory is written by its peers only before its own wait
+// on the matching barrier returns, so every CTA may exit right after its last push.
 constexpr int kClusterCtas = 8;
 constexpr int kClusterMaxTokens = kClusterCtas * kTokensPerGroup;
 
@@ -383,10 +386,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-// Shared-memory layout of the cluster routing kernel for (T, H, E).
+constexpr int kMmaIlp = 4;  // 8-expert column blocks per warp pass (one A fragment serves all)
+
+// Shared-memory layout of the cluster routing kernel for (T, H, E, k).  A warp
+// item is (16-token row block, kMmaIlp column blocks); when there are fewer items
+// than warps, each item's K range is split over nsplit warps whose partial sums
+// meet in the split area.
 struct ClusterRouteSmem {
   int mrows, erows, pitch;        // staged x rows (multiple of 16), router rows (multiple of 8), row bytes
-  size_t x_off, w_off, part_off, lg_off, idx_off, bar_off, total;
+  int nitems, nsplit;
+  size_t x_off, w_off, split_off, recv_off, lg_off, bias_off, idx_off, bar_off, total;
 };
 __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int E, int k) {
   ClusterRouteSmem L;
@@ -395,58 +404,77 @@ __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int
   L.mrows = ((T + 15) / 16) * 16;
   L.erows = ((E + 7) / 8) * 8;
   L.pitch = kmax * 2 + 16;  // +16 bytes: rows fall in different banks for ldmatrix
+  const int ngroups = (L.erows / 8 + kMmaIlp - 1) / kMmaIlp;
+  L.nitems = (L.mrows / 16) * ngroups;
+  L.nsplit = 1;
+  while (L.nsplit * 2 * L.nitems <= kRouteWarps) L.nsplit *= 2;
   L.x_off = 0;
   L.w_off = L.x_off + (size_t)L.mrows * L.pitch;
-  L.part_off = L.w_off + (size_t)L.erows * L.pitch;
-  L.lg_off = L.part_off + sizeof(float) * (size_t)L.mrows * L.erows;
-  L.idx_off = L.lg_off + sizeof(float) * (size_t)kTokensPerGroup * L.erows;
+  L.split_off = L.w_off + (size_t)L.erows * L.pitch;
+  const size_t split_bytes = L.nsplit > 1 ? sizeof(float) * (size_t)L.nsplit * L.mrows * L.erows : 0;
+  L.recv_off = L.split_off + split_bytes;  // [kClusterCtas][kTokensPerGroup][erows] partials
+  L.lg_off = L.recv_off + sizeof(float) * (size_t)kClusterCtas * kTokensPerGroup * L.erows;
+  L.bias_off = L.lg_off + sizeof(float) * (size_t)kTokensPerGroup * L.erows;
+  L.idx_off = L.bias_off + sizeof(float) * (size_t)L.erows;
   L.bar_off = L.idx_off + ((sizeof(int32_t) * (size_t)T * k + 15) / 16) * 16;
-  L.total = L.bar_off + 16;
+  L.total = L.bar_off + 32;
   return L;
 }
 
 constexpr uint64_t kRouteWaitLimit = 1000000000ull;  // ns a bounded wait may take (1 s)
-constexpr int kMmaIlp = 4;                            // independent output tiles per warp pass
 
 __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThreads)
     route_cluster_kernel(RouteParams p) {
   extern __shared__ __align__(16) uint8_t rc_smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (!p.wait_at_end) pdl_wait();
-  pdl_launch_dependents();
   namespace cg = cooperative_groups;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = (int)cluster.block_rank();
+  const int rank = (int)cg::this_cluster().block_rank();
   const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k);
   uint8_t* xs = rc_smem + L.x_off;
   uint8_t* wsm = rc_smem + L.w_off;
-  float* part = reinterpret_cast<float*>(rc_smem + L.part_off);  // [mrows][erows]
-  float* lg = reinterpret_cast<float*>(rc_smem + L.lg_off);      // [8][erows]
-  int32_t* sidx = reinterpret_cast<int32_t*>(rc_smem + L.idx_off);  // [T*k], used in CTA 0
+  float* split = reinterpret_cast<float*>(rc_smem + L.split_off);  // [nsplit][mrows][erows]
+  float* recv = reinterpret_cast<float*>(rc_smem + L.recv_off);    // [src rank][token - 8*rank][erows]
+  float* lg = reinterpret_cast<float*>(rc_smem + L.lg_off);        // [8][erows]
+  float* sbias = reinterpret_cast<float*>(rc_smem + L.bias_off);   // [erows]
+  int32_t* sidx = reinterpret_cast<int32_t*>(rc_smem + L.idx_off); // [T*k], filled in CTA 0
   uint64_t* bar = reinterpret_cast<uint64_t*>(rc_smem + L.bar_off);
+  uint64_t* bar_stage = bar;      // this CTA's operand slices have landed
+  uint64_t* bar_part = bar + 1;   // every peer's partials of this CTA's tokens have landed
+  uint64_t* bar_idx = bar + 2;    // (CTA 0) every token's top-k indices have landed
+  const int t_own = rank * kTokensPerGroup;
+  const int n_own = max(0, min(kTokensPerGroup, p.T - t_own));
+  const bool builds = rank == 0 && p.build_table;
 
   // this CTA's slice of the hidden dimension, in steps of 16
   const int ksteps = p.H / 16;
   const int ks0 = rank * ksteps / kClusterCtas, ks1 = (rank + 1) * ksteps / kClusterCtas;
   const uint32_t slice_bytes = (uint32_t)(ks1 - ks0) * 32;
-  // stage the slices of x rows and router rows with one bulk copy per row; rows past
-  // T (x) or E (router) are zero-filled
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(bar_stage, 1);
+    mbar_init(bar_part, 1);
+    mbar_init(bar_idx, 1);
     fence_mbar_init();
+    if (n_own > 0) mbar_arrive_expect_tx(bar_part, (uint32_t)(kClusterCtas * n_own * L.erows * sizeof(float)));
+    if (builds) mbar_arrive_expect_tx(bar_idx, (uint32_t)(p.T * p.k * sizeof(int32_t)));
+    if (slice_bytes > 0) mbar_arrive_expect_tx(bar_stage, slice_bytes * (uint32_t)(p.T + p.E));
   }
   __syncthreads();
-  // the copies first (their latency is the long pole), then the zero rows they never touch
+  cluster_arrive_release();  // this CTA's barriers are initialised
+  // Router rows and bias first: weights, never written by the launches before this
+  // one.  Then the dependency wait, and only after it the activation rows (x may
+  // come from the previous kernel) and every write.
   if (slice_bytes > 0) {
-    if (tid == 0) mbar_arrive_expect_tx(bar, slice_bytes * (uint32_t)(p.T + p.E));
-    for (int r = tid; r < p.T + p.E; r += kRouteThreads) {
-      if (r < p.T)
-        bulk_load(xs + (size_t)r * L.pitch, p.x + (size_t)r * p.H + ks0 * 16, slice_bytes, bar);
-      else
-        bulk_load(wsm + (size_t)(r - p.T) * L.pitch, p.w_router + (size_t)(r - p.T) * p.H + ks0 * 16, slice_bytes,
-                  bar);
-    }
+    for (int r = tid; r < p.E; r += kRouteThreads)
+      bulk_load(wsm + (size_t)r * L.pitch, p.w_router + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
   }
+  if (p.bias && n_own > 0 && tid < p.E) sbias[tid] = __ldg(p.bias + tid);
+  pdl_wait();
+  pdl_launch_dependents();
+  if (slice_bytes > 0) {
+    for (int r = tid; r < p.T; r += kRouteThreads)
+      bulk_load(xs + (size_t)r * L.pitch, p.x + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
+  }
+  // rows the copies never touch: x rows past T, router rows past E
   for (int i = tid; i < (L.mrows - p.T) * (L.pitch / 16); i += kRouteThreads) {
     const int r = p.T + i / (L.pitch / 16), c = i % (L.pitch / 16);
     *reinterpret_cast<uint4*>(xs + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
@@ -455,17 +483,23 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     const int r = p.E + i / (L.pitch / 16), c = i % (L.pitch / 16);
     *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
   }
-  if (slice_bytes > 0 && !mbar_wait_bounded(bar, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
-  __syncthreads();  // zero rows written by other threads
-  // partial logits: a warp takes one 16-token row block and kMmaIlp consecutive
-  // 8-expert column blocks, so each A fragment loaded from shared memory serves
-  // kMmaIlp MMAs (shared-memory bandwidth, not the tensor pipe, bounds this phase)
+  if (slice_bytes > 0 && !mbar_wait_bounded(bar_stage, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
+  __syncthreads();  // zero rows and the bias written by other threads
+  cluster_wait_acquire();  // every peer's barriers are initialised: pushes may start
+
+  // shared::cluster addresses of every owner's receive area and barrier
+  const uint32_t recv_u = smem_u32(recv), bar_part_u = smem_u32(bar_part);
+  // partial logits: a warp takes one (row block, column group) item, or one K
+  // share of it; each A fragment loaded from shared memory serves kMmaIlp MMAs
   {
     const int ntn = L.erows / 8;
-    const int ngroups = (ntn + kMmaIlp - 1) / kMmaIlp, nitems = (L.mrows / 16) * ngroups;
+    const int ngroups = (ntn + kMmaIlp - 1) / kMmaIlp;
+    const int kn = ks1 - ks0;
     const uint32_t xs_u = smem_u32(xs), ws_u = smem_u32(wsm);
-    for (int item = warp; item < nitems; item += kRouteWarps) {
+    for (int job = warp; job < L.nitems * L.nsplit; job += kRouteWarps) {
+      const int item = job / L.nsplit, sp = job - item * L.nsplit;
       const int mi = item / ngroups, n0 = (item - mi * ngroups) * kMmaIlp;
+      const int kk0 = sp * kn / L.nsplit, kk1 = (sp + 1) * kn / L.nsplit;
       float c[kMmaIlp][4];
       uint32_t b_addr[kMmaIlp];
       // ldmatrix row addresses: A rows mi*16 + lane%16, column half lane/16; B rows
@@ -477,7 +511,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
         b_addr[q] = ws_u + (uint32_t)((ni * 8 + (lane & 7)) * L.pitch + ((lane >> 3) & 1) * 16);
         c[q][0] = c[q][1] = c[q][2] = c[q][3] = 0.f;
       }
-      for (int kk = 0; kk < ks1 - ks0; ++kk) {
+      for (int kk = kk0; kk < kk1; ++kk) {
         uint32_t a[4];
         ldmatrix_x4(a, a_addr + kk * 32);
 #pragma unroll
@@ -487,48 +521,72 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
           mma_bf16_16816(c[q], a, b);
         }
       }
+      // fragment rows r0 = mi*16 + lane/4 and r0 + 8, columns ni*8 + 2*(lane%4) + {0,1}
+      const int r0 = mi * 16 + (lane >> 2);
 #pragma unroll
       for (int q = 0; q < kMmaIlp; ++q) {
         const int ni = n0 + q;
         if (ni >= ntn) break;
-        const int r0 = mi * 16 + (lane >> 2), c0 = ni * 8 + (lane & 3) * 2;
-        part[r0 * L.erows + c0] = c[q][0];
-        part[r0 * L.erows + c0 + 1] = c[q][1];
-        part[(r0 + 8) * L.erows + c0] = c[q][2];
-        part[(r0 + 8) * L.erows + c0 + 1] = c[q][3];
+        const int c0 = ni * 8 + (lane & 3) * 2;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = r0 + 8 * h;
+          if (L.nsplit > 1) {
+            *reinterpret_cast<float2*>(split + ((size_t)sp * L.mrows + r) * L.erows + c0) =
+                make_float2(c[q][2 * h], c[q][2 * h + 1]);
+          } else if (r < p.T) {
+            const uint32_t owner = (uint32_t)(r / kTokensPerGroup);
+            const uint32_t off = (uint32_t)(((rank * kTokensPerGroup + r % kTokensPerGroup) * L.erows + c0) * 4);
+            st_async_v2_f32(mapa_shared(recv_u + off, owner), c[q][2 * h], c[q][2 * h + 1],
+                            mapa_shared(bar_part_u, owner));
+          }
+        }
+      }
+    }
+    if (L.nsplit > 1) {
+      // the K shares of each partial, summed in share order, then pushed
+      __syncthreads();
+      const int c4n = L.erows / 4;
+      for (int i = tid; i < p.T * c4n; i += kRouteThreads) {
+        const int r = i / c4n, c4 = i - r * c4n;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < L.nsplit; ++sp) {
+          const float4 u = *reinterpret_cast<const float4*>(split + ((size_t)sp * L.mrows + r) * L.erows + 4 * c4);
+          v.x += u.x;
+          v.y += u.y;
+          v.z += u.z;
+          v.w += u.w;
+        }
+        const uint32_t owner = (uint32_t)(r / kTokensPerGroup);
+        const uint32_t off = (uint32_t)(((rank * kTokensPerGroup + r % kTokensPerGroup) * L.erows + 4 * c4) * 4);
+        st_async_v4_f32(mapa_shared(recv_u + off, owner), v, mapa_shared(bar_part_u, owner));
       }
     }
   }
-  cluster.sync();  // every CTA's partials are complete and visible in the cluster
-  // logits of tokens 8*rank .. 8*rank+7: partials summed in rank order
-  const int t0 = rank * kTokensPerGroup;
-  for (int i = tid; i < kTokensPerGroup * p.E; i += kRouteThreads) {
-    const int r = i / p.E, e = i - r * p.E, t = t0 + r;
-    if (t < p.T) {
+  // logits of this CTA's tokens: partials summed in rank order, then the bias
+  if (n_own > 0) {
+    if (!mbar_wait_cluster_bounded(bar_part, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
+    for (int i = tid; i < n_own * p.E; i += kRouteThreads) {
+      const int r = i / p.E, e = i - r * p.E;
       float sum = 0.f;
 #pragma unroll
-      for (int b = 0; b < kClusterCtas; ++b) {
-        const float* pb = cluster.map_shared_rank(part, b);
-        sum += pb[t * L.erows + e];
-      }
-      if (p.bias) sum += __ldg(p.bias + e);
+      for (int b = 0; b < kClusterCtas; ++b) sum += recv[(b * kTokensPerGroup + r) * L.erows + e];
+      if (p.bias) sum += sbias[e];
       lg[r * L.erows + e] = sum;
-      p.logits[(size_t)t * p.E + e] = sum;
+      p.logits[(size_t)(t_own + r) * p.E + e] = sum;
+    }
+    __syncthreads();
+    // top-k of one token per warp; the indices also go to CTA 0
+    if (warp < n_own) {
+      const int t = t_own + warp;
+      const int sel = topk_softmax_warp<true>(lg + warp * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k,
+                                              p.topk_w + (size_t)t * p.k);
+      if (p.build_table && lane < p.k)
+        st_async_b32(mapa_shared(smem_u32(sidx + t * p.k + lane), 0), (uint32_t)sel, mapa_shared(smem_u32(bar_idx), 0));
     }
   }
-  __syncthreads();
-  // top-k of one token per warp; the indices also go to CTA 0's shared memory, where
-  // the tile table is built
-  if (warp < kTokensPerGroup && t0 + warp < p.T) {
-    const int t = t0 + warp;
-    int32_t* idx_cta0 = cluster.map_shared_rank(sidx, 0) + (size_t)t * p.k;
-    topk_softmax_warp<true>(lg + warp * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k, p.topk_w + (size_t)t * p.k,
-                            p.build_table ? idx_cta0 : nullptr);
-  }
-  // every CTA is done with its peers' shared memory and has delivered its top-k
-  cluster.sync();
-  if (rank != 0 || !p.build_table) return;
-  if (p.wait_at_end) pdl_wait();
+  if (!builds) return;
+  if (!mbar_wait_cluster_bounded(bar_idx, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
   build_tile_table_block<true>(sidx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
                                p.num_tiles, p.status);
 }

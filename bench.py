@@ -284,9 +284,13 @@ def main():
                           "status": layer.device_status(T)}))
         return
 
-    # one CUDA graph per weight copy: a replay is one step (the layer runs inside a
-    # captured decode step in the pages' engine); --eager times plain launches
+    # the layer runs inside a captured decode step in the pages' engine: one CUDA
+    # graph holds the calls of every weight copy in sequence (consecutive layers of
+    # a step, each with its own weights), so a layer's first launch overlaps the
+    # previous layer's last as it would in that step.  Single-call graphs serve the
+    # remainder of K steps and the per-stage split; --eager times plain launches.
     nk = 4  # stages bracketed by moe_forward_timed's events (MOE_FORWARD_STAGES)
+    step_calls = copies * math.ceil(8 / copies)  # layer calls per step graph: >= 8, whole rotations
     names = ["route_topk_table", "encode_x", "gateup_swiglu", "down_combine"]
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -318,6 +322,10 @@ def main():
                 call(j)
                 hout.copy_(out, non_blocking=True)
             e2e_graphs.append(eg)
+        step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(step_graph, stream=side):
+            for j in range(step_calls):
+                call(j)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -326,6 +334,17 @@ def main():
             call(i)
         else:
             graphs[i % copies].replay()
+
+    def run_steps(n):
+        # n layer calls: whole multi-call graphs, then single-call graphs for the rest
+        if args.eager:
+            for s_ in range(n):
+                call(s_)
+            return
+        for _ in range(n // step_calls):
+            step_graph.replay()
+        for s_ in range(n % step_calls):
+            graphs[s_ % copies].replay()
 
     clocks = ClockSampler(local)
     # pre-warm: bring clocks up (~0.5 s of steps), then the W warm-up steps
@@ -336,15 +355,12 @@ def main():
             step(i)
             i += 1
         torch.cuda.synchronize()
-    for _ in range(args.warmup):
-        step(i)
-        i += 1
+    run_steps(args.warmup)
     barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for s_ in range(args.steps):
-        step(i + s_)
+    run_steps(args.steps)
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -427,7 +443,9 @@ def main():
                          f"({copies * alg_bytes / 1e6:.0f} MB of experts touched per rotation > 4x L2)",
                    "parallelism": f"replicas x{world}"},
         "us_per_call": us,
-        "timing": "eager launches" if args.eager else "CUDA graph replay per step",
+        "timing": "eager launches" if args.eager else
+                  f"CUDA graphs of {step_calls} consecutive layer calls cycling over {copies} weight "
+                  f"copies, replayed",
         "eager_us_per_call": eager_ms * 1e3,
         "layer_hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "layer_roofline_frac": alg_bytes / (ms * 1e-3) / 1e9 / peak,

@@ -190,9 +190,10 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* router
 /* moe_forward_timed: moe_forward that also records caller-created CUDA events
  * (cudaEvent_t, passed as void*) on `stream` around its MOE_FORWARD_STAGES stages:
  * events[i] just before stage i and events[MOE_FORWARD_STAGES] after the last one.
- * The stages are route + top-k + tile table, the per-token encoding of x, gate/up
- * + SwiGLU (two launches: the gather of the encoded rows by perm, then the GEMM),
- * and down + combine (two launches).  It gives the per-stage time split ("Where the
+ * The stages are route + top-k + tile table, the per-token encoding of x (which
+ * waits for routing and writes the tile order itself: the permute step), the
+ * gate/up + SwiGLU GEMM, and down + combine (two launches).  It gives the
+ * per-stage time split ("Where the
  * time went": per-section times of a decode step).  events must hold
  * MOE_FORWARD_STAGES + 1 valid events.                                            */
 #define MOE_FORWARD_STAGES 4
@@ -202,7 +203,7 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
                       void* const* events, moe_stream_t stream);
 
 /* Number of kernels moe_forward launches for a shape (for launch accounting):
- * route + top-k + table, encode x, gather x, gate/up, down, combine.               */
+ * route + top-k + table, encode + permute x, gate/up, down, combine.             */
 int moe_forward_launches(int T, int H, int I, int E, int k);
 
 /* Synchronises `stream`, reads the workspace's device status word into *status

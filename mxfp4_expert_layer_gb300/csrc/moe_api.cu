@@ -173,21 +173,37 @@ int persistent_ctas() {
 
 // ------------------------------------------------------------------ stage bodies
 // Per-token activation encoding.
-int run_encode_x(const uint16_t* x, int T, int H, void* ws, const WsLayout& L, cudaStream_t stream,
-                 bool wait_at_end = false) {
+int run_encode_x(const uint16_t* x, int T, int H, void* ws, const WsLayout& L, cudaStream_t stream) {
   EncodeXParams q{};
   q.x = x;
   q.T = T; q.H = H;
-  q.wait_at_end = wait_at_end ? 1 : 0;
   q.q = ws_ptr<uint8_t>(ws, L.xt_q);
   q.sf = ws_ptr<uint32_t>(ws, L.xt_sf);
   return cuda_status(launch_encode_x(q, stream));
 }
 
-// The permute (gather of the encoded rows into tile order) and the gate/up GEMM; x
-// must already be encoded in the workspace (run_encode_x).
-int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm, const void* w_gateup,
-               int T, int H, int I, int E, int k, void* ws, const WsLayout& L, cudaStream_t stream) {
+// Per-token activation encoding that overlaps the routing launch before it, waits
+// for it, and writes the encoded rows straight into tile order (the permute step).
+int run_encode_permute_x(const uint16_t* x, const int32_t* idx, int T, int H, int E, int k, int bm, void* ws,
+                         const WsLayout& L, cudaStream_t stream) {
+  EncodeXParams q{};
+  q.x = x;
+  q.T = T; q.H = H;
+  q.wait_at_end = 1;
+  q.scatter = 1;
+  q.topk_idx = idx;
+  q.inv_perm = ws_ptr<int32_t>(ws, L.inv_perm);
+  q.offsets = ws_ptr<int32_t>(ws, L.offsets);
+  q.tile_first = ws_ptr<int32_t>(ws, L.tile_first);
+  q.E = E; q.k = k; q.bm = bm; q.max_tiles = L.max_tiles; q.kg_tile = L.kg_h;
+  q.q_tile = ws_ptr<uint8_t>(ws, L.x_q);
+  q.sf_tile = ws_ptr<uint8_t>(ws, L.x_sf);
+  return cuda_status(launch_encode_x(q, stream));
+}
+
+// The permute (gather of the token-order encoded rows into tile order).
+int run_gather_x(const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm, int T, int H, int k,
+                 void* ws, const WsLayout& L, cudaStream_t stream) {
   GatherXParams gx{};
   gx.xt_q = ws_ptr<uint8_t>(ws, L.xt_q);
   gx.xt_sf = ws_ptr<uint32_t>(ws, L.xt_sf);
@@ -197,14 +213,18 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   gx.T = T; gx.k = k; gx.bm = bm; gx.max_tiles = L.max_tiles; gx.kg = L.kg_h;
   gx.q = ws_ptr<uint8_t>(ws, L.x_q);
   gx.sf = ws_ptr<uint8_t>(ws, L.x_sf);
-  if (launch_gather_x(gx, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return cuda_status(launch_gather_x(gx, stream));
+}
 
+// The gate/up GEMM + SwiGLU over x in tile order (run_gather_x or run_encode_permute_x).
+int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm, const void* w_gateup,
+               int T, int H, int I, int E, int k, void* ws, const WsLayout& L, cudaStream_t stream) {
   const PreparedLayout P = make_prepared_layout(E, 2 * I, H, 2);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_gateup, P, bm)) return MOE_ERR_CUDA;
-  if (!act_map(g.tm_act, gx.q, H, L.max_tiles, bm)) return MOE_ERR_CUDA;
+  if (!act_map(g.tm_act, ws_ptr<uint8_t>(ws, L.x_q), H, L.max_tiles, bm)) return MOE_ERR_CUDA;
   g.w_sf = static_cast<const uint8_t*>(w_gateup) + P.scales_off;
-  g.act_sf = gx.sf;
+  g.act_sf = ws_ptr<uint8_t>(ws, L.x_sf);
   g.tiles = tiles;
   g.num_tiles = num_tiles;
   g.perm = perm;
@@ -391,6 +411,8 @@ int moe_mxfp4_gateup_swiglu(const uint16_t* x, const int32_t* perm, const int32_
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   st = run_encode_x(x, T, H, workspace, L, s);
   if (st != MOE_OK) return st;
+  st = run_gather_x(perm, reinterpret_cast<const TileEntry*>(tiles), num_tiles, bm, T, H, k, workspace, L, s);
+  if (st != MOE_OK) return st;
   return run_gateup(perm, reinterpret_cast<const TileEntry*>(tiles), num_tiles, bm, w_gateup, T, H, I, E, k,
                     workspace, L, s);
 }
@@ -463,18 +485,19 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   r.inv_perm = ws_ptr<int32_t>(ws, L.inv_perm);
   r.tiles = tiles;
   r.num_tiles = num_tiles;
+  r.tile_first = ws_ptr<int32_t>(ws, L.tile_first);
   bool ev_ok = true;
   auto mark = [&](int i) {
     if (events && record_event(events[i], s) != cudaSuccess) ev_ok = false;
   };
-  // stages: [0] route + top-k + tile table, [1] encode x, [2] gate/up, [3] down + combine.
-  // Routing goes first (it waits for the previous kernel); the encoding overlaps it
-  // and waits for it at its end, so that the gather after the encoding sees both.
+  // stages: [0] route + top-k + tile table, [1] encode + permute x, [2] gate/up,
+  // [3] down + combine.  Routing goes first (it waits for the previous kernel); the
+  // encoding overlaps it, waits for it at its end and writes the tile order.
   mark(0);
   if (!ev_ok) return MOE_ERR_INVALID_ARG;
   if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(1);
-  st = run_encode_x(x, T, H, ws, L, s, /*wait_at_end=*/true);
+  st = run_encode_permute_x(x, idx, T, H, E, k, bm, ws, L, s);
   if (st != MOE_OK) return st;
   mark(2);
   st = run_gateup(perm, tiles, num_tiles, bm, w_gateup, T, H, I, E, k, ws, L, s);
@@ -503,7 +526,7 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
 
 int moe_forward_launches(int T, int H, int I, int E, int k) {
   if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
-  return 6;  // route + table, encode x, gather x, gate/up, down, combine
+  return 5;  // route + table, encode + permute x, gate/up, down, combine
 }
 
 int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream) {

@@ -29,20 +29,30 @@ __device__ __forceinline__ float quad_max(float v) {
 // is written as kTerms E2M1 terms x ~ sum_t q_t * 2^p_t, each term with its own
 // E8M0 exponent chosen for the residual left by the terms before.  Values past H
 // up to the next multiple of 64 are encoded as zeros so every 64-value MMA step
-// reads finite data.  The gate/up GEMM gathers these rows by perm (the permute
-// step), so each token is encoded once however many experts it is routed to.
+// reads finite data.  Each token is encoded once however many experts it is routed
+// to.  Either the rows are written in token order and the gather below permutes
+// them, or (scatter, in the layer's forward) the warp waits for routing and writes
+// its encoded values straight to the tile rows of the token's k assignments -- the
+// permute step without a launch of its own.
 __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) {
   // the previous kernel may still write x or read this call's buffers, unless the
-  // launch before this one already waited for it
-  if (!p.wait_at_end) ptx::pdl_wait();
-  ptx::pdl_launch_dependents();
+  // launch before this one already waited for it.  Waiting at the end, this launch
+  // also signals its dependents only after that wait: the GEMM after it reads the
+  // tile table before its own wait.
+  if (!p.wait_at_end) {
+    ptx::pdl_wait();
+    ptx::pdl_launch_dependents();
+  }
   const int lane = threadIdx.x & 31;
   const long long gw = ((long long)blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
   const int nvec_pad = ((p.H + 63) / 64) * 8;  // 8-value vectors per row, padded to 64 values
   const int nchunks = (nvec_pad + 31) / 32;
   const int t = (int)(gw / nchunks);
   if (t >= p.T) {
-    if (p.wait_at_end) ptx::pdl_wait();
+    if (p.wait_at_end) {
+      ptx::pdl_wait();
+      ptx::pdl_launch_dependents();
+    }
     return;
   }
   const int chunk = (int)(gw - (long long)t * nchunks);
@@ -62,6 +72,7 @@ __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) 
     for (int i = 0; i < 8; ++i) f[i] = 0.f;
   }
   const int kgroup = v >> 4;  // 16 vectors = 128 values per K group
+  uint32_t words[kTerms], sfws[kTerms];
 #pragma unroll
   for (int term = 0; term < kTerms; ++term) {
     float amax = 0.f;
@@ -84,13 +95,44 @@ __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) 
     const uint32_t sfw = __shfl_sync(0xffffffffu, e8, base) | (__shfl_sync(0xffffffffu, e8, base + 4) << 8) |
                          (__shfl_sync(0xffffffffu, e8, base + 8) << 16) |
                          (__shfl_sync(0xffffffffu, e8, base + 12) << 24);
-    if (v < nvec_pad) {
+    words[term] = word;
+    sfws[term] = sfw;
+    if (!p.scatter && v < nvec_pad) {
       const size_t row = ((size_t)kgroup * p.T + t) * kTerms + term;
       *reinterpret_cast<uint32_t*>(p.q + row * 64 + (v & 15) * 4) = word;
       if ((lane & 15) == 0) p.sf[row] = sfw;
     }
   }
-  if (p.wait_at_end) ptx::pdl_wait();
+  if (!p.wait_at_end) return;
+  ptx::pdl_wait();  // routing has completed: its tile table is visible
+  ptx::pdl_launch_dependents();
+  if (!p.scatter) return;
+  // the permute step: this token's rows go to the tile rows of its k assignments
+  // (expert e, sorted row s: tile tile_first[e] + (s - offsets[e]) / bm)
+  for (int j0 = 0; j0 < p.k; j0 += 32) {
+    int tile_j = -1, r_j = 0;
+    if (j0 + lane < p.k) {
+      const int a = t * p.k + j0 + lane;
+      const int e = __ldcg(p.topk_idx + a);
+      const int srow = __ldcg(p.inv_perm + a);
+      if (e >= 0 && e < p.E) {
+        const int q = srow - __ldcg(p.offsets + e);
+        tile_j = __ldcg(p.tile_first + e) + q / p.bm;
+        r_j = q % p.bm;
+      }
+    }
+    const int nj = min(32, p.k - j0);
+    for (int j = 0; j < nj; ++j) {
+      const int tile = __shfl_sync(0xffffffffu, tile_j, j), r = __shfl_sync(0xffffffffu, r_j, j);
+      if (tile < 0 || tile >= p.max_tiles || v >= nvec_pad) continue;
+      uint8_t* sf = p.sf_tile + ((size_t)tile * p.kg_tile + kgroup) * (kSfAtomBytes * act_sf_atoms(p.bm));
+#pragma unroll
+      for (int term = 0; term < kTerms; ++term) {
+        *reinterpret_cast<uint32_t*>(p.q_tile + act_offset(tile, term, r, v * 8, p.max_tiles, p.bm)) = words[term];
+        if ((lane & 15) == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(term, r, p.bm), 0)) = sfws[term];
+      }
+    }
+  }
 }
 
 cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream) {

@@ -40,6 +40,7 @@ struct RouteParams {
   int build_table;          // also build the tile table (last block)
   int bm;
   int32_t *counts, *offsets, *perm, *inv_perm, *num_tiles;
+  int32_t* tile_first;      // i32 [E]: index of each expert's first tile (or null)
   TileEntry* tiles;
   uint32_t* status;
 };
@@ -57,6 +58,16 @@ struct EncodeXParams {
   uint32_t* sf;            // [kg][T][kTerms]: E8M0 exponents of the 4 MX blocks of a K group
   int wait_at_end;         // dependency wait after the encoding (the launch before it already
                            // waited for earlier work), so this launch completes after that one
+  // permute after the wait (needs wait_at_end): the encoded rows go straight to the
+  // tile rows of the token's k assignments instead of q / sf
+  int scatter;
+  const int32_t* topk_idx;    // [T, k]
+  const int32_t* inv_perm;    // [T*k]: sorted row of each assignment
+  const int32_t* offsets;     // [E]: first sorted row of each expert
+  const int32_t* tile_first;  // [E]: first tile of each expert
+  int E, k, bm, max_tiles, kg_tile;
+  uint8_t* q_tile;            // GatherXParams::q layout
+  uint8_t* sf_tile;           // GatherXParams::sf layout
 };
 cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream);
 

@@ -59,7 +59,7 @@ __device__ __forceinline__ bool topk_better(float v1, int i1, float v2, int i2) 
 template <bool kSharedIdx = false>
 __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, int E, int bm, int32_t* counts,
                                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, TileEntry* tiles,
-                                       int32_t* num_tiles, uint32_t* status) {
+                                       int32_t* num_tiles, uint32_t* status, int32_t* tile_first = nullptr) {
   __shared__ int hist[kRouteWarps][kMaxExperts];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid < E) {
@@ -119,6 +119,7 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
       }
       counts[e] = c;
       offsets[e] = off;
+      if (tile_first) tile_first[e] = t0;
       int run = off;
 #pragma unroll
       for (int w = 0; w < kRouteWarps; ++w) {
@@ -354,7 +355,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     __threadfence();
   }
   build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                         p.num_tiles, p.status);
+                         p.num_tiles, p.status, p.tile_first);
 }
 
 // ------------------------------------------------------------------ decode routing
@@ -588,7 +589,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   if (!builds) return;
   if (!mbar_wait_cluster_bounded(bar_idx, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
   build_tile_table_block<true>(sidx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                               p.num_tiles, p.status);
+                               p.num_tiles, p.status, p.tile_first);
 }
 
 __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t* idx, int Tk, int E, int bm,

@@ -61,7 +61,7 @@ def test_sizes_and_policy(lib):
     atoms = E * 2 * 23 * 24 * 512
     assert n == ((codes + 255) // 256 * 256 + atoms + 255) // 256 * 256 + 256
     assert L.moe_prepared_weight_bytes(E, 2 * I + 1, H, L.MOE_WEIGHTS_GATEUP) == 0
-    assert L.moe_forward_launches(64, 2880, 2880, 32, 4) == 6
+    assert L.moe_forward_launches(64, 2880, 2880, 32, 4) == 5
 
 
 def test_host_argument_checks_return_codes(lib):

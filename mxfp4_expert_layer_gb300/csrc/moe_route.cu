@@ -172,37 +172,55 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
 template <bool kShared = false>
 __device__ int topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out) {
   const int lane = threadIdx.x & 31;
-  float v[kMaxExperts / 32];
-#pragma unroll
-  for (int i = 0; i < kMaxExperts / 32; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? (kShared ? lg_row[e] : __ldcg(lg_row + e)) : -INFINITY;
-  }
-  unsigned taken = 0;  // bit i: element e = lane + 32*i already selected
   float my_v = -INFINITY;  // lane j keeps the j-th selection
   int my_i = 0;
-  for (int j = 0; j < k; ++j) {
-    // this lane's best remaining element (larger value, then smaller index)
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+  if (E <= 32) {
+    // one logit per lane: a round is one warp max of the order-preserving key, the
+    // lowest lane holding it (= the lower expert index among equal values), and a
+    // shuffle of its value; a selected lane's key drops to 0, below every logit's
+    const float vl = lane < E ? (kShared ? lg_row[lane] : __ldcg(lg_row + lane)) : -INFINITY;
+    uint32_t key = lane < E ? sortable_key(vl) : 0u;
+    for (int j = 0; j < k; ++j) {
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      const int win = __ffs(__ballot_sync(0xffffffffu, key == kmax)) - 1;
+      const float bv = __shfl_sync(0xffffffffu, vl, win);
+      if (lane == win) key = 0u;
+      if (lane == j) {
+        my_v = bv;
+        my_i = win;
+      }
+    }
+  } else {
+    float v[kMaxExperts / 32];
 #pragma unroll
     for (int i = 0; i < kMaxExperts / 32; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && topk_better(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
-      }
+      v[i] = (e < E) ? (kShared ? lg_row[e] : __ldcg(lg_row + e)) : -INFINITY;
     }
-    // warp arg-max in two reductions: the largest value (as an order-preserving
-    // unsigned key), then the smallest index among the lanes holding it
-    const uint32_t key = sortable_key(bv);
-    const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
-    bi = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)bi : 0xffffffffu);
-    bv = __shfl_sync(0xffffffffu, bv, bi & 31);
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) {
-      my_v = bv;
-      my_i = bi;
+    unsigned taken = 0;  // bit i: element e = lane + 32*i already selected
+    for (int j = 0; j < k; ++j) {
+      // this lane's best remaining element (larger value, then smaller index)
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && topk_better(v[i], e, bv, bi)) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+      // warp arg-max in two reductions: the largest value (as an order-preserving
+      // unsigned key), then the smallest index among the lanes holding it
+      const uint32_t key = sortable_key(bv);
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+      bi = (int)__reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)bi : 0xffffffffu);
+      bv = __shfl_sync(0xffffffffu, bv, bi & 31);
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == j) {
+        my_v = bv;
+        my_i = bi;
+      }
     }
   }
   // softmax over the k selected: exponentials relative to the largest (selection 0),

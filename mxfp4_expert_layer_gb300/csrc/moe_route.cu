@@ -87,52 +87,71 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
   }
   __syncthreads();
   // phase 2 (warp 0): lane l owns experts [l*per, l*per + per); counts, then one
-  // warp scan of (rows, tiles) gives each expert's first sorted row and first tile
+  // warp scan of (rows, tiles) gives each expert's first sorted row and first tile.
+  // bm is a power of two; rows and tiles share one 32-bit scan when both fit in 16 bits.
   if (warp == 0) {
-    const int per = ceil_div(E, 32);
-    const int e0 = lane * per, e1 = min(E, e0 + per);
+    const int lgbm = __ffs(bm) - 1;
+    const int per = (E + 31) >> 5;
+    const int e0 = lane * per;
+    int cnt[kMaxExperts / 32];
     int rows = 0, ntl = 0;
-    for (int e = e0; e < e1; ++e) {
+#pragma unroll
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
       int c = 0;
+      if (i < per && e0 + i < E) {
 #pragma unroll
-      for (int w = 0; w < kRouteWarps; ++w) c += hist[w][e];
+        for (int w = 0; w < kRouteWarps; ++w) c += hist[w][e0 + i];
+      }
+      cnt[i] = c;
       rows += c;
-      ntl += ceil_div(c, bm);
+      ntl += (c + bm - 1) >> lgbm;
     }
-    int rows_incl = rows, ntl_incl = ntl;
+    int rows_incl, ntl_incl;
+    if (Tk < 65536) {
+      int packed = rows | (ntl << 16);  // tiles <= Tk / bm + E < 65536 as well
 #pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int ro = __shfl_up_sync(0xffffffffu, rows_incl, d);
-      const int to = __shfl_up_sync(0xffffffffu, ntl_incl, d);
-      if (lane >= d) {
-        rows_incl += ro;
-        ntl_incl += to;
+      for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, packed, d);
+        if (lane >= d) packed += o;
+      }
+      rows_incl = packed & 0xFFFF;
+      ntl_incl = (int)((unsigned)packed >> 16);
+    } else {
+      rows_incl = rows;
+      ntl_incl = ntl;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int ro = __shfl_up_sync(0xffffffffu, rows_incl, d);
+        const int to = __shfl_up_sync(0xffffffffu, ntl_incl, d);
+        if (lane >= d) {
+          rows_incl += ro;
+          ntl_incl += to;
+        }
       }
     }
     int off = rows_incl - rows, t0 = ntl_incl - ntl;
-    for (int e = e0; e < e1; ++e) {
-      int h[kRouteWarps], c = 0;
 #pragma unroll
-      for (int w = 0; w < kRouteWarps; ++w) {
-        h[w] = hist[w][e];
-        c += h[w];
-      }
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+      const int e = e0 + i;
+      if (i >= per || e >= E) break;
+      const int c = cnt[i];
       counts[e] = c;
       offsets[e] = off;
       if (tile_first) tile_first[e] = t0;
       int run = off;
 #pragma unroll
       for (int w = 0; w < kRouteWarps; ++w) {
+        const int h = hist[w][e];
         hist[w][e] = run;  // becomes the next free sorted row of (warp, expert)
-        run += h[w];
+        run += h;
       }
-      const int nt = ceil_div(c, bm);
+      const int nt = (c + bm - 1) >> lgbm;
       for (int q = 0; q < nt; ++q) {
         TileEntry te;
         te.expert = e;
-        te.row_begin = off + q * bm;
-        te.n_rows = min(bm, c - q * bm);
-        te.pad_row = (t0 + q) * bm;
+        te.row_begin = off + (q << lgbm);
+        te.n_rows = min(bm, c - (q << lgbm));
+        te.pad_row = (t0 + q) << lgbm;
         tiles[t0 + q] = te;
       }
       off += c;

@@ -629,6 +629,155 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
                                p.num_tiles, p.status, p.tile_first);
 }
 
+// ------------------------------------------------------------------ many tokens
+// T > 64: one block per 32 tokens computes the logits of all experts on the tensor
+// cores (mma.sync bf16, fp32 accumulate), with x and router chunks of 128 values
+// staged by cp.async into a double-buffered ring; then one warp per token selects
+// its top-k, and the last block to finish (an integer arrival count, no spinning)
+// builds the tile table.  Every block reads the router weights once (L2).
+constexpr int kMmaTokens = 32;
+constexpr int kMmaKChunk = 128;
+constexpr int kMmaPitch = kMmaKChunk * 2 + 16;  // bytes per staged row: an odd multiple of 16
+constexpr int kMmaMaxNtpw = kMaxExperts / 8 / kRouteWarps;  // 8-expert column blocks per warp
+
+struct MmaRouteSmem {
+  int erows;
+  size_t x_off[2], w_off[2], lg_off, total;
+};
+__host__ __device__ inline MmaRouteSmem mma_route_smem(int E) {
+  MmaRouteSmem L;
+  L.erows = ((E + 7) / 8) * 8;
+  const size_t xb = (size_t)kMmaTokens * kMmaPitch, wb = (size_t)L.erows * kMmaPitch;
+  L.x_off[0] = 0;
+  L.w_off[0] = xb;
+  L.x_off[1] = xb + wb;
+  L.w_off[1] = 2 * xb + wb;
+  L.lg_off = 2 * (xb + wb);
+  L.total = L.lg_off + sizeof(float) * (size_t)kMmaTokens * L.erows;
+  return L;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_mma_kernel(RouteParams p) {
+  extern __shared__ __align__(16) uint8_t rm_smem[];
+  __shared__ int s_last;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();  // the previous kernel may still write x or read this call's outputs
+  pdl_launch_dependents();
+  const MmaRouteSmem L = mma_route_smem(p.E);
+  const int t0 = blockIdx.x * kMmaTokens;
+  const int nt = min(kMmaTokens, p.T - t0);
+  const int nchunks = (p.H + kMmaKChunk - 1) / kMmaKChunk;
+  const uint32_t smem0 = smem_u32(rm_smem);
+  // chunk c of x rows t0.. and of every router row into buffer b; 16-byte segments
+  // past H or past the last token / expert are zero-filled (H is a multiple of 32)
+  auto stage = [&](int c, int b) {
+    const int k0 = c * kMmaKChunk;
+    for (int i = tid; i < kMmaTokens * (kMmaKChunk / 8); i += kRouteThreads) {
+      const int r = i / (kMmaKChunk / 8), sg = i - r * (kMmaKChunk / 8), k = k0 + sg * 8;
+      const bool ok = r < nt && k < p.H;
+      cp_async16(smem0 + (uint32_t)(L.x_off[b] + r * kMmaPitch + sg * 16), ok ? p.x + (size_t)(t0 + r) * p.H + k : p.x,
+                 ok ? 16u : 0u);
+    }
+    for (int i = tid; i < L.erows * (kMmaKChunk / 8); i += kRouteThreads) {
+      const int r = i / (kMmaKChunk / 8), sg = i - r * (kMmaKChunk / 8), k = k0 + sg * 8;
+      const bool ok = r < p.E && k < p.H;
+      cp_async16(smem0 + (uint32_t)(L.w_off[b] + r * kMmaPitch + sg * 16),
+                 ok ? p.w_router + (size_t)r * p.H + k : p.w_router, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  // warp w owns 8-expert column blocks [w ntpw, (w + 1) ntpw) and both 16-token row blocks
+  const int ntiles = L.erows / 8;
+  const int ntpw = (ntiles + kRouteWarps - 1) / kRouteWarps;
+  const int nb0 = warp * ntpw;
+  float acc[2][kMmaMaxNtpw][4];
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int q = 0; q < kMmaMaxNtpw; ++q) acc[mi][q][0] = acc[mi][q][1] = acc[mi][q][2] = acc[mi][q][3] = 0.f;
+  stage(0, 0);
+  for (int c = 0; c < nchunks; ++c) {
+    const int b = c & 1;
+    if (c + 1 < nchunks) {
+      stage(c + 1, b ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t xs = smem0 + (uint32_t)L.x_off[b], wsm = smem0 + (uint32_t)L.w_off[b];
+#pragma unroll
+    for (int ks = 0; ks < kMmaKChunk / 16; ++ks) {
+      uint32_t a0[4], a1[4];
+      ldmatrix_x4(a0, xs + (uint32_t)(((lane & 15)) * kMmaPitch + ks * 32 + (lane >> 4) * 16));
+      ldmatrix_x4(a1, xs + (uint32_t)((16 + (lane & 15)) * kMmaPitch + ks * 32 + (lane >> 4) * 16));
+#pragma unroll
+      for (int q = 0; q < kMmaMaxNtpw; ++q) {
+        const int ni = nb0 + q;
+        if (q < ntpw && ni < ntiles) {
+          uint32_t bf[2];
+          ldmatrix_x2(bf, wsm + (uint32_t)((ni * 8 + (lane & 7)) * kMmaPitch + ks * 32 + ((lane >> 3) & 1) * 16));
+          mma_bf16_16816(acc[0][q], a0, bf);
+          mma_bf16_16816(acc[1][q], a1, bf);
+        }
+      }
+    }
+    __syncthreads();  // buffer b is staged again two chunks later
+  }
+  // logits (+ bias): fragment rows mi*16 + lane/4 (+8), columns ni*8 + 2*(lane%4) (+1)
+  float* lg = reinterpret_cast<float*>(rm_smem + L.lg_off);  // [32][erows]
+#pragma unroll
+  for (int mi = 0; mi < 2; ++mi)
+#pragma unroll
+    for (int q = 0; q < kMmaMaxNtpw; ++q) {
+      const int ni = nb0 + q;
+      if (q >= ntpw || ni >= ntiles) continue;
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int r = mi * 16 + (lane >> 2) + 8 * h, e = ni * 8 + (lane & 3) * 2 + cc;
+          float v = acc[mi][q][2 * h + cc];
+          if (e < p.E) {
+            if (p.bias) v += __ldg(p.bias + e);
+            lg[r * L.erows + e] = v;
+            if (r < nt) p.logits[(size_t)(t0 + r) * p.E + e] = v;
+          }
+        }
+    }
+  __syncthreads();
+  // top-k of one token per warp
+  for (int r = warp; r < nt; r += kRouteWarps) {
+    const int t = t0 + r;
+    topk_softmax_warp<true>(lg + r * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k, p.topk_w + (size_t)t * p.k);
+  }
+  if (!p.build_table) return;
+  // the last block to finish builds the table
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned old = atomicAdd(p.sync, 1u);
+    s_last = (old == gridDim.x - 1) ? 1 : 0;
+    if (s_last) p.sync[0] = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
+                         p.num_tiles, p.status, p.tile_first);
+}
+
 __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t* idx, int Tk, int E, int bm,
                                                                    int32_t* counts, int32_t* offsets, int32_t* perm,
                                                                    int32_t* inv_perm, TileEntry* tiles,
@@ -667,6 +816,20 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
   size_t csmem = 0;
   if (use_cluster_route(p, &csmem))
     return launch_pdl(route_cluster_kernel, dim3(kClusterCtas), dim3(kRouteThreads), csmem, stream, p);
+  if (!p.from_logits) {
+    // many tokens: tensor-core logits, 32 tokens per block
+    const MmaRouteSmem L = mma_route_smem(p.E);
+    static int configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64 || configured[dev] < (int)L.total) {
+      e = cudaFuncSetAttribute(route_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
+      if (e != cudaSuccess) return e;
+      if (dev >= 0 && dev < 64) configured[dev] = (int)L.total;
+    }
+    return launch_pdl(route_mma_kernel, dim3(ceil_div(p.T, kMmaTokens)), dim3(kRouteThreads), L.total, stream, p);
+  }
   const int groups = ceil_div(p.T, kTokensPerGroup);
   dim3 grid(groups, p.from_logits ? 1 : ceil_div(p.E, p.experts_per_block));
   const size_t smem = p.from_logits ? 0 : (size_t)kTokensPerGroup * p.H * sizeof(uint16_t);

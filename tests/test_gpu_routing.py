@@ -53,6 +53,26 @@ def test_router_logits_and_selection(api, name, T):
     assert ok.mean() > 0.9
 
 
+@pytest.mark.parametrize("T,H,E,k,zipf", [(100, 256, 256, 8, None), (300, 512, 32, 4, 1.1), (65, 2880, 128, 4, None)])
+def test_router_many_tokens(api, T, H, E, k, zipf):
+    """The many-token router (blocks of 32 tokens on the tensor cores): a partial last
+    block, 256 experts (several column blocks per warp), 32 experts (idle warps), a bias."""
+    inp = make_layer(T=T, H=H, I=64, E=E, k=k, seed=T + E, zipf_s=zipf)
+    x, wr = to_dev(inp.x), to_dev(inp.w_router)
+    bias = None if inp.router_bias is None else to_dev(inp.router_bias)
+    lg, idx, w = api.route(x, wr, k, bias=bias)
+    ref = oracle.router_logits(inp.x, inp.w_router, inp.router_bias)
+    xa = np.abs(oracle.bf16_to_f32(inp.x)).astype(np.float64)
+    wa = np.abs(oracle.bf16_to_f32(inp.w_router)).astype(np.float64)
+    bound = inp.H * 2.0 ** -24 * (xa @ wa.T) + 1e-6
+    assert np.all(np.abs(lg.cpu().numpy() - ref) <= bound)
+    margin = oracle.topk_margin(ref, k)
+    ok = margin > 1e-4
+    ref_idx, _ = oracle.topk_softmax(ref, k)
+    assert np.array_equal(idx.cpu().numpy()[ok], ref_idx[ok])
+    assert ok.mean() > 0.8
+
+
 CASES = [(4, 8, 2, 16, 0.0), (1, 32, 4, 16, 0.0), (64, 32, 4, 16, 0.0), (64, 128, 4, 16, 0.0),
          (4096, 128, 4, 128, 1.1), (4096, 128, 4, 64, 0.0), (777, 16, 2, 64, 1.5), (300, 1, 1, 128, 0.0),
          (50, 256, 8, 16, 0.7), (2048, 8, 8, 128, 0.0)]

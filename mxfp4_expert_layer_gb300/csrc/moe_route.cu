@@ -774,8 +774,35 @@ __global__ void __launch_bounds__(kRouteThreads) route_mma_kernel(RouteParams p)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                         p.num_tiles, p.status, p.tile_first);
+  // every block's indices into this block's (now idle) shared memory first, with
+  // wide loads all in flight, so the table's passes over them do not wait on L2
+  const int Tk = p.T * p.k;
+  if ((size_t)Tk * sizeof(int32_t) <= L.total) {
+    int32_t* sidx = reinterpret_cast<int32_t*>(rm_smem);
+    // wide loads only from a 16-byte aligned array (a caller's output buffer may not be)
+    const int n4 = (reinterpret_cast<uintptr_t>(p.topk_idx) & 15) == 0 ? Tk / 4 : 0;
+    const int4* src4 = reinterpret_cast<const int4*>(p.topk_idx);
+    for (int i0 = tid; i0 < n4; i0 += 8 * kRouteThreads) {
+      int4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kRouteThreads;
+        v[u] = i < n4 ? __ldcg(src4 + i) : make_int4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + u * kRouteThreads;
+        if (i < n4) reinterpret_cast<int4*>(sidx)[i] = v[u];
+      }
+    }
+    for (int i = n4 * 4 + tid; i < Tk; i += kRouteThreads) sidx[i] = __ldcg(p.topk_idx + i);
+    __syncthreads();
+    build_tile_table_block<true>(sidx, Tk, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
+                                 p.num_tiles, p.status, p.tile_first);
+  } else {
+    build_tile_table_block(p.topk_idx, Tk, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
+                           p.num_tiles, p.status, p.tile_first);
+  }
 }
 
 __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t* idx, int Tk, int E, int bm,

@@ -8,6 +8,9 @@ imports the product path.
 
 from .moe_oracle import (  # noqa: F401
     E2M1_VALUES,
+    GATING_SIGMOID,
+    GATING_SOFTMAX_ALL,
+    GATING_SOFTMAX_TOPK,
     bf16_round,
     bf16_to_f32,
     decode_e8m0,
@@ -18,6 +21,7 @@ from .moe_oracle import (  # noqa: F401
     router_logits,
     tile_rows_policy,
     tile_table,
+    topk_gating,
     topk_margin,
     topk_softmax,
     max_tiles_bound,

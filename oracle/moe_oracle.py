@@ -112,6 +112,34 @@ def topk_softmax(logits: np.ndarray, k: int, dtype=np.float32):
     return idx, w.astype(dtype)
 
 
+# Gating variants ("triton-kernels" README, section "Project Structure": the router
+# does softmax or sigmoid gating + top-k; section "References": DeepSeek-V3, sigmoid
+# gating).  The selection is the same in every variant (both maps are increasing):
+GATING_SOFTMAX_TOPK = 0  # softmax over the k selected logits (the default)
+GATING_SOFTMAX_ALL = 1   # softmax over all E logits; the selected experts' probabilities
+GATING_SIGMOID = 2       # sigmoid of each selected logit, normalised to sum to 1
+
+
+def topk_gating(logits: np.ndarray, k: int, gating: int = GATING_SOFTMAX_TOPK, dtype=np.float32):
+    """Top-k experts per token by (logit descending, expert index ascending) and their
+    weights under ``gating``.  Returns (idx int32 [T, k], w [T, k])."""
+    if gating == GATING_SOFTMAX_TOPK:
+        return topk_softmax(logits, k, dtype)
+    idx, _ = topk_softmax(logits, k, dtype)
+    lg = np.asarray(logits).astype(dtype)
+    sel = np.take_along_axis(lg, idx, axis=1)
+    if gating == GATING_SOFTMAX_ALL:
+        m = lg.max(axis=1, keepdims=True)
+        ex = np.exp(lg - m)
+        w = np.take_along_axis(ex, idx, axis=1) / ex.sum(axis=1, keepdims=True)
+    elif gating == GATING_SIGMOID:
+        sg = 1.0 / (1.0 + np.exp(-sel))
+        w = sg / sg.sum(axis=1, keepdims=True)
+    else:
+        raise ValueError("gating must be 0, 1 or 2")
+    return idx, w.astype(dtype)
+
+
 def topk_margin(logits: np.ndarray, k: int) -> np.ndarray:
     """Per token: (k-th largest logit) - ((k+1)-th largest); +inf when k == E.  A
     small margin marks a near-tie whose selection depends on rounding."""
@@ -192,10 +220,11 @@ def expert_output(h_rows: np.ndarray, dn_codes_e, dn_scales_e, dtype=np.float32)
     return (np.asarray(h_rows, dtype=dtype) @ w.T).astype(dtype)
 
 
-def moe_layer(inp, dtype=np.float32, tokens=None, logits=None, return_hidden=False):
+def moe_layer(inp, dtype=np.float32, tokens=None, logits=None, return_hidden=False,
+              gating=GATING_SOFTMAX_TOPK):
     """The whole layer on the tokens ``tokens`` (default: all).
 
-    Router -> top-k + softmax -> per expert: gate/up + SwiGLU, down -> per token
+    Router -> top-k + gating weights -> per expert: gate/up + SwiGLU, down -> per token
     out[t] = sum_{j=0..k-1} w[t, j] * y[t, j] (j ascending), rounded once to bf16.
     ``logits`` may be supplied (float [T, E]) instead of being computed.
 
@@ -209,7 +238,7 @@ def moe_layer(inp, dtype=np.float32, tokens=None, logits=None, return_hidden=Fal
         lg = router_logits(inp.x[tok], inp.w_router, inp.router_bias, dtype)
     else:
         lg = np.asarray(logits, dtype=dtype)[tok]
-    idx, w = topk_softmax(lg, k, dtype)
+    idx, w = topk_gating(lg, k, gating, dtype)
     n = tok.size
     y = np.zeros((n, k, H), dtype=dtype)
     h_all = np.zeros((n, k, I), dtype=dtype) if return_hidden else None

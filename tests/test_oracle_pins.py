@@ -57,6 +57,47 @@ def test_topk_single_expert_weight_is_one():
     assert np.all(idx[:, 0] == lg.argmax(1)) and np.all(w == 1)
 
 
+def test_gating_variants_closed_forms():
+    """Each gating variant against its closed form, evaluated one value at a time with
+    the math module (not the oracle's vectorised expression), plus invariants."""
+    import math
+    rows = [[2.0, 1.0, 0.0, -1.0], [0.5, -0.25, 3.0, 3.0], [0.0, 0.0, 0.0, 0.0], [-4.0, 7.5, 1.25, -0.5]]
+    lg = np.array(rows, np.float64)
+    k = 2
+    for gating in (oracle.GATING_SOFTMAX_TOPK, oracle.GATING_SOFTMAX_ALL, oracle.GATING_SIGMOID):
+        idx, w = oracle.topk_gating(lg, k, gating, np.float64)
+        for t, row in enumerate(rows):
+            order = sorted(range(len(row)), key=lambda e: (-row[e], e))[:k]
+            assert list(idx[t]) == order
+            if gating == oracle.GATING_SOFTMAX_TOPK:
+                z = sum(math.exp(row[e] - row[order[0]]) for e in order)
+                want = [math.exp(row[e] - row[order[0]]) / z for e in order]
+            elif gating == oracle.GATING_SOFTMAX_ALL:
+                z = sum(math.exp(v - max(row)) for v in row)
+                want = [math.exp(row[e] - max(row)) / z for e in order]
+            else:
+                sg = [1.0 / (1.0 + math.exp(-row[e])) for e in order]
+                want = [v / sum(sg) for v in sg]
+            np.testing.assert_allclose(w[t], want, rtol=1e-13)
+    rng = np.random.default_rng(4)
+    lg = rng.standard_normal((7, 6))
+    # all experts selected: softmax over all = softmax over the selected
+    i0, w0 = oracle.topk_gating(lg, 6, oracle.GATING_SOFTMAX_TOPK, np.float64)
+    i1, w1 = oracle.topk_gating(lg, 6, oracle.GATING_SOFTMAX_ALL, np.float64)
+    assert np.array_equal(i0, i1)
+    np.testing.assert_allclose(w0, w1, rtol=1e-12)
+    # the same selection in every variant; sigmoid weights sum to 1, softmax-over-all
+    # weights of a strict subset to less than 1
+    i2, w2 = oracle.topk_gating(lg, 3, oracle.GATING_SIGMOID, np.float64)
+    i3, w3 = oracle.topk_gating(lg, 3, oracle.GATING_SOFTMAX_ALL, np.float64)
+    assert np.array_equal(i2, oracle.topk_softmax(lg, 3, np.float64)[0]) and np.array_equal(i2, i3)
+    np.testing.assert_allclose(w2.sum(1), 1.0, rtol=1e-12)
+    assert np.all(w3.sum(1) < 1.0)
+    # equal logits: sigmoid gating gives every selected expert 1/k
+    _, w4 = oracle.topk_gating(np.zeros((2, 5)), 4, oracle.GATING_SIGMOID, np.float64)
+    np.testing.assert_allclose(w4, 0.25, rtol=1e-15)
+
+
 def test_tile_table_brute_force_and_invariants():
     cases = []
     for (T, E, k, bm, skew, seed) in [(4, 8, 2, 16, 0, 0), (1, 32, 4, 16, 0, 1),

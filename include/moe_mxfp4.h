@@ -54,6 +54,13 @@ typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t */
 #define MOE_WEIGHTS_DOWN 1
 
 #define MOE_ROUTE_FROM_LOGITS 1 /* moe_route: `logits` is an input, skip the GEMV */
+/* Gating variants (moe_route flags, moe_forward_gated): the k experts are selected the
+ * same way in every one (the k largest logits, ties to the lower index); only their
+ * weights differ.  Default (neither flag): softmax over the k selected logits.
+ * "triton-kernels" README, "Project Structure" (router: softmax / sigmoid gating +
+ * top-k) and "References" (DeepSeek-V3: sigmoid gating).                          */
+#define MOE_ROUTE_GATING_SOFTMAX_ALL 2 /* w_j = exp(l_j) / sum over all E of exp(l_e)   */
+#define MOE_ROUTE_GATING_SIGMOID 4     /* w_j = sigmoid(l_j) / sum over the k selected  */
 
 /* Static description of a status code; never NULL. */
 const char* moe_error_string(int status);
@@ -95,7 +102,8 @@ size_t moe_workspace_bytes(int T, int H, int I, int E, int k);
 /* ------------------------------------------------------------------ stage calls
  * moe_route: logits[t, e] = sum_h x[t, h] * w_router[e, h] (+ router_bias[e]) in
  * fp32; then per token the k largest logits (ties: lower expert index first),
- * listed in that order, and weights = softmax over those k logits.
+ * listed in that order, and weights = softmax over those k logits (or the gating
+ * variant a MOE_ROUTE_GATING_* flag names; both flags at once is invalid).
  *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL.
  *   logits f32 [T, E]: written, or read when flags has MOE_ROUTE_FROM_LOGITS (then
  *   x, w_router and router_bias may be NULL).
@@ -178,7 +186,15 @@ int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t*
                        moe_stream_t stream);
 
 /* ------------------------------------------------------------------ whole layer
- * moe_forward: the whole layer, out = MoE(x), on one stream with no host sync.
+ * moe_forward_gated: moe_forward with the top-k weights of the gating variant
+ * `gating` (0, MOE_ROUTE_GATING_SOFTMAX_ALL or MOE_ROUTE_GATING_SIGMOID; any other
+ * value is MOE_ERR_INVALID_ARG).                                                   */
+int moe_forward_gated(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
+                      const void* w_down, int T, int H, int I, int E, int k, int gating, void* workspace,
+                      size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                      moe_stream_t stream);
+
+/* moe_forward: the whole layer, out = MoE(x), on one stream with no host sync.
  *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL;
  *   w_gateup / w_down: prepared weights; out bf16 [T, H];
  *   topk_idx_out i32 [T, k] and topk_w_out f32 [T, k]: optional copies (NULL to skip).

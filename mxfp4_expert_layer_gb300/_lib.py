@@ -22,6 +22,8 @@ MOE_ERR_NAN_SCALE = -6
 MOE_WEIGHTS_GATEUP = 0
 MOE_WEIGHTS_DOWN = 1
 MOE_ROUTE_FROM_LOGITS = 1
+MOE_ROUTE_GATING_SOFTMAX_ALL = 2
+MOE_ROUTE_GATING_SIGMOID = 4
 
 # every symbol the header declares, with its C signature
 _P = ctypes.c_void_p
@@ -41,6 +43,7 @@ SIGNATURES = {
     "moe_mxfp4_down_combine": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P]),
     "moe_hidden_dequant": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P, _P]),
     "moe_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P]),
+    "moe_forward_gated": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P]),
     "moe_forward_timed": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P, _P]),
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I]),
     "moe_get_device_status": (_I, [_P, _S, ctypes.POINTER(_I), _P]),
@@ -98,6 +101,7 @@ moe_mxfp4_gateup_swiglu = _call("moe_mxfp4_gateup_swiglu")
 moe_mxfp4_down_combine = _call("moe_mxfp4_down_combine")
 moe_hidden_dequant = _call("moe_hidden_dequant")
 moe_forward = _call("moe_forward")
+moe_forward_gated = _call("moe_forward_gated")
 moe_forward_timed = _call("moe_forward_timed")
 moe_forward_launches = _call("moe_forward_launches")
 moe_get_device_status = _call("moe_get_device_status")

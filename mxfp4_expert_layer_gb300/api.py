@@ -58,8 +58,10 @@ def max_tiles(T: int, k: int, E: int, bm: int) -> int:
     return L.moe_max_tiles(T, k, E, bm)
 
 
-def route(x, w_router, k, bias=None, logits=None, from_logits=False, ws=None):
-    """Router logits (or given ones) -> (logits, topk_idx int32, topk_w float32)."""
+def route(x, w_router, k, bias=None, logits=None, from_logits=False, ws=None, gating=0):
+    """Router logits (or given ones) -> (logits, topk_idx int32, topk_w float32).
+    ``gating``: 0 (softmax over the k selected), MOE_ROUTE_GATING_SOFTMAX_ALL or
+    MOE_ROUTE_GATING_SIGMOID."""
     if from_logits:
         T, E = logits.shape
         H = 32
@@ -74,7 +76,7 @@ def route(x, w_router, k, bias=None, logits=None, from_logits=False, ws=None):
     w = torch.empty(T, k, dtype=torch.float32, device=dev)
     if ws is None:
         ws = workspace(T, 32, 32, E, k, dev)
-    flags = L.MOE_ROUTE_FROM_LOGITS if from_logits else 0
+    flags = (L.MOE_ROUTE_FROM_LOGITS if from_logits else 0) | gating
     L.check("moe_route", L.moe_route(_ptr(x), _ptr(w_router), _ptr(bias), T, H, E, k, logits.data_ptr(), flags,
                                      idx.data_ptr(), w.data_ptr(), ws.data_ptr(), ws.numel(), _stream()))
     return logits, idx, w
@@ -129,13 +131,19 @@ class MoELayer:
         return ws
 
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, topk_idx=None, topk_w=None,
-                ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+                ws: Optional[torch.Tensor] = None, gating: int = 0) -> torch.Tensor:
         _need_cuda(x)
         T = x.shape[0]
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
         if ws is None:
             ws = self.workspace(T)
+        if gating:
+            L.check("moe_forward_gated", L.moe_forward_gated(
+                x.data_ptr(), self.w_router.data_ptr(), _ptr(self.router_bias), self.w_gateup.data_ptr(),
+                self.w_down.data_ptr(), T, self.H, self.I, self.E, self.k, gating, ws.data_ptr(), ws.numel(),
+                out.data_ptr(), _ptr(topk_idx), _ptr(topk_w), _stream()))
+            return out
         L.check("moe_forward", L.moe_forward(
             x.data_ptr(), self.w_router.data_ptr(), _ptr(self.router_bias), self.w_gateup.data_ptr(),
             self.w_down.data_ptr(), T, self.H, self.I, self.E, self.k, ws.data_ptr(), ws.numel(), out.data_ptr(),

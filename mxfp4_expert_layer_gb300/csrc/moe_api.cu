@@ -281,6 +281,10 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   return cuda_status(launch_combine(c, stream));
 }
 
+static_assert(MOE_ROUTE_FROM_LOGITS == kRouteFlagFromLogits && MOE_ROUTE_GATING_SOFTMAX_ALL == kRouteFlagSoftmaxAll &&
+                  MOE_ROUTE_GATING_SIGMOID == kRouteFlagSigmoid,
+              "route flag values");
+
 RouteParams route_params(const uint16_t* x, const uint16_t* w_router, const float* bias, int T, int H, int E, int k,
                          float* logits, int from_logits, int32_t* idx, float* w, void* ws, const WsLayout& L) {
   RouteParams r{};
@@ -366,7 +370,8 @@ size_t moe_workspace_bytes(int T, int H, int I, int E, int k) {
 int moe_route(const uint16_t* x, const uint16_t* w_router, const float* router_bias, int T, int H, int E, int k,
               float* logits, int flags, int32_t* topk_idx, float* topk_w, void* workspace, size_t workspace_bytes,
               moe_stream_t stream) {
-  if (flags & ~MOE_ROUTE_FROM_LOGITS) return MOE_ERR_INVALID_ARG;
+  const int gating = gating_from_flags(flags);
+  if (gating < 0) return MOE_ERR_INVALID_ARG;
   const int from_logits = (flags & MOE_ROUTE_FROM_LOGITS) ? 1 : 0;
   const int Hs = from_logits ? 32 : H;
   int st = check_shape(T, Hs, 32, E, k);
@@ -379,6 +384,7 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* router_b
   RouteParams r = route_params(x, w_router, router_bias, T, Hs, E, k, logits, from_logits, topk_idx, topk_w,
                                workspace, L);
   r.build_table = 0;
+  r.gating = gating;
   return cuda_status(launch_route(r, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -458,7 +464,7 @@ int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t*
 static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float* router_bias,
                         const void* w_gateup, const void* w_down, int T, int H, int I, int E, int k,
                         void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out,
-                        float* topk_w_out, void* const* events, moe_stream_t stream) {
+                        float* topk_w_out, void* const* events, moe_stream_t stream, int gating = kGatingSoftmaxTopk) {
   int st = check_shape(T, H, I, E, k);
   if (st != MOE_OK) return st;
   if (!x || !w_router || !w_gateup || !w_down || !workspace || !out) return MOE_ERR_INVALID_ARG;
@@ -478,6 +484,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
 
   RouteParams r = route_params(x, w_router, router_bias, T, H, E, k, ws_ptr<float>(ws, L.logits), 0, idx, w, ws, L);
   r.build_table = 1;
+  r.gating = gating;
   r.bm = bm;
   r.counts = ws_ptr<int32_t>(ws, L.counts);
   r.offsets = ws_ptr<int32_t>(ws, L.offsets);
@@ -513,6 +520,16 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* router
                 uint16_t* out, int32_t* topk_idx_out, float* topk_w_out, moe_stream_t stream) {
   return forward_impl(x, w_router, router_bias, w_gateup, w_down, T, H, I, E, k, workspace, workspace_bytes, out,
                       topk_idx_out, topk_w_out, nullptr, stream);
+}
+
+int moe_forward_gated(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
+                      const void* w_down, int T, int H, int I, int E, int k, int gating, void* workspace,
+                      size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                      moe_stream_t stream) {
+  const int g = gating == 0 ? kGatingSoftmaxTopk : gating_from_flags(gating);
+  if (g < 0 || (gating & MOE_ROUTE_FROM_LOGITS)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x, w_router, router_bias, w_gateup, w_down, T, H, I, E, k, workspace, workspace_bytes, out,
+                      topk_idx_out, topk_w_out, nullptr, stream, g);
 }
 
 int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,

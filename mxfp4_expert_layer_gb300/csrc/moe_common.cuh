@@ -18,6 +18,12 @@ constexpr int kKGroup = 128;         // K values per pipeline stage (4 MX blocks
 constexpr int kMTile = 128;          // weight rows per MMA tile (MMA M)
 constexpr int kSfAtomBytes = 512;    // scale-factor atom: 128 rows x 4 MX blocks
 constexpr int kMaxExperts = 256;
+// Gating variants of the top-k weights (the selection is the same in every one):
+// softmax over the k selected logits, softmax over all E logits (the selected
+// probabilities), or the selected logits' sigmoids normalised to sum to one.
+constexpr int kGatingSoftmaxTopk = 0;
+constexpr int kGatingSoftmaxAll = 1;
+constexpr int kGatingSigmoid = 2;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxCtas = 160;        // persistent GEMM CTAs (one per SM; GB300 has 152)
 constexpr int kTerms = 4;            // E2M1 terms of the activation encoding

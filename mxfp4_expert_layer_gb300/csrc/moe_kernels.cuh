@@ -26,12 +26,22 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
+// Route flags (the public MOE_ROUTE_* values) -> gating variant, or -1 for a bad set.
+constexpr int kRouteFlagFromLogits = 1, kRouteFlagSoftmaxAll = 2, kRouteFlagSigmoid = 4;
+inline int gating_from_flags(int flags) {
+  if (flags & ~(kRouteFlagFromLogits | kRouteFlagSoftmaxAll | kRouteFlagSigmoid)) return -1;
+  const bool all = (flags & kRouteFlagSoftmaxAll) != 0, sig = (flags & kRouteFlagSigmoid) != 0;
+  if (all && sig) return -1;
+  return all ? kGatingSoftmaxAll : sig ? kGatingSigmoid : kGatingSoftmaxTopk;
+}
+
 struct RouteParams {
   const uint16_t* x;        // bf16 [T, H]
   const uint16_t* w_router; // bf16 [E, H]
   const float* bias;        // f32 [E] or null
   int T, H, E, k;
   int from_logits;          // logits are an input
+  int gating;               // kGatingSoftmaxTopk / kGatingSoftmaxAll / kGatingSigmoid
   int experts_per_block;    // experts per block slice (multiple of 8)
   float* logits;            // f32 [T, E]
   int32_t* topk_idx;        // i32 [T, k]

@@ -54,7 +54,8 @@ extern "C" int moe_route_noalloc(const uint16_t* x, const uint16_t* w_router, co
                                  int H, int E, int k, float* logits, int flags, int32_t* topk_idx, float* topk_w,
                                  moe_stream_t stream) {
   using namespace moe;
-  if (flags & ~MOE_ROUTE_FROM_LOGITS) return MOE_ERR_INVALID_ARG;
+  const int gating = gating_from_flags(flags);
+  if (gating < 0) return MOE_ERR_INVALID_ARG;
   const int from_logits = (flags & MOE_ROUTE_FROM_LOGITS) ? 1 : 0;
   const int Hs = from_logits ? 32 : H;
   if (T < 1 || T > kNoAllocMaxTokens) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -77,6 +78,7 @@ extern "C" int moe_route_noalloc(const uint16_t* x, const uint16_t* w_router, co
   r.bias = router_bias;
   r.T = T; r.H = Hs; r.E = E; r.k = k;
   r.from_logits = from_logits;
+  r.gating = gating;
   r.experts_per_block = T <= 64 ? 8 : 32;
   r.logits = logits;
   r.topk_idx = topk_idx;

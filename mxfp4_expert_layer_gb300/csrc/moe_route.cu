@@ -185,14 +185,19 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
 }
 
 // Top-k of one token by one warp: each lane holds logits e = lane + 32*i; k rounds
-// of a warp arg-max on (value desc, index asc).  Softmax over the k selected.
+// of a warp arg-max on (value desc, index asc).  Weights by `gating` (MoeGating):
+// softmax over the k selected (exponentials relative to the largest, summed in
+// selection order), softmax over all E (the selected exponentials over the sum of all,
+// reduced by a fixed butterfly), or the selected sigmoids normalised to sum to one.
 // kShared: the logits row is in shared memory (else global, read through L2).
 // Returns the j-th selected expert in lane j < k.
 template <bool kShared = false>
-__device__ int topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out) {
+__device__ int topk_softmax_warp(const float* __restrict__ lg_row, int E, int k, int32_t* idx_out, float* w_out,
+                                 int gating = kGatingSoftmaxTopk) {
   const int lane = threadIdx.x & 31;
   float my_v = -INFINITY;  // lane j keeps the j-th selection
   int my_i = 0;
+  float all_part = 0.f;    // softmax over all: this lane's share of sum_e exp(l_e - max)
   if (E <= 32) {
     // one logit per lane: a round is one warp max of the order-preserving key, the
     // lowest lane holding it (= the lower expert index among equal values), and a
@@ -208,6 +213,10 @@ __device__ int topk_softmax_warp(const float* __restrict__ lg_row, int E, int k,
         my_v = bv;
         my_i = win;
       }
+    }
+    if (gating == kGatingSoftmaxAll) {
+      const float mx = __shfl_sync(0xffffffffu, my_v, 0);  // every lane takes part
+      if (lane < E) all_part = expf(vl - mx);
     }
   } else {
     float v[kMaxExperts / 32];
@@ -241,16 +250,31 @@ __device__ int topk_softmax_warp(const float* __restrict__ lg_row, int E, int k,
         my_i = bi;
       }
     }
+    if (gating == kGatingSoftmaxAll) {
+      const float mx = __shfl_sync(0xffffffffu, my_v, 0);
+#pragma unroll
+      for (int i = 0; i < kMaxExperts / 32; ++i)
+        if (lane + 32 * i < E) all_part += expf(v[i] - mx);
+    }
   }
-  // softmax over the k selected: exponentials relative to the largest (selection 0),
-  // summed in selection order by lane 0, one division per selection
   const float m = __shfl_sync(0xffffffffu, my_v, 0);
-  const float ex = lane < k ? expf(my_v - m) : 0.f;
-  float s = 0.f;
-  for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, ex, j);
+  float num, den = 0.f;
+  if (gating == kGatingSigmoid) {
+    num = lane < k ? 1.f / (1.f + expf(-my_v)) : 0.f;
+    for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, num, j);
+  } else {
+    num = lane < k ? expf(my_v - m) : 0.f;
+    if (gating == kGatingSoftmaxAll) {
+      den = all_part;
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) den += __shfl_xor_sync(0xffffffffu, den, d);
+    } else {
+      for (int j = 0; j < k; ++j) den += __shfl_sync(0xffffffffu, num, j);
+    }
+  }
   if (lane < k) {
     idx_out[lane] = my_i;
-    w_out[lane] = ex / s;
+    w_out[lane] = num / den;
   }
   return my_i;
 }
@@ -375,7 +399,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   if (warp < nt) {
     const int t = t0 + warp;
     topk_softmax_warp(p.logits + (size_t)t * p.E, p.E, p.k, p.topk_idx + (size_t)t * p.k,
-                      p.topk_w + (size_t)t * p.k);
+                      p.topk_w + (size_t)t * p.k, p.gating);
   }
   if (!p.build_table) return;
   __threadfence();
@@ -618,7 +642,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     if (warp < n_own) {
       const int t = t_own + warp;
       const int sel = topk_softmax_warp<true>(lg + warp * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k,
-                                              p.topk_w + (size_t)t * p.k);
+                                              p.topk_w + (size_t)t * p.k, p.gating);
       if (p.build_table && lane < p.k)
         st_async_b32(mapa_shared(smem_u32(sidx + t * p.k + lane), 0), (uint32_t)sel, mapa_shared(smem_u32(bar_idx), 0));
     }
@@ -760,7 +784,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_mma_kernel(RouteParams p)
   // top-k of one token per warp
   for (int r = warp; r < nt; r += kRouteWarps) {
     const int t = t0 + r;
-    topk_softmax_warp<true>(lg + r * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k, p.topk_w + (size_t)t * p.k);
+    topk_softmax_warp<true>(lg + r * L.erows, p.E, p.k, p.topk_idx + (size_t)t * p.k, p.topk_w + (size_t)t * p.k,
+                            p.gating);
   }
   if (!p.build_table) return;
   // the last block to finish builds the table

@@ -84,6 +84,11 @@ def test_host_argument_checks_return_codes(lib):
     assert fwd(T=0) == L.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_route(fake, fake, None, T, H, E, k, fake, 7, fake, fake, fake, ws, None) == L.MOE_ERR_INVALID_ARG
     assert L.moe_route(None, None, None, T, H, E, k, None, 0, fake, fake, fake, ws, None) == L.MOE_ERR_INVALID_ARG
+    # both gating variants at once, or an unknown flag bit
+    assert L.moe_route(fake, fake, None, T, H, E, k, fake, 6, fake, fake, fake, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_route(fake, fake, None, T, H, E, k, fake, 8, fake, fake, fake, ws, None) == L.MOE_ERR_INVALID_ARG
+    assert L.moe_forward_gated(fake, fake, None, fake, fake, T, H, I, E, k, 3, fake, ws, fake, None, None,
+                               None) == L.MOE_ERR_INVALID_ARG
     assert L.moe_build_tile_table(fake, T, k, E, 32, fake, fake, fake, fake, fake, fake, None) == \
         L.MOE_ERR_UNSUPPORTED_SHAPE                            # tile rows must be 16, 64 or 128
     assert L.moe_prepare_weights(fake, fake, E, 2 * I, H, 5, fake, 1 << 40, None) == L.MOE_ERR_UNSUPPORTED_SHAPE

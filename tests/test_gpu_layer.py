@@ -76,21 +76,24 @@ def test_prepare_rejects_nan_scale():
     assert ei.value.status == L.MOE_ERR_NAN_SCALE
 
 
-def run_layer(inp, tokens=None):
+def run_layer(inp, tokens=None, gating=0):
     import torch
     layer = build_layer(inp)
     x = to_dev(inp.x)
     idx = torch.empty(inp.T, inp.k, dtype=torch.int32, device="cuda")
     w = torch.empty(inp.T, inp.k, dtype=torch.float32, device="cuda")
-    out = layer(x, topk_idx=idx, topk_w=w)
+    out = layer(x, topk_idx=idx, topk_w=w, gating=gating)
     torch.cuda.synchronize()
     assert layer.device_status(inp.T) == 0
     return layer, bf16_bits_to_f32(bf16_to_np(out)), idx.cpu().numpy(), w.cpu().numpy()
 
 
-def check_layer(inp, tokens=None, margin=1e-4):
-    layer, out, idx, w = run_layer(inp)
-    ref = oracle.moe_layer(inp, tokens=tokens)
+GATING_OF_FLAG = {0: 0, 2: 1, 4: 2}  # MOE_ROUTE_GATING_* flag -> oracle gating variant
+
+
+def check_layer(inp, tokens=None, margin=1e-4, gating=0):
+    layer, out, idx, w = run_layer(inp, gating=gating)
+    ref = oracle.moe_layer(inp, tokens=tokens, gating=GATING_OF_FLAG[gating])
     tok = ref["tokens"]
     # compare tokens whose routing is not a near tie under fp32 logit rounding
     keep = oracle.topk_margin(ref["logits"], inp.k) > margin
@@ -103,6 +106,12 @@ def check_layer(inp, tokens=None, margin=1e-4):
 
 def test_layer_tiny():
     check_layer(make_config("tiny"))
+
+
+@pytest.mark.parametrize("name,gating", [("tiny", 2), ("tiny", 4), ("gptoss20b_b1", 4), ("gptoss20b_b64", 2)])
+def test_layer_gating_variants(name, gating):
+    """moe_forward_gated: softmax over all experts (flag 2) and normalised sigmoid (4)."""
+    check_layer(make_config(name), gating=gating)
 
 
 def test_layer_gptoss20b_b1():

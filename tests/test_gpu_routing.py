@@ -30,6 +30,33 @@ def test_topk_softmax_from_identical_logits(api, T, E, k, seed):
     np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("T,E,k,seed", [(5, 8, 2, 0), (3, 32, 4, 1), (70, 128, 4, 2), (37, 256, 8, 3)])
+@pytest.mark.parametrize("flag,gating", [(2, 1), (4, 2)])
+def test_gating_variants_from_identical_logits(api, T, E, k, seed, flag, gating):
+    """Softmax over all experts (flag 2) and normalised sigmoid (flag 4): the same
+    selection as the default, weights by the oracle's variant."""
+    lg = random_logits(T, E, seed=seed, n_ties=T // 3)
+    _, idx, w = api.route(None, None, k, logits=to_dev(lg), from_logits=True, gating=flag)
+    ref_idx, ref_w = oracle.topk_gating(lg, k, gating)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("name,T,flag,gating", [("gptoss20b_b64", None, 4, 2), ("gptoss120b_b64", None, 2, 1),
+                                                ("gptoss120b_prefill4096", 300, 4, 2)])
+def test_router_gating_variants(api, name, T, flag, gating):
+    """The variants through the decode cluster router and the many-token router."""
+    inp = make_config(name, T=T)
+    x, wr = to_dev(inp.x), to_dev(inp.w_router)
+    bias = None if inp.router_bias is None else to_dev(inp.router_bias)
+    lg, idx, w = api.route(x, wr, inp.k, bias=bias, gating=flag)
+    # weights from the GPU's own logits: the selection is bit-exact and the weights
+    # follow the variant's formula
+    ref_idx, ref_w = oracle.topk_gating(lg.cpu().numpy(), inp.k, gating)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+
+
 @pytest.mark.parametrize("name,T", [("tiny", None), ("gptoss20b_b1", None), ("gptoss20b_b64", None),
                                     ("gptoss120b_b64", None), ("gptoss120b_prefill4096", None)])
 def test_router_logits_and_selection(api, name, T):

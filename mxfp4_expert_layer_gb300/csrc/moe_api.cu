@@ -124,26 +124,6 @@ bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P,
                   kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// Encoded activations {kstage/2 bytes, max_tiles * kTerms * bm rows, stages}: one
-// tile's kTerms * bm rows of a stage are contiguous (boxes of at most 256 rows).
-// Token-major tiles (at most 16 rows) get kActBoxes maps whose boxes hold the rows of
-// 1, 2, 4, 8 or 16 tokens, so a stage loads only its tile's real tokens.
-bool act_map(CUtensorMap (&out)[kActBoxes], const void* base, int K, int max_tiles, int bm) {
-  const cuuint64_t rows = (cuuint64_t)max_tiles * kTerms * bm;
-  const int kb = gemm_kstage(bm) / 2;
-  cuuint64_t dims[3] = {(cuuint64_t)kb, rows, (cuuint64_t)ceil_div(K, gemm_kstage(bm))};
-  cuuint64_t strides[2] = {(cuuint64_t)kb, (cuuint64_t)kb * rows};
-  for (int q = 0; q < kActBoxes; ++q) {
-    int box_rows = kTerms * bm < 256 ? kTerms * bm : 256;
-    if (act_token_major(bm)) box_rows = min(kTerms << q, kTerms * bm);
-    cuuint32_t box[3] = {(cuuint32_t)kb, (cuuint32_t)box_rows, 1};
-    if (!make_map(&out[q], base, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box,
-                  kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
-      return false;
-  }
-  return true;
-}
-
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Records a caller event; while the stream is being captured the record is made an
@@ -222,7 +202,7 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   const PreparedLayout P = make_prepared_layout(E, 2 * I, H, 2);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_gateup, P, bm)) return MOE_ERR_CUDA;
-  if (!act_map(g.tm_act, ws_ptr<uint8_t>(ws, L.x_q), H, L.max_tiles, bm)) return MOE_ERR_CUDA;
+  g.act_q = ws_ptr<uint8_t>(ws, L.x_q);
   g.w_sf = static_cast<const uint8_t*>(w_gateup) + P.scales_off;
   g.act_sf = ws_ptr<uint8_t>(ws, L.x_sf);
   g.tiles = tiles;
@@ -251,7 +231,7 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   const PreparedLayout P = make_prepared_layout(E, H, I, 1);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_down, P, bm)) return MOE_ERR_CUDA;
-  if (!act_map(g.tm_act, ws_ptr<uint8_t>(ws, L.h_q), I, L.max_tiles, bm)) return MOE_ERR_CUDA;
+  g.act_q = ws_ptr<uint8_t>(ws, L.h_q);
   g.w_sf = static_cast<const uint8_t*>(w_down) + P.scales_off;
   g.act_sf = ws_ptr<uint8_t>(ws, L.h_sf);
   g.tiles = tiles;

@@ -168,9 +168,10 @@ __global__ void __launch_bounds__(kAuxThreads) gather_x_kernel(GatherXParams p) 
   uint8_t* sf = p.sf + ((size_t)tile * p.kg + kg) * (kSfAtomBytes * act_sf_atoms(p.bm));
 #pragma unroll
   for (int t = 0; t < kTerms; ++t) {
-    uint4* dst = reinterpret_cast<uint4*>(p.q + act_offset(tile, t, r, kg * kKGroup, p.max_tiles, p.bm));
+    // 16-byte chunks (32 values each) land at their swizzled positions
 #pragma unroll
-    for (int j = 0; j < 4; ++j) dst[j] = v[t * 4 + j];
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(p.q + act_offset(tile, t, r, kg * kKGroup + 32 * j, p.max_tiles, p.bm)) = v[t * 4 + j];
     *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(t, r, p.bm), 0)) = ew[t];
   }
 }

@@ -27,7 +27,6 @@ constexpr int kGatingSigmoid = 2;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxCtas = 160;        // persistent GEMM CTAs (one per SM; GB300 has 152)
 constexpr int kTerms = 4;            // E2M1 terms of the activation encoding
-constexpr int kActBoxes = 5;         // B box heights 4 x {1, 2, 4, 8, 16} rows for 16-row tiles
 
 // Device status word bits (read back with moe_get_device_status).
 constexpr uint32_t kStatusTimeoutMain = 1u << 0;
@@ -237,19 +236,24 @@ __device__ __forceinline__ float e2m1_to_f32(uint32_t code) {
 // the tile's real tokens come first and one TMA box of 4 x (tokens rounded up to a
 // power of two) rows covers them; larger tiles are term major (one MMA per term).
 __host__ __device__ constexpr bool act_token_major(int bm) { return kTerms * bm <= 64; }
-// K values per pipeline stage of the expert GEMMs: 256 (128-byte rows, 128-byte
-// swizzle) for 16-row decode tiles, whose weights stream at the HBM rate; 128
-// (64-byte rows) for larger tiles, whose bigger B tiles would leave too few stages.
-__host__ __device__ constexpr int gemm_kstage(int bm) { return act_token_major(bm) ? 256 : 128; }
+// K values per pipeline stage of the expert GEMMs: 256 for every tile size (128-byte
+// operand rows, 128-byte swizzle).
+__host__ __device__ constexpr int gemm_kstage(int) { return 256; }
 __host__ __device__ inline int act_row(int t, int r, int bm) {
   return act_token_major(bm) ? r * kTerms + t : t * bm + r;
 }
 // Byte offset of the code byte holding values (k, k+1) (k even) of term t of row r
 // of tile `tile` in an encoded activation buffer
-// [K / kstage][max_tiles][kTerms * bm rows][kstage / 2 bytes], kstage = gemm_kstage(bm).
+// [K / 256][max_tiles][kTerms * bm rows][128 bytes].  One tile's rows of one stage
+// form a contiguous image that is exactly the 128-byte-swizzled shared-memory tile
+// the MMA reads (16-byte chunk c of image row i stored at chunk c ^ (i % 8)), so
+// the GEMMs load it with a plain bulk copy; writers of more than one byte at a time
+// stay within one 16-byte chunk.
 __host__ __device__ inline size_t act_offset(int tile, int t, int r, int k, int max_tiles, int bm) {
-  const int ks = gemm_kstage(bm);
-  return (((size_t)(k / ks) * max_tiles + tile) * (kTerms * bm) + act_row(t, r, bm)) * (ks / 2) + ((k % ks) >> 1);
+  const int row = act_row(t, r, bm);
+  const int byte = (k % 256) >> 1;
+  return (((size_t)(k / 256) * max_tiles + tile) * (kTerms * bm) + row) * 128 +
+         ((((byte >> 4) ^ (row & 7)) << 4) | (byte & 15));
 }
 
 // Scale atom byte offset of (row r within a tile, MX block b within a K group).

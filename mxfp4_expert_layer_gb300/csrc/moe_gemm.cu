@@ -57,7 +57,6 @@ struct GemmCfg {
   static constexpr int kVals = kA * BM;                      // values per row after summing terms
   static constexpr int kBRows = kTerms * BM;                 // B tile rows (terms x token rows)
   static constexpr int kBBytes = kBRows * kKBytes;
-  static constexpr int kBBoxRows = kBRows < 256 ? kBRows : 256;
   static constexpr int kNbAtoms = (kBRows + 127) / 128;      // B scale atoms per stage
   static constexpr int kSfBytes = (kA + kNbAtoms) * kAtoms * kSfAtomBytes;
   static constexpr int kStageRaw = kA * kATileBytes + kBBytes + kSfBytes;
@@ -68,7 +67,6 @@ struct GemmCfg {
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kBarBytes = 2048;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
-  static constexpr uint32_t kTxBytes = kA * kATileBytes + kBBytes + kSfBytes;  // full B box
   static constexpr uint32_t kTxNoB = kA * kATileBytes + kSfBytes;                // all but the B codes
   // MMA issuers: with two weight tiles per stage each of two threads issues one
   // tile's MMAs (its own accumulator, scale copies and B scale columns)
@@ -83,7 +81,6 @@ struct GemmCfg {
   static constexpr bool kLoadAll = kAccCols <= 128;
   static_assert(kTmemNeed <= 512, "tensor memory budget");
   static_assert(kStages >= 2, "pipeline depth");
-  static_assert(kBRows % kBBoxRows == 0, "B tile = whole TMA boxes");
 };
 
 // Raster: units are grouped in blocks of `group` tiles; within a block the M tile
@@ -162,7 +159,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&p.tm_w);
-    for (int q = 0; q < (C::kConcat ? kActBoxes : 1); ++q) tma_prefetch_desc(&p.tm_act[q]);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -203,7 +199,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       // iterator over this CTA's (segment, K group) iterations
-      int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0, boxq = 0;
+      int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0, b_rows = C::kBRows;
       auto open_seg = [&]() {
         int u, kk0;
         bool whole;
@@ -212,17 +208,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
         const TileEntry te = load_tile(p.tiles + tile);
         expert = te.expert;
-        // token-major tiles: the smallest box (4 x 2^q rows) holding the real tokens
-        boxq = 0;
-        while ((1 << boxq) < te.n_rows && boxq < kActBoxes - 1) ++boxq;
+        // token-major tiles: only the real tokens' rows (kTerms per token) are loaded
+        b_rows = C::kConcat ? kTerms * max(1, min(te.n_rows, BM)) : C::kBRows;
       };
       auto advance = [&]() {
         if (++kk == kk1 && ++si < sch.nseg) open_seg();
       };
       // bytes the stage's barrier expects for the current tile
-      auto tx_bytes = [&]() -> uint32_t {
-        return C::kConcat ? C::kTxNoB + (uint32_t)(kTerms << boxq) * (uint32_t)C::kKBytes : C::kTxBytes;
-      };
+      auto tx_bytes = [&]() -> uint32_t { return C::kTxNoB + (uint32_t)b_rows * (uint32_t)C::kKBytes; };
       // Weights are read once per call.  When more units than CTAs stream them, mark
       // them evict-first so that the activation tiles every unit of a tile re-reads
       // stay in L2; a single wave keeps the normal policy (faster there).
@@ -242,14 +235,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
                          &full_bar[s], w_policy);
         }
       };
-      auto load_b = [&](int s, int b_tile_idx, int b_kk, int q) {
-        if constexpr (C::kConcat) {
-          tma_load_3d(b_tile(s), &p.tm_act[q], &full_bar[s], 0, b_tile_idx * C::kBRows, b_kk);
-        } else {
-          for (int bx = 0; bx < C::kBRows / C::kBBoxRows; ++bx)
-            tma_load_3d(b_tile(s) + bx * C::kBBoxRows * C::kKBytes, &p.tm_act[0], &full_bar[s], 0,
-                        b_tile_idx * C::kBRows + bx * C::kBBoxRows, b_kk);
-        }
+      auto load_b = [&](int s, int b_tile_idx, int b_kk, int rows) {
+        // the (stage, tile) image is contiguous and already swizzled: one bulk copy
+        bulk_load(b_tile(s), p.act_q + ((size_t)b_kk * p.max_tiles + b_tile_idx) * (size_t)(C::kBRows * C::kKBytes),
+                  (uint32_t)rows * (uint32_t)C::kKBytes, &full_bar[s]);
         // the stage's kAtoms K groups of scale atoms are adjacent
         bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * p.kg_sf + (size_t)b_kk * C::kAtoms) * (kSfAtomBytes * C::kNbAtoms),
                   C::kAtoms * C::kNbAtoms * kSfAtomBytes, &full_bar[s]);
@@ -260,19 +249,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         open_seg();
         // weights of the first stages depend only on the routing: stream them while
         // the previous kernel finishes
-        int pre_tile[C::kStages], pre_kk[C::kStages], pre_q[C::kStages];
+        int pre_tile[C::kStages], pre_kk[C::kStages], pre_rows[C::kStages];
         int npre = 0;
         while (npre < C::kStages && si < sch.nseg) {
           mbar_arrive_expect_tx(&full_bar[npre], tx_bytes());  // fresh stages: no wait
           load_a(npre);
           pre_tile[npre] = tile;
           pre_kk[npre] = kk;
-          pre_q[npre] = boxq;
+          pre_rows[npre] = b_rows;
           ++npre;
           advance();
         }
         pdl_wait();
-        for (int i = 0; i < npre; ++i) load_b(i, pre_tile[i], pre_kk[i], pre_q[i]);
+        for (int i = 0; i < npre; ++i) load_b(i, pre_tile[i], pre_kk[i], pre_rows[i]);
         g = npre;
         for (; si < sch.nseg; ++g) {
           const int s = g % C::kStages;
@@ -285,7 +274,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
           }
           mbar_arrive_expect_tx(&full_bar[s], tx_bytes());
           load_a(s);
-          load_b(s, tile, kk, boxq);
+          load_b(s, tile, kk, b_rows);
           advance();
         }
       } else {

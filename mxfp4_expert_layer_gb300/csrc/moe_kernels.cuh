@@ -98,10 +98,9 @@ cudaError_t launch_gather_x(const GatherXParams& p, cudaStream_t stream);
 struct GemmParams {
   // operand tensor maps (TMA)
   CUtensorMap tm_w;        // weights: packed E2M1 codes, row major [E*groups][rows][K/2 B]
-  // activations (x gathered, or h): packed E2M1 terms
-  // [stages][max_tiles*kTerms*bm][kstage/2 bytes]; tiles of at most 16 rows use box
-  // q = 4 * 2^q rows (q < kActBoxes), others box 0
-  CUtensorMap tm_act[kActBoxes];
+  // activations (x in tile order, or h): packed E2M1 terms, act_offset layout
+  // [stages][max_tiles][kTerms*bm rows][128 B], each (stage, tile) image pre-swizzled
+  const uint8_t* act_q;
   const uint8_t* w_sf;     // weight scale atoms [E][groups][mt][kg_sf][512]
   const uint8_t* act_sf;   // activation scale atoms [max_tiles][kg_sf][512 * act_sf_atoms]
   const TileEntry* tiles;

@@ -36,7 +36,6 @@ namespace {
 
 // warps: 0 TMA producer, 1 MMA issuer, 2-5 epilogue (one per tensor-memory lane
 // quarter), 6 second MMA issuer (used when a stage carries two weight tiles)
-constexpr int kGemmThreads = 224;
 constexpr int kSecondIssuerWarp = 6;
 constexpr uint64_t kWaitLimit = 1000000000ull;  // ns a bounded mbarrier wait may take (1 s)
 
@@ -61,11 +60,21 @@ struct GemmCfg {
   static constexpr int kSfBytes = (kA + kNbAtoms) * kAtoms * kSfAtomBytes;
   static constexpr int kStageRaw = kA * kATileBytes + kBBytes + kSfBytes;
   static constexpr int kStageBytes = (kStageRaw + 1023) / 1024 * 1024;
-  static constexpr int kEpiBytes = 16 * kMTile * 4 + 2 * 128 * 4;  // h transpose chunk + row metadata
-  static constexpr int kSmemBudget = 216 * 1024 - kEpiBytes;
+  // the epilogue reads the whole accumulator into registers before releasing it
+  static constexpr bool kLoadAll = kAccCols <= 128;
+  // larger tiles: two epilogue warp groups take alternate 16-column chunks of the
+  // accumulator (its long encode of h is latency-bound with one warp per scheduler)
+  static constexpr int kEpiGroups = kLoadAll ? 1 : 2;
+  static constexpr int kThreads = 224 + 128 * (kEpiGroups - 1);
+  static constexpr int kEpiGroupBytes = 16 * kMTile * 4 + 2 * 128 * 4;  // h transpose chunk + row metadata
+  static constexpr int kEpiBytes = kEpiGroups * kEpiGroupBytes;
+  static constexpr int kBarBytes = 2048;
+  // two groups: the whole 227 KB a block may have (two stages of the largest tile);
+  // one group: the depth measured best for the small tiles (a fifth BM=16 stage was slower)
+  static constexpr int kSmemBudget =
+      kEpiGroups == 2 ? 232448 - 1024 /*align*/ - kBarBytes - kEpiBytes : 216 * 1024 - kEpiBytes;
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kBarBytes = 2048;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
   static constexpr uint32_t kTxNoB = kA * kATileBytes + kSfBytes;                // all but the B codes
   // MMA issuers: with two weight tiles per stage each of two threads issues one
@@ -77,8 +86,6 @@ struct GemmCfg {
   static constexpr int kTmemNeed = kNumAcc * kAccCols + kSfCols;
   static constexpr int kTmemCols = kTmemNeed <= 32 ? 32 : kTmemNeed <= 64 ? 64 : kTmemNeed <= 128 ? 128
                                    : kTmemNeed <= 256 ? 256 : 512;
-  // the epilogue reads the whole accumulator into registers before releasing it
-  static constexpr bool kLoadAll = kAccCols <= 128;
   static_assert(kTmemNeed <= 512, "tensor memory budget");
   static_assert(kStages >= 2, "pipeline depth");
 };
@@ -120,13 +127,13 @@ struct Schedule {
 // the E2M1 encoding error that follows)
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __expf(-g)); }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 
 }  // namespace
 
 template <int BM, bool GATEUP, bool MPAIR>
-__global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
+    moe_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = GemmCfg<BM, GATEUP, MPAIR>;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -136,9 +143,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
   uint64_t* acce_bar = accf_bar + 2;             // [2] accumulator drained
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
   int* s_flags = reinterpret_cast<int*>(tmem_slot + 4);  // [0] error, [1] unit finisher
-  float* s_xpose = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);  // [16][128]
-  int* s_rowa = reinterpret_cast<int*>(s_xpose + 16 * kMTile);   // [128] assignment of each tile row
-  float* s_roww = reinterpret_cast<float*>(s_rowa + 128);         // [128] its top-k weight
+  // per epilogue group: h transpose [16][128], row assignment [128], its top-k weight [128]
+  uint8_t* epi_smem = smem + C::kStages * C::kStageBytes + C::kBarBytes;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&accf_bar[b], C::kIssuers);
-      mbar_init(&acce_bar[b], 128);
+      mbar_init(&acce_bar[b], 128 * C::kEpiGroups);
     }
     s_flags[0] = 0;
     fence_mbar_init();
@@ -364,12 +370,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         if (!err) mma_commit(&accf_bar[b]);
       }
     }
-  } else if (warp >= 2 && warp < 6) {
+  } else if ((warp >= 2 && warp < 6) || (C::kEpiGroups == 2 && warp >= 7 && warp < 11)) {
     // ------------------------------------------------------------ epilogue
     pdl_wait();  // h (down) comes from the immediately preceding kernel
+    const int eg = warp < 6 ? 0 : 1;       // epilogue group: warps 2-5, or 7-10
     const int q = warp & 3;                // tensor-memory lane quarter of this warp
     const int m = q * 32 + lane;           // row of the 128-row tile
-    const int et = threadIdx.x - 64;       // 0..127 within the epilogue warps
+    const int et = threadIdx.x - (eg == 0 ? 64 : 224);  // 0..127 within the group
+    float* s_xpose = reinterpret_cast<float*>(epi_smem + eg * C::kEpiGroupBytes);
+    int* s_rowa = reinterpret_cast<int*>(s_xpose + 16 * kMTile);
+    float* s_roww = reinterpret_cast<float*>(s_rowa + 128);
+    auto epi_bar = [eg]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + eg) : "memory"); };
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int i_pad = (p.I + 63) / 64 * 64;  // h features written (zeros past I)
     for (int si = 0; si < sch.nseg; ++si) {
@@ -505,8 +516,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1) moe_gemm_kernel(const __grid_
         for (int c0 = 0; c0 < BM; c0 += 16)
           if (c0 < nrows) consume(c0, vals + c0, C::kA > 1 ? vals + BM + c0 : nullptr);
       } else {
-        // accumulator too large for registers (per-term MMAs): 16 columns at a time
-        for (int c0 = 0; c0 < BM; c0 += 16) {
+        // accumulator too large for registers (per-term MMAs): 16 columns at a time,
+        // the groups taking alternate chunks
+        for (int c0 = 16 * eg; c0 < BM; c0 += 16 * C::kEpiGroups) {
           if (c0 >= nrows) break;
           uint32_t rg[16], ru[16];
           float va[16], vb[16];
@@ -547,7 +559,7 @@ static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  return launch_pdl(kern, dim3(p.grid), dim3(kGemmThreads), C::kSmemBytes, stream, p);
+  return launch_pdl(kern, dim3(p.grid), dim3(C::kThreads), C::kSmemBytes, stream, p);
 }
 
 template <bool GATEUP, bool MPAIR>

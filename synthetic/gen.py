@@ -92,6 +92,9 @@ CONFIGS = {
     "gptoss120b_b64": LayerConfig(
         "gptoss120b_b64", T=64, H=2880, I=2880, E=128, k=4, scale_lo=120, scale_hi=124,
         description="gpt-oss-120b-shaped MoE layer, decode batch 64"),
+    "gptoss120b_b1": LayerConfig(
+        "gptoss120b_b1", T=1, H=2880, I=2880, E=128, k=4, scale_lo=120, scale_hi=124,
+        description="gpt-oss-120b-shaped MoE layer, decode batch 1"),
     "gptoss120b_prefill4096": LayerConfig(
         "gptoss120b_prefill4096", T=4096, H=2880, I=2880, E=128, k=4, scale_lo=120,
         scale_hi=124, zipf_s=1.1, zipf_beta=1.0,
@@ -138,6 +141,16 @@ def make_config(name: str, seed: int = 0, T: Optional[int] = None) -> LayerInput
     return make_layer(c.T if T is None else T, c.H, c.I, c.E, c.k, seed=seed,
                       scale_lo=c.scale_lo, scale_hi=c.scale_hi, zipf_s=c.zipf_s,
                       zipf_beta=c.zipf_beta, name=name)
+
+
+def make_norm_inputs(T: int, H: int, seed: int = 0):
+    """Inputs of the RMSNorm + residual step before the layer: the residual stream
+    (bf16 [T, H], normal with standard deviation 2), the per-feature norm weight
+    (bf16 [H], 1 + 0.25 * normal) and eps = 1e-5."""
+    rng = np.random.Generator(np.random.PCG64(seed + 7919))
+    residual = bf16_bits_from_f32(2.0 * rng.standard_normal((T, H), dtype=np.float32))
+    gamma = bf16_bits_from_f32(1.0 + 0.25 * rng.standard_normal(H, dtype=np.float32))
+    return residual, gamma, 1e-5
 
 
 def random_logits(T: int, E: int, seed: int = 0, n_ties: int = 0) -> np.ndarray:

@@ -122,6 +122,10 @@ def test_layer_gptoss20b_b64():
     check_layer(make_config("gptoss20b_b64"))
 
 
+def test_layer_gptoss120b_b1():
+    check_layer(make_config("gptoss120b_b1"))
+
+
 def test_layer_gptoss120b_b64_sampled():
     check_layer(make_config("gptoss120b_b64"), tokens=np.arange(0, 64, 4))
 

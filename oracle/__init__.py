@@ -11,6 +11,7 @@ from .moe_oracle import (  # noqa: F401
     GATING_SIGMOID,
     GATING_SOFTMAX_ALL,
     GATING_SOFTMAX_TOPK,
+    bf16_bits,
     bf16_round,
     bf16_to_f32,
     decode_e8m0,
@@ -18,6 +19,8 @@ from .moe_oracle import (  # noqa: F401
     expert_hidden,
     expert_output,
     moe_layer,
+    moe_layer_norm,
+    rmsnorm_residual,
     router_logits,
     tile_rows_policy,
     tile_table,

@@ -220,6 +220,49 @@ def expert_output(h_rows: np.ndarray, dn_codes_e, dn_scales_e, dtype=np.float32)
     return (np.asarray(h_rows, dtype=dtype) @ w.T).astype(dtype)
 
 
+def bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round to the nearest bf16 (ties to even) and return the bit patterns."""
+    return (bf16_round(a).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def rmsnorm_residual(x_bits: np.ndarray, r_bits: np.ndarray, gamma_bits: np.ndarray, eps: float,
+                     dtype=np.float32):
+    """The step before the router on every decode layer: residual add, then RMSNorm.
+
+    "triton-kernels" README (github bassrehab/triton-kernels), section "Kernels"
+    (row ``rmsnorm_residual_fused``) and section "Quick Start", "Fused RMSNorm +
+    Residual": the normalisation of x + residual with a per-feature weight and eps;
+    "A 297-line kernel file that decodes faster than vLLM" (cloudy.so), section "Where
+    the time went", row "RMSNorm + residual" (the step just before "Router + top-k").
+    RMSNorm itself (Zhang & Sennrich, 2019): y = s / sqrt(mean(s^2) + eps) * gamma.
+
+    Readings: the sum s = x + r is what the bf16 residual stream holds, so it is
+    rounded to bf16 once (from its float32 value) and the norm is taken of that
+    rounded s; y is rounded to bf16 (the layer's activations are bf16).
+    Returns (s, y) as bf16 bit patterns, [T, H] each.
+    """
+    x = bf16_to_f32(x_bits)
+    r = bf16_to_f32(r_bits)
+    s = bf16_round((x + r).astype(np.float32))
+    sd = s.astype(dtype)
+    ms = np.mean(sd * sd, axis=-1, keepdims=True)
+    y = sd / np.sqrt(ms + dtype(eps)) * bf16_to_f32(gamma_bits).astype(dtype)
+    return bf16_bits(s), bf16_bits(y.astype(np.float32))
+
+
+def moe_layer_norm(inp, residual_bits: np.ndarray, gamma_bits: np.ndarray, eps: float,
+                   dtype=np.float32, **kw):
+    """RMSNorm + residual (``rmsnorm_residual``), then the layer on the normalised
+    rows: ``moe_layer`` with x replaced by y.  The result adds "residual_out" (s) and
+    "x_norm" (y), bf16 bit patterns of all T rows."""
+    import dataclasses
+    s_bits, y_bits = rmsnorm_residual(inp.x, residual_bits, gamma_bits, eps, dtype)
+    res = moe_layer(dataclasses.replace(inp, x=y_bits), dtype=dtype, **kw)
+    res["residual_out"] = s_bits
+    res["x_norm"] = y_bits
+    return res
+
+
 def moe_layer(inp, dtype=np.float32, tokens=None, logits=None, return_hidden=False,
               gating=GATING_SOFTMAX_TOPK):
     """The whole layer on the tokens ``tokens`` (default: all).

@@ -13,6 +13,7 @@ from .gen import (  # noqa: F401
     bf16_bits_to_f32,
     make_layer,
     make_config,
+    make_norm_inputs,
     random_logits,
     random_topk_idx,
     zipf_router_bias,

@@ -177,3 +177,70 @@ def test_layer_matches_torch_cpu_library_path():
     assert np.array_equal(top.indices.numpy(), res["idx"])
     ref = out.numpy()
     assert np.abs(res["out_unrounded"] - ref).max() <= 1e-5 * np.abs(ref).max()
+
+
+def _f(bits):
+    return oracle.bf16_to_f32(bits)
+
+
+def _b(vals):
+    return oracle.bf16_bits(np.asarray(vals, dtype=np.float32))
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_rmsnorm_residual_closed_forms(dtype):
+    # s = (1 + 2, 4 + 0) = (3, 4): mean square 12.5; y = (3, 4) / sqrt(12.5), rounded by
+    # hand to bf16: 0.848528 -> 217 * 2^-8, 1.131371 -> 145 * 2^-7
+    s, y = oracle.rmsnorm_residual(_b([[1, 4]]), _b([[2, 0]]), _b([1, 1]), 0.0, dtype)
+    assert np.array_equal(_f(s), np.array([[3.0, 4.0]], np.float32))
+    assert np.array_equal(_f(y), np.array([[217 * 2.0 ** -8, 145 * 2.0 ** -7]], np.float32))
+    # eps inside the root: 12.5 + 3.5 = 16 -> (0.75, 1), and the weight multiplies
+    _, y = oracle.rmsnorm_residual(_b([[3, 4]]), _b([[0, 0]]), _b([1, -2]), 3.5, dtype)
+    assert np.array_equal(_f(y), np.array([[0.75, -2.0]], np.float32))
+    # a row of +-c has rms c: y is the sign times the weight, whatever c (eps 0)
+    g = _b(np.linspace(-1.5, 1.5, 64))
+    for c in (3.0, 0.375, 96.0):
+        row = np.where(np.arange(64) % 2 == 0, c, -c)
+        _, y = oracle.rmsnorm_residual(_b(row[None]), _b(np.zeros((1, 64))), g, 0.0, dtype)
+        assert np.array_equal(_f(y)[0], np.sign(row) * _f(g))
+    # a zero row with eps > 0 normalises to zeros
+    _, y = oracle.rmsnorm_residual(_b(np.zeros((1, 8))), _b(np.zeros((1, 8))), _b(np.ones(8)), 1e-5, dtype)
+    assert np.array_equal(_f(y), np.zeros((1, 8), np.float32))
+
+
+def test_rmsnorm_residual_rounds_the_stream_once():
+    # 1 + 2^-9 is a quarter bf16 ulp above 1 (rounds down), 1 + 3 * 2^-9 three
+    # quarters (rounds up to 1 + 2^-7): the sum is held in bf16 before the norm
+    s, _ = oracle.rmsnorm_residual(_b([[1.0, 1.0]]), _b([[2.0 ** -9, 3 * 2.0 ** -9]]), _b([1, 1]), 0.0)
+    assert np.array_equal(_f(s), np.array([[1.0, 1.0 + 2.0 ** -7]], np.float32))
+
+
+def test_rmsnorm_residual_invariants():
+    from synthetic import make_norm_inputs
+    inp = make_layer(T=16, H=384, I=64, E=4, k=2, seed=5)
+    r, g, _ = make_norm_inputs(16, 384, seed=5)
+    s, y = oracle.rmsnorm_residual(inp.x, r, g, 0.0, np.float64)
+    # unit weight: every row has mean square 1 up to bf16 rounding
+    _, y1 = oracle.rmsnorm_residual(inp.x, r, _b(np.ones(384)), 0.0, np.float64)
+    ms = np.mean(_f(y1).astype(np.float64) ** 2, axis=1)
+    assert np.all(np.abs(ms - 1.0) < 4e-3)
+    # scaling the stream by a power of two changes nothing (eps 0), and x and the
+    # residual enter only through their sum
+    s2, y2 = oracle.rmsnorm_residual(_b(_f(inp.x) * 8), _b(_f(r) * 8), g, 0.0, np.float64)
+    assert np.array_equal(y2, y) and np.array_equal(_f(s2), _f(s) * 8)
+    s3, y3 = oracle.rmsnorm_residual(r, inp.x, g, 0.0, np.float64)
+    assert np.array_equal(s3, s) and np.array_equal(y3, y)
+
+
+def test_layer_norm_is_scale_free_and_routes_on_the_normalised_rows():
+    from synthetic import make_norm_inputs
+    inp = make_config("tiny")
+    r, g, _ = make_norm_inputs(inp.T, inp.H, seed=3)
+    a = oracle.moe_layer_norm(inp, r, g, 0.0)
+    import dataclasses
+    b = oracle.moe_layer_norm(dataclasses.replace(inp, x=_b(_f(inp.x) * 4)), _b(_f(r) * 4), g, 0.0)
+    assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["idx"], b["idx"])
+    assert np.array_equal(_f(b["residual_out"]), _f(a["residual_out"]) * 4)
+    # the router sees y: its logits are y @ W_r^T
+    lg = _f(a["x_norm"]).astype(np.float64) @ _f(inp.w_router).astype(np.float64).T
+    assert np.allclose(a["logits"], lg, rtol=1e-5, atol=1e-5)

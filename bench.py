@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--norm", action="store_true",
+                    help="RMSNorm + residual fused in front of the layer (moe_forward_norm)")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA-graph replays")
     ap.add_argument("--profile", action="store_true",
                     help="minimal run for ncu: no pre-warm, no graphs, no CPU baseline, no clock sampling")
@@ -258,15 +260,28 @@ def main():
     # touched experts of every call come from HBM and nothing a real model would not
     # find in L2 (another layer's router, another step's activations) is found there
     copies = max(1, min(16, math.ceil(4 * L2_BYTES / max(alg_bytes, 1))))
-    wsets = [(layer.w_gateup, layer.w_down, wr, x)] + [
-        (layer.w_gateup.clone(), layer.w_down.clone(), wr.clone(), x.clone()) for _ in range(copies - 1)]
+    if args.norm:
+        from synthetic import make_norm_inputs
+        r_np, g_np, eps = make_norm_inputs(T, H, seed=rank)
+        resid = to(r_np.view(np.int16)).view(torch.bfloat16)
+        gamma = to(g_np.view(np.int16)).view(torch.bfloat16)
+        res_out = torch.empty_like(x)
+    else:
+        resid = x  # unused
+    wsets = [(layer.w_gateup, layer.w_down, wr, x, resid)] + [
+        (layer.w_gateup.clone(), layer.w_down.clone(), wr.clone(), x.clone(), resid.clone())
+        for _ in range(copies - 1)]
     ws = layer.workspace(T)
 
-    def call(i, events=None):
-        wgu, wd, wr_i, x_i = wsets[i % copies]
+    def call(i, events=None, norm=args.norm):
+        wgu, wd, wr_i, x_i, r_i = wsets[i % copies]
         b = None if bias is None else bias.data_ptr()
         cs = torch.cuda.current_stream().cuda_stream
-        if events is None:
+        if norm and events is None:
+            st = L.moe_forward_norm(x_i.data_ptr(), r_i.data_ptr(), gamma.data_ptr(), eps, wr_i.data_ptr(), b,
+                                    wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k, 0, ws.data_ptr(), ws.numel(),
+                                    out.data_ptr(), res_out.data_ptr(), None, None, cs)
+        elif events is None:
             st = L.moe_forward(x_i.data_ptr(), wr_i.data_ptr(), b, wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k,
                                ws.data_ptr(), ws.numel(), out.data_ptr(), None, None, cs)
         else:
@@ -297,6 +312,8 @@ def main():
     graphs, tgraphs, tevents = [], [], []
     hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
     hx.copy_(x.cpu())
+    hr = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+    hr.copy_(resid.cpu())
     hout = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
     e2e_graphs = []
     with torch.cuda.stream(side):
@@ -319,6 +336,8 @@ def main():
             eg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(eg, stream=side):
                 wsets[j][3].copy_(hx, non_blocking=True)
+                if args.norm:
+                    wsets[j][4].copy_(hr, non_blocking=True)
                 call(j)
                 hout.copy_(out, non_blocking=True)
             e2e_graphs.append(eg)
@@ -326,6 +345,12 @@ def main():
         with torch.cuda.graph(step_graph, stream=side):
             for j in range(step_calls):
                 call(j)
+        if args.norm:
+            # the same step without the norm step, for its cost
+            plain_graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(plain_graph, stream=side):
+                for j in range(step_calls):
+                    call(j, norm=False)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -367,6 +392,17 @@ def main():
     ms = ev0.elapsed_time(ev1) / args.steps
     ms = max_over_ranks(ms, world)
     i += args.steps
+
+    plain_us = None
+    if args.norm:
+        torch.cuda.synchronize()
+        reps_p = max(1, args.steps // step_calls)
+        ev0.record(stream)
+        for _ in range(reps_p):
+            plain_graph.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        plain_us = ev0.elapsed_time(ev1) * 1e3 / (reps_p * step_calls)
 
     # eager launches, for reference (host launch overhead included)
     torch.cuda.synchronize()
@@ -452,12 +488,18 @@ def main():
         "per_kernel_us": {n: v * 1e3 for n, v in zip(names, per_kernel)},
         "roofline": roof,
         "tensor_pipe": tensor_pipe,
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": T * H * 2 * (2 if args.norm else 1),
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms},
         "gpu_launches": launches * args.steps,
         "clocks": clk,
         "device_status": status,
     }
+    if args.norm:
+        line["config"]["norm"] = "RMSNorm + residual fused in front of the layer (moe_forward_norm)"
+        line["norm_step"] = {"us_per_call_without_norm": plain_us, "added_us": us - plain_us,
+                             "per_kernel_note": "per_kernel_us and roofline come from the layer's timed "
+                                                "graphs without the norm step"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp)
     print(json.dumps(line))

@@ -194,6 +194,29 @@ int moe_forward_gated(const uint16_t* x, const uint16_t* w_router, const float* 
                       size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
                       moe_stream_t stream);
 
+/* moe_forward_norm: the step before the layer fused into it, then the layer:
+ *   s = bf16(x + residual)                      (the residual stream, returned)
+ *   y = bf16(s / sqrt(mean_H(s^2) + eps) * norm_weight)
+ *   out = MoE(y)  (moe_forward_gated on y; `gating` as there).
+ * Sources: "triton-kernels" README, "Kernels" (rmsnorm_residual_fused) and "Quick
+ * Start", "Fused RMSNorm + Residual"; the decode-engine page "A 297-line kernel file
+ * that decodes faster than vLLM", "Where the time went", row "RMSNorm + residual".
+ * No launch is added: the routing kernel and the encoder each normalise the rows
+ * they read (the same bits: one fixed summation order), and the combine kernel
+ * writes residual_out.
+ *   x, residual bf16 [T, H]; norm_weight bf16 [H]; all 16-byte aligned.
+ *   eps: finite and >= 0.
+ *   residual_out: bf16 [T, H] or NULL.  It may be x or residual itself: it is
+ *   written after every read of both.  It may not be `out`.
+ * Errors: MOE_ERR_INVALID_ARG for a NULL or misaligned x, residual or norm_weight,
+ * a bad eps or gating value, or residual_out == out.  Everything else is as for
+ * moe_forward.                                                                     */
+int moe_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* norm_weight, float eps,
+                     const uint16_t* w_router, const float* router_bias, const void* w_gateup, const void* w_down,
+                     int T, int H, int I, int E, int k, int gating, void* workspace, size_t workspace_bytes,
+                     uint16_t* out, uint16_t* residual_out, int32_t* topk_idx_out, float* topk_w_out,
+                     moe_stream_t stream);
+
 /* moe_forward: the whole layer, out = MoE(x), on one stream with no host sync.
  *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL;
  *   w_gateup / w_down: prepared weights; out bf16 [T, H];

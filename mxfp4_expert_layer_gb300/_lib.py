@@ -44,6 +44,8 @@ SIGNATURES = {
     "moe_hidden_dequant": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P, _P]),
     "moe_forward": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P]),
     "moe_forward_gated": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P]),
+    "moe_forward_norm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P, _P,
+                              _P, _P, _P]),
     "moe_forward_timed": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P, _P]),
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I]),
     "moe_get_device_status": (_I, [_P, _S, ctypes.POINTER(_I), _P]),
@@ -102,6 +104,7 @@ moe_mxfp4_down_combine = _call("moe_mxfp4_down_combine")
 moe_hidden_dequant = _call("moe_hidden_dequant")
 moe_forward = _call("moe_forward")
 moe_forward_gated = _call("moe_forward_gated")
+moe_forward_norm = _call("moe_forward_norm")
 moe_forward_timed = _call("moe_forward_timed")
 moe_forward_launches = _call("moe_forward_launches")
 moe_get_device_status = _call("moe_get_device_status")

@@ -131,13 +131,27 @@ class MoELayer:
         return ws
 
     def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, topk_idx=None, topk_w=None,
-                ws: Optional[torch.Tensor] = None, gating: int = 0) -> torch.Tensor:
+                ws: Optional[torch.Tensor] = None, gating: int = 0, residual: Optional[torch.Tensor] = None,
+                norm_weight: Optional[torch.Tensor] = None, eps: float = 1e-5,
+                residual_out: Optional[torch.Tensor] = None) -> torch.Tensor:
+        """out = MoE(x); with ``residual`` and ``norm_weight``, out = MoE(RMSNorm(x +
+        residual)) and, when given, ``residual_out`` receives bf16(x + residual)
+        (moe_forward_norm)."""
         _need_cuda(x)
         T = x.shape[0]
         if out is None:
             out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
         if ws is None:
             ws = self.workspace(T)
+        if residual is not None or norm_weight is not None:
+            if residual is None or norm_weight is None:
+                raise ValueError("the norm step needs both residual and norm_weight")
+            L.check("moe_forward_norm", L.moe_forward_norm(
+                x.data_ptr(), residual.data_ptr(), norm_weight.data_ptr(), eps, self.w_router.data_ptr(),
+                _ptr(self.router_bias), self.w_gateup.data_ptr(), self.w_down.data_ptr(), T, self.H, self.I,
+                self.E, self.k, gating, ws.data_ptr(), ws.numel(), out.data_ptr(), _ptr(residual_out),
+                _ptr(topk_idx), _ptr(topk_w), _stream()))
+            return out
         if gating:
             L.check("moe_forward_gated", L.moe_forward_gated(
                 x.data_ptr(), self.w_router.data_ptr(), _ptr(self.router_bias), self.w_gateup.data_ptr(),

@@ -165,9 +165,10 @@ int run_encode_x(const uint16_t* x, int T, int H, void* ws, const WsLayout& L, c
 // Per-token activation encoding that overlaps the routing launch before it, waits
 // for it, and writes the encoded rows straight into tile order (the permute step).
 int run_encode_permute_x(const uint16_t* x, const int32_t* idx, int T, int H, int E, int k, int bm, void* ws,
-                         const WsLayout& L, cudaStream_t stream) {
+                         const WsLayout& L, cudaStream_t stream, const NormArgs& norm = NormArgs{}) {
   EncodeXParams q{};
   q.x = x;
+  q.norm = norm;
   q.T = T; q.H = H;
   q.wait_at_end = 1;
   q.scatter = 1;
@@ -227,7 +228,8 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
 
 int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm, const float* topk_w,
              const void* w_down, int T, int H, int I, int E, int k, void* ws, const WsLayout& L, uint16_t* out,
-             cudaStream_t stream) {
+             cudaStream_t stream, const uint16_t* x = nullptr, const uint16_t* residual = nullptr,
+             uint16_t* residual_out = nullptr) {
   const PreparedLayout P = make_prepared_layout(E, H, I, 1);
   GemmParams g{};
   if (!weight_map(&g.tm_w, w_down, P, bm)) return MOE_ERR_CUDA;
@@ -258,6 +260,9 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   c.slots = g.slots;
   c.T = T; c.H = H; c.k = k;
   c.out = out;
+  c.x = x;
+  c.residual = residual;
+  c.residual_out = residual_out;
   return cuda_status(launch_combine(c, stream));
 }
 
@@ -444,7 +449,8 @@ int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t*
 static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float* router_bias,
                         const void* w_gateup, const void* w_down, int T, int H, int I, int E, int k,
                         void* workspace, size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out,
-                        float* topk_w_out, void* const* events, moe_stream_t stream, int gating = kGatingSoftmaxTopk) {
+                        float* topk_w_out, void* const* events, moe_stream_t stream, int gating = kGatingSoftmaxTopk,
+                        const NormArgs& norm = NormArgs{}, uint16_t* residual_out = nullptr) {
   int st = check_shape(T, H, I, E, k);
   if (st != MOE_OK) return st;
   if (!x || !w_router || !w_gateup || !w_down || !workspace || !out) return MOE_ERR_INVALID_ARG;
@@ -473,6 +479,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   r.tiles = tiles;
   r.num_tiles = num_tiles;
   r.tile_first = ws_ptr<int32_t>(ws, L.tile_first);
+  r.norm = norm;
   bool ev_ok = true;
   auto mark = [&](int i) {
     if (events && record_event(events[i], s) != cudaSuccess) ev_ok = false;
@@ -484,13 +491,14 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   if (!ev_ok) return MOE_ERR_INVALID_ARG;
   if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
   mark(1);
-  st = run_encode_permute_x(x, idx, T, H, E, k, bm, ws, L, s);
+  st = run_encode_permute_x(x, idx, T, H, E, k, bm, ws, L, s, norm);
   if (st != MOE_OK) return st;
   mark(2);
   st = run_gateup(perm, tiles, num_tiles, bm, w_gateup, T, H, I, E, k, ws, L, s);
   if (st != MOE_OK) return st;
   mark(3);
-  st = run_down(perm, tiles, num_tiles, bm, w, w_down, T, H, I, E, k, ws, L, out, s);
+  st = run_down(perm, tiles, num_tiles, bm, w, w_down, T, H, I, E, k, ws, L, out, s, x, norm.residual,
+                residual_out);
   mark(4);
   return st;
 }
@@ -510,6 +518,24 @@ int moe_forward_gated(const uint16_t* x, const uint16_t* w_router, const float* 
   if (g < 0 || (gating & MOE_ROUTE_FROM_LOGITS)) return MOE_ERR_INVALID_ARG;
   return forward_impl(x, w_router, router_bias, w_gateup, w_down, T, H, I, E, k, workspace, workspace_bytes, out,
                       topk_idx_out, topk_w_out, nullptr, stream, g);
+}
+
+int moe_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t* norm_weight, float eps,
+                     const uint16_t* w_router, const float* router_bias, const void* w_gateup, const void* w_down,
+                     int T, int H, int I, int E, int k, int gating, void* workspace, size_t workspace_bytes,
+                     uint16_t* out, uint16_t* residual_out, int32_t* topk_idx_out, float* topk_w_out,
+                     moe_stream_t stream) {
+  const int g = gating == 0 ? kGatingSoftmaxTopk : gating_from_flags(gating);
+  if (g < 0 || (gating & MOE_ROUTE_FROM_LOGITS)) return MOE_ERR_INVALID_ARG;
+  if (!residual || !norm_weight || !aligned(residual, 16) || !aligned(norm_weight, 16)) return MOE_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !(eps < 3.0e38f)) return MOE_ERR_INVALID_ARG;  // negative, NaN or infinite
+  if (residual_out && (!aligned(residual_out, 16) || residual_out == out)) return MOE_ERR_INVALID_ARG;
+  NormArgs norm;
+  norm.residual = residual;
+  norm.norm_w = norm_weight;
+  norm.eps = eps;
+  return forward_impl(x, w_router, router_bias, w_gateup, w_down, T, H, I, E, k, workspace, workspace_bytes, out,
+                      topk_idx_out, topk_w_out, nullptr, stream, g, norm, residual_out);
 }
 
 int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,

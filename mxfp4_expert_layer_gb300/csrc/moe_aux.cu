@@ -59,8 +59,15 @@ __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) 
   const int v = chunk * 32 + lane;
   const int nvec = p.H / 8;
   float f[8];
+  // with the norm step, the row's 1 / rms (the same bits the router computes)
+  const float rinv = p.norm.norm_w ? norm_row_rinv(p.x + (size_t)t * p.H, p.norm.residual + (size_t)t * p.H, p.H,
+                                                   p.norm.eps)
+                                   : 0.f;
   if (v < nvec) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + v);
+    uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + v);
+    if (p.norm.norm_w)
+      raw = norm_apply8(raw, __ldg(reinterpret_cast<const uint4*>(p.norm.residual + (size_t)t * p.H) + v),
+                        __ldg(reinterpret_cast<const uint4*>(p.norm.norm_w) + v), rinv);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -207,7 +214,24 @@ __global__ void __launch_bounds__(kAuxThreads) combine_kernel(CombineParams p) {
                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.y)) << 16);
   const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.z)) |
                       ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc.w)) << 16);
+  // the residual stream after the norm step's add, read before out is written and
+  // written by the thread that read it: out and residual_out may each alias x or residual
+  uint2 res = make_uint2(0, 0);
+  if (p.residual_out) {
+    const uint2 xv = reinterpret_cast<const uint2*>(p.x + (size_t)t * p.H)[q];
+    const uint2 rv = reinterpret_cast<const uint2*>(p.residual + (size_t)t * p.H)[q];
+    const uint32_t xw[2] = {xv.x, xv.y}, rw[2] = {rv.x, rv.y};
+    uint32_t o[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float a = bf16_round_f32(__fadd_rn(__uint_as_float(xw[i] << 16), __uint_as_float(rw[i] << 16)));
+      const float b = bf16_round_f32(__fadd_rn(__uint_as_float(xw[i] & 0xFFFF0000u), __uint_as_float(rw[i] & 0xFFFF0000u)));
+      o[i] = (__float_as_uint(a) >> 16) | (__float_as_uint(b) & 0xFFFF0000u);
+    }
+    res = make_uint2(o[0], o[1]);
+  }
   reinterpret_cast<uint2*>(p.out + (size_t)t * p.H)[q] = make_uint2(lo, hi);
+  if (p.residual_out) reinterpret_cast<uint2*>(p.residual_out + (size_t)t * p.H)[q] = res;
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {

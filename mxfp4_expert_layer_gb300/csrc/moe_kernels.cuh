@@ -53,6 +53,7 @@ struct RouteParams {
   int32_t* tile_first;      // i32 [E]: index of each expert's first tile (or null)
   TileEntry* tiles;
   uint32_t* status;
+  NormArgs norm;            // the router sees y = RMSNorm(x + residual) (norm.norm_w set)
 };
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream);
@@ -78,6 +79,7 @@ struct EncodeXParams {
   int E, k, bm, max_tiles, kg_tile;
   uint8_t* q_tile;            // GatherXParams::q layout
   uint8_t* sf_tile;           // GatherXParams::sf layout
+  NormArgs norm;              // encode y = RMSNorm(x + residual) instead of x (norm.norm_w set)
 };
 cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream);
 
@@ -133,6 +135,11 @@ struct CombineParams {
   const float* slots;      // f32 [T*k, H], slot t*k + j = w_tj * y_tj
   int T, H, k;
   uint16_t* out;           // bf16 [T, H]
+  // optional residual stream output bf16(x + residual) (the norm step's sum); written
+  // here, after every reader of x and residual has finished, so it may alias either
+  const uint16_t* x;
+  const uint16_t* residual;
+  uint16_t* residual_out;
 };
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 

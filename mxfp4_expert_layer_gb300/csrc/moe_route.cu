@@ -457,9 +457,10 @@ constexpr int kMmaIlp = 4;  // 8-expert column blocks per warp pass (one A fragm
 struct ClusterRouteSmem {
   int mrows, erows, pitch;        // staged x rows (multiple of 16), router rows (multiple of 8), row bytes
   int nitems, nsplit;
-  size_t x_off, w_off, split_off, recv_off, lg_off, bias_off, idx_off, bar_off, total;
+  size_t x_off, w_off, split_off, recv_off, lg_off, bias_off, idx_off, norm_off, bar_off, total;
 };
-__host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int E, int k) {
+static_assert(kClusterCtas == kNormSlices, "a cluster CTA sums one range of the norm's row cut");
+__host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int E, int k, bool norm) {
   ClusterRouteSmem L;
   const int ksteps = H / 16;
   const int kmax = ((ksteps + kClusterCtas - 1) / kClusterCtas) * 16;  // largest slice, elements
@@ -478,7 +479,10 @@ __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int
   L.lg_off = L.recv_off + sizeof(float) * (size_t)kClusterCtas * kTokensPerGroup * L.erows;
   L.bias_off = L.lg_off + sizeof(float) * (size_t)kTokensPerGroup * L.erows;
   L.idx_off = L.bias_off + sizeof(float) * (size_t)L.erows;
-  L.bar_off = L.idx_off + ((sizeof(int32_t) * (size_t)T * k + 15) / 16) * 16;
+  L.norm_off = L.idx_off + ((sizeof(int32_t) * (size_t)T * k + 15) / 16) * 16;
+  // norm step: [kClusterCtas][mrows] range sums received, [mrows] own sums, [mrows] 1 / rms
+  const size_t norm_bytes = norm ? sizeof(float) * (size_t)(kClusterCtas + 2) * L.mrows : 0;
+  L.bar_off = L.norm_off + norm_bytes;
   L.total = L.bar_off + 32;
   return L;
 }
@@ -491,7 +495,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   namespace cg = cooperative_groups;
   const int rank = (int)cg::this_cluster().block_rank();
-  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k);
+  const bool norm = p.norm.norm_w != nullptr;
+  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k, norm);
   uint8_t* xs = rc_smem + L.x_off;
   uint8_t* wsm = rc_smem + L.w_off;
   float* split = reinterpret_cast<float*>(rc_smem + L.split_off);  // [nsplit][mrows][erows]
@@ -503,6 +508,10 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   uint64_t* bar_stage = bar;      // this CTA's operand slices have landed
   uint64_t* bar_part = bar + 1;   // every peer's partials of this CTA's tokens have landed
   uint64_t* bar_idx = bar + 2;    // (CTA 0) every token's top-k indices have landed
+  uint64_t* bar_norm = bar + 3;   // (norm step) every CTA's range sums have landed
+  float* norm_recv = reinterpret_cast<float*>(rc_smem + L.norm_off);  // [src rank][mrows]
+  float* norm_own = norm_recv + kClusterCtas * L.mrows;               // [mrows]
+  float* norm_rinv_s = norm_own + L.mrows;                            // [mrows]
   const int t_own = rank * kTokensPerGroup;
   const int n_own = max(0, min(kTokensPerGroup, p.T - t_own));
   const bool builds = rank == 0 && p.build_table;
@@ -515,7 +524,9 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     mbar_init(bar_stage, 1);
     mbar_init(bar_part, 1);
     mbar_init(bar_idx, 1);
+    mbar_init(bar_norm, 1);
     fence_mbar_init();
+    if (norm) mbar_arrive_expect_tx(bar_norm, (uint32_t)(kClusterCtas * p.T * sizeof(float)));
     if (n_own > 0) mbar_arrive_expect_tx(bar_part, (uint32_t)(kClusterCtas * n_own * L.erows * sizeof(float)));
     if (builds) mbar_arrive_expect_tx(bar_idx, (uint32_t)(p.T * p.k * sizeof(int32_t)));
     if (slice_bytes > 0) mbar_arrive_expect_tx(bar_stage, slice_bytes * (uint32_t)(p.T + p.E));
@@ -536,6 +547,13 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     for (int r = tid; r < p.T; r += kRouteThreads)
       bulk_load(xs + (size_t)r * L.pitch, p.x + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
   }
+  if (norm) {
+    // norm step: this CTA's range of every row (the same range cut every kernel uses)
+    for (int t = warp; t < p.T; t += kRouteWarps) {
+      const float ssq = norm_range_ssq(p.x + (size_t)t * p.H, p.norm.residual + (size_t)t * p.H, 2 * ks0, 2 * ks1);
+      if (lane == 0) norm_own[t] = ssq;
+    }
+  }
   // rows the copies never touch: x rows past T, router rows past E
   for (int i = tid; i < (L.mrows - p.T) * (L.pitch / 16); i += kRouteThreads) {
     const int r = p.T + i / (L.pitch / 16), c = i % (L.pitch / 16);
@@ -548,6 +566,33 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   if (slice_bytes > 0 && !mbar_wait_bounded(bar_stage, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
   __syncthreads();  // zero rows and the bias written by other threads
   cluster_wait_acquire();  // every peer's barriers are initialised: pushes may start
+  if (norm) {
+    // every CTA gets every range sum, adds them in range order (the same bits in
+    // every CTA and in the encoder) and turns its x slice into y in place
+    for (int i = tid; i < p.T * kClusterCtas; i += kRouteThreads) {
+      const int t = i / kClusterCtas;
+      const uint32_t dst = (uint32_t)(i - t * kClusterCtas);
+      st_async_b32(mapa_shared(smem_u32(norm_recv + rank * L.mrows + t), dst), __float_as_uint(norm_own[t]),
+                   mapa_shared(smem_u32(bar_norm), dst));
+    }
+    if (!mbar_wait_cluster_bounded(bar_norm, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
+    for (int t = tid; t < p.T; t += kRouteThreads) {
+      float part[kNormSlices];
+#pragma unroll
+      for (int q = 0; q < kNormSlices; ++q) part[q] = norm_recv[q * L.mrows + t];
+      norm_rinv_s[t] = norm_rinv(part, p.H, p.norm.eps);
+    }
+    __syncthreads();
+    const int nv = 2 * (ks1 - ks0);
+    const uint4* rres = reinterpret_cast<const uint4*>(p.norm.residual);
+    const uint4* gam = reinterpret_cast<const uint4*>(p.norm.norm_w) + 2 * ks0;
+    for (int i = tid; i < p.T * nv; i += kRouteThreads) {
+      const int t = i / nv, v = i - t * nv;
+      uint4* xp = reinterpret_cast<uint4*>(xs + (size_t)t * L.pitch) + v;
+      *xp = norm_apply8(*xp, __ldg(rres + (size_t)t * (p.H / 8) + 2 * ks0 + v), __ldg(gam + v), norm_rinv_s[t]);
+    }
+    __syncthreads();
+  }
 
   // shared::cluster addresses of every owner's receive area and barrier
   const uint32_t recv_u = smem_u32(recv), bar_part_u = smem_u32(bar_part);
@@ -666,17 +711,24 @@ constexpr int kMmaMaxNtpw = kMaxExperts / 8 / kRouteWarps;  // 8-expert column b
 
 struct MmaRouteSmem {
   int erows;
-  size_t x_off[2], w_off[2], lg_off, total;
+  size_t stage, xo, wo, ro, go, lg_off, total;  // stage b of buffer "o" starts at b * stage + o
+  __host__ __device__ size_t x_off(int b) const { return b * stage + xo; }
+  __host__ __device__ size_t w_off(int b) const { return b * stage + wo; }
+  __host__ __device__ size_t r_off(int b) const { return b * stage + ro; }
+  __host__ __device__ size_t g_off(int b) const { return b * stage + go; }
 };
-__host__ __device__ inline MmaRouteSmem mma_route_smem(int E) {
+// norm: two more buffers per stage, the residual chunk [32][pitch] and the weight chunk [128]
+__host__ __device__ inline MmaRouteSmem mma_route_smem(int E, bool norm) {
   MmaRouteSmem L;
   L.erows = ((E + 7) / 8) * 8;
   const size_t xb = (size_t)kMmaTokens * kMmaPitch, wb = (size_t)L.erows * kMmaPitch;
-  L.x_off[0] = 0;
-  L.w_off[0] = xb;
-  L.x_off[1] = xb + wb;
-  L.w_off[1] = 2 * xb + wb;
-  L.lg_off = 2 * (xb + wb);
+  const size_t rb = norm ? xb : 0, gb = norm ? kMmaKChunk * 2 : 0;
+  L.stage = xb + wb + rb + gb;
+  L.xo = 0;
+  L.wo = xb;
+  L.ro = xb + wb;
+  L.go = xb + wb + rb;
+  L.lg_off = 2 * L.stage;
   L.total = L.lg_off + sizeof(float) * (size_t)kMmaTokens * L.erows;
   return L;
 }
@@ -695,10 +747,12 @@ __device__ __forceinline__ void cp_async_wait() {
 __global__ void __launch_bounds__(kRouteThreads) route_mma_kernel(RouteParams p) {
   extern __shared__ __align__(16) uint8_t rm_smem[];
   __shared__ int s_last;
+  __shared__ float s_rinv[kMmaTokens];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();  // the previous kernel may still write x or read this call's outputs
   pdl_launch_dependents();
-  const MmaRouteSmem L = mma_route_smem(p.E);
+  const bool norm = p.norm.norm_w != nullptr;
+  const MmaRouteSmem L = mma_route_smem(p.E, norm);
   const int t0 = blockIdx.x * kMmaTokens;
   const int nt = min(kMmaTokens, p.T - t0);
   const int nchunks = (p.H + kMmaKChunk - 1) / kMmaKChunk;
@@ -710,17 +764,38 @@ __global__ void __launch_bounds__(kRouteThreads) route_mma_kernel(RouteParams p)
     for (int i = tid; i < kMmaTokens * (kMmaKChunk / 8); i += kRouteThreads) {
       const int r = i / (kMmaKChunk / 8), sg = i - r * (kMmaKChunk / 8), k = k0 + sg * 8;
       const bool ok = r < nt && k < p.H;
-      cp_async16(smem0 + (uint32_t)(L.x_off[b] + r * kMmaPitch + sg * 16), ok ? p.x + (size_t)(t0 + r) * p.H + k : p.x,
+      cp_async16(smem0 + (uint32_t)(L.x_off(b) + r * kMmaPitch + sg * 16), ok ? p.x + (size_t)(t0 + r) * p.H + k : p.x,
                  ok ? 16u : 0u);
     }
     for (int i = tid; i < L.erows * (kMmaKChunk / 8); i += kRouteThreads) {
       const int r = i / (kMmaKChunk / 8), sg = i - r * (kMmaKChunk / 8), k = k0 + sg * 8;
       const bool ok = r < p.E && k < p.H;
-      cp_async16(smem0 + (uint32_t)(L.w_off[b] + r * kMmaPitch + sg * 16),
+      cp_async16(smem0 + (uint32_t)(L.w_off(b) + r * kMmaPitch + sg * 16),
                  ok ? p.w_router + (size_t)r * p.H + k : p.w_router, ok ? 16u : 0u);
+    }
+    if (norm) {
+      for (int i = tid; i < kMmaTokens * (kMmaKChunk / 8); i += kRouteThreads) {
+        const int r = i / (kMmaKChunk / 8), sg = i - r * (kMmaKChunk / 8), k = k0 + sg * 8;
+        const bool ok = r < nt && k < p.H;
+        cp_async16(smem0 + (uint32_t)(L.r_off(b) + r * kMmaPitch + sg * 16),
+                   ok ? p.norm.residual + (size_t)(t0 + r) * p.H + k : p.norm.residual, ok ? 16u : 0u);
+      }
+      for (int sg = tid; sg < kMmaKChunk / 8; sg += kRouteThreads) {
+        const bool ok = k0 + sg * 8 < p.H;
+        cp_async16(smem0 + (uint32_t)(L.g_off(b) + sg * 16), ok ? p.norm.norm_w + k0 + sg * 8 : p.norm.norm_w,
+                   ok ? 16u : 0u);
+      }
     }
     cp_async_commit();
   };
+  if (norm) {
+    // 1 / rms of the block's rows (the same range cut and order as every other kernel)
+    for (int r = warp; r < nt; r += kRouteWarps) {
+      const float ri = norm_row_rinv(p.x + (size_t)(t0 + r) * p.H, p.norm.residual + (size_t)(t0 + r) * p.H, p.H,
+                                     p.norm.eps);
+      if (lane == 0) s_rinv[r] = ri;
+    }
+  }
   // warp w owns 8-expert column blocks [w ntpw, (w + 1) ntpw) and both 16-token row blocks
   const int ntiles = L.erows / 8;
   const int ntpw = (ntiles + kRouteWarps - 1) / kRouteWarps;
@@ -740,7 +815,20 @@ __global__ void __launch_bounds__(kRouteThreads) route_mma_kernel(RouteParams p)
       cp_async_wait<0>();
     }
     __syncthreads();
-    const uint32_t xs = smem0 + (uint32_t)L.x_off[b], wsm = smem0 + (uint32_t)L.w_off[b];
+    if (norm) {
+      // x chunk -> y chunk in place
+      const int k0 = c * kMmaKChunk;
+      for (int i = tid; i < nt * (kMmaKChunk / 8); i += kRouteThreads) {
+        const int r = i / (kMmaKChunk / 8), sg = i - r * (kMmaKChunk / 8);
+        if (k0 + sg * 8 >= p.H) continue;
+        uint4* xp = reinterpret_cast<uint4*>(rm_smem + L.x_off(b) + r * kMmaPitch + sg * 16);
+        const uint4 rv = *reinterpret_cast<const uint4*>(rm_smem + L.r_off(b) + r * kMmaPitch + sg * 16);
+        const uint4 gv = *reinterpret_cast<const uint4*>(rm_smem + L.g_off(b) + sg * 16);
+        *xp = norm_apply8(*xp, rv, gv, s_rinv[r]);
+      }
+      __syncthreads();
+    }
+    const uint32_t xs = smem0 + (uint32_t)L.x_off(b), wsm = smem0 + (uint32_t)L.w_off(b);
 #pragma unroll
     for (int ks = 0; ks < kMmaKChunk / 16; ++ks) {
       uint32_t a0[4], a1[4];
@@ -841,7 +929,7 @@ __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t
 // the device can place one cluster of kClusterCtas CTAs with that much memory.
 static bool use_cluster_route(const RouteParams& p, size_t* smem_out) {
   if (p.from_logits || p.T > kClusterMaxTokens) return false;
-  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k);
+  const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k, p.norm.norm_w != nullptr);
   if (L.total > 200 * 1024) return false;
   static int state[64] = {};  // 0 unknown, 1 usable, -1 not
   int dev = 0;
@@ -870,7 +958,7 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
     return launch_pdl(route_cluster_kernel, dim3(kClusterCtas), dim3(kRouteThreads), csmem, stream, p);
   if (!p.from_logits) {
     // many tokens: tensor-core logits, 32 tokens per block
-    const MmaRouteSmem L = mma_route_smem(p.E);
+    const MmaRouteSmem L = mma_route_smem(p.E, p.norm.norm_w != nullptr);
     static int configured[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -89,6 +89,18 @@ def test_host_argument_checks_return_codes(lib):
     assert L.moe_route(fake, fake, None, T, H, E, k, fake, 8, fake, fake, fake, ws, None) == L.MOE_ERR_INVALID_ARG
     assert L.moe_forward_gated(fake, fake, None, fake, fake, T, H, I, E, k, 3, fake, ws, fake, None, None,
                                None) == L.MOE_ERR_INVALID_ARG
+    # the norm step: missing or misaligned residual / weight, bad eps, residual_out == out
+    def fnorm(res=fake, gam=fake, eps=1e-5, gating=0, rout=None, out=fake):
+        return L.moe_forward_norm(fake, res, gam, eps, fake, None, fake, fake, T, H, I, E, k, gating, fake, ws, out,
+                                  rout, None, None, None)
+    assert fnorm(res=None) == L.MOE_ERR_INVALID_ARG
+    assert fnorm(gam=fake + 2) == L.MOE_ERR_INVALID_ARG
+    assert fnorm(eps=-1.0) == L.MOE_ERR_INVALID_ARG
+    assert fnorm(eps=float("nan")) == L.MOE_ERR_INVALID_ARG
+    assert fnorm(eps=float("inf")) == L.MOE_ERR_INVALID_ARG
+    assert fnorm(gating=3) == L.MOE_ERR_INVALID_ARG
+    assert fnorm(rout=fake) == L.MOE_ERR_INVALID_ARG           # residual_out may not be out
+    assert fnorm(rout=fake + 8) == L.MOE_ERR_INVALID_ARG       # misaligned residual_out
     assert L.moe_build_tile_table(fake, T, k, E, 32, fake, fake, fake, fake, fake, fake, None) == \
         L.MOE_ERR_UNSUPPORTED_SHAPE                            # tile rows must be 16, 64 or 128
     assert L.moe_prepare_weights(fake, fake, E, 2 * I, H, 5, fake, 1 << 40, None) == L.MOE_ERR_UNSUPPORTED_SHAPE

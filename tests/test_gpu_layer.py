@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import oracle
-from synthetic import make_config, make_layer
+from synthetic import make_config, make_layer, make_norm_inputs
 from tests.gpu_helpers import TOL_MAX_ABS, TOL_REL_FROB, bf16_bits_to_f32, bf16_to_np, build_layer, errors, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -215,3 +215,35 @@ def test_consecutive_calls_with_new_routing(name):
         keep = oracle.topk_margin(ref["logits"], inp.k) > 1e-4
         rel, mx = errors(bf16_bits_to_f32(bf16_to_np(out))[keep], ref["out"][keep])
         assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)
+
+
+@pytest.mark.parametrize("name,T", [("tiny", None), ("gptoss20b_b1", None), ("gptoss20b_b64", None),
+                                    ("gptoss20b_b64", 200)])
+def test_layer_norm_residual(name, T):
+    """RMSNorm + residual in front of the layer: the router (cluster kernel for T <= 64,
+    many-token kernel above) and the encoder normalise the rows themselves; the
+    combine kernel writes the residual stream."""
+    import torch
+    inp = make_config(name, T=T)
+    r, g, eps = make_norm_inputs(inp.T, inp.H, seed=1)
+    layer = build_layer(inp)
+    x, rd, gd = to_dev(inp.x), to_dev(r), to_dev(g)
+    idx = torch.empty(inp.T, inp.k, dtype=torch.int32, device="cuda")
+    w = torch.empty(inp.T, inp.k, dtype=torch.float32, device="cuda")
+    res_out = torch.empty_like(x)
+    out = layer(x, topk_idx=idx, topk_w=w, residual=rd, norm_weight=gd, eps=eps, residual_out=res_out)
+    torch.cuda.synchronize()
+    assert layer.device_status(inp.T) == 0
+    ref = oracle.moe_layer_norm(inp, r, g, eps)
+    assert np.array_equal(bf16_to_np(res_out), ref["residual_out"])
+    got = bf16_bits_to_f32(bf16_to_np(out))
+    keep = oracle.topk_margin(ref["logits"], inp.k) > 1e-4
+    assert keep.mean() > 0.9
+    assert np.array_equal(idx.cpu().numpy()[keep], ref["idx"][keep])
+    rel, mx = errors(got[keep], ref["out"][keep])
+    assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)
+    # in place: the residual stream written over the residual input, same results
+    rd2 = rd.clone()
+    out2 = layer(x, residual=rd2, norm_weight=gd, eps=eps, residual_out=rd2)
+    torch.cuda.synchronize()
+    assert torch.equal(out2, out) and torch.equal(rd2, res_out)

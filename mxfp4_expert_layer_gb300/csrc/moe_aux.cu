@@ -34,6 +34,9 @@ __device__ __forceinline__ float quad_max(float v) {
 // them, or (scatter, in the layer's forward) the warp waits for routing and writes
 // its encoded values straight to the tile rows of the token's k assignments -- the
 // permute step without a launch of its own.
+// kNorm: the rows are y = RMSNorm(x + residual) (a separate instance: the norm's
+// loads need registers the plain encoding does not)
+template <bool kNorm>
 __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) {
   // the previous kernel may still write x or read this call's buffers, unless the
   // launch before this one already waited for it.  Waiting at the end, this launch
@@ -60,12 +63,11 @@ __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) 
   const int nvec = p.H / 8;
   float f[8];
   // with the norm step, the row's 1 / rms (the same bits the router computes)
-  const float rinv = p.norm.norm_w ? norm_row_rinv(p.x + (size_t)t * p.H, p.norm.residual + (size_t)t * p.H, p.H,
-                                                   p.norm.eps)
-                                   : 0.f;
+  const float rinv =
+      kNorm ? norm_row_rinv(p.x + (size_t)t * p.H, p.norm.residual + (size_t)t * p.H, p.H, p.norm.eps) : 0.f;
   if (v < nvec) {
     uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + v);
-    if (p.norm.norm_w)
+    if (kNorm)
       raw = norm_apply8(raw, __ldg(reinterpret_cast<const uint4*>(p.norm.residual + (size_t)t * p.H) + v),
                         __ldg(reinterpret_cast<const uint4*>(p.norm.norm_w) + v), rinv);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -146,7 +148,9 @@ cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream) {
   const int nvec_pad = ((p.H + 63) / 64) * 8;
   const long long warps = (long long)p.T * ((nvec_pad + 31) / 32);
   const int blocks = (int)((warps * 32 + kAuxThreads - 1) / kAuxThreads);
-  return launch_pdl(encode_x_kernel, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
+  if (p.norm.norm_w)
+    return launch_pdl(encode_x_kernel<true>, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
+  return launch_pdl(encode_x_kernel<false>, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
 }
 
 // The permute step: every (tile row, K group) copies its token's four encoded

@@ -4,6 +4,7 @@
 #include <cuda.h>
 
 #include "moe_common.cuh"
+#include "moe_norm.cuh"
 
 namespace moe {
 
@@ -34,6 +35,13 @@ inline int gating_from_flags(int flags) {
   if (all && sig) return -1;
   return all ? kGatingSoftmaxAll : sig ? kGatingSigmoid : kGatingSoftmaxTopk;
 }
+
+// Optional RMSNorm + residual in front of the layer (norm_w null: x is the input).
+struct NormArgs {
+  const uint16_t* residual;  // bf16 [T, H]
+  const uint16_t* norm_w;    // bf16 [H]
+  float eps;
+};
 
 struct RouteParams {
   const uint16_t* x;        // bf16 [T, H]

@@ -457,7 +457,7 @@ constexpr int kMmaIlp = 4;  // 8-expert column blocks per warp pass (one A fragm
 struct ClusterRouteSmem {
   int mrows, erows, pitch;        // staged x rows (multiple of 16), router rows (multiple of 8), row bytes
   int nitems, nsplit;
-  size_t x_off, w_off, split_off, recv_off, lg_off, bias_off, idx_off, norm_off, bar_off, total;
+  size_t x_off, w_off, rs_off, split_off, recv_off, lg_off, bias_off, idx_off, norm_off, bar_off, total;
 };
 static_assert(kClusterCtas == kNormSlices, "a cluster CTA sums one range of the norm's row cut");
 __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int E, int k, bool norm) {
@@ -473,7 +473,8 @@ __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int
   while (L.nsplit * 2 * L.nitems <= kRouteWarps) L.nsplit *= 2;
   L.x_off = 0;
   L.w_off = L.x_off + (size_t)L.mrows * L.pitch;
-  L.split_off = L.w_off + (size_t)L.erows * L.pitch;
+  L.rs_off = L.w_off + (size_t)L.erows * L.pitch;  // norm step: residual slices, like x
+  L.split_off = L.rs_off + (norm ? (size_t)L.mrows * L.pitch : 0);
   const size_t split_bytes = L.nsplit > 1 ? sizeof(float) * (size_t)L.nsplit * L.mrows * L.erows : 0;
   L.recv_off = L.split_off + split_bytes;  // [kClusterCtas][kTokensPerGroup][erows] partials
   L.lg_off = L.recv_off + sizeof(float) * (size_t)kClusterCtas * kTokensPerGroup * L.erows;
@@ -499,6 +500,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k, norm);
   uint8_t* xs = rc_smem + L.x_off;
   uint8_t* wsm = rc_smem + L.w_off;
+  uint8_t* rs = rc_smem + L.rs_off;
   float* split = reinterpret_cast<float*>(rc_smem + L.split_off);  // [nsplit][mrows][erows]
   float* recv = reinterpret_cast<float*>(rc_smem + L.recv_off);    // [src rank][token - 8*rank][erows]
   float* lg = reinterpret_cast<float*>(rc_smem + L.lg_off);        // [8][erows]
@@ -529,7 +531,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     if (norm) mbar_arrive_expect_tx(bar_norm, (uint32_t)(kClusterCtas * p.T * sizeof(float)));
     if (n_own > 0) mbar_arrive_expect_tx(bar_part, (uint32_t)(kClusterCtas * n_own * L.erows * sizeof(float)));
     if (builds) mbar_arrive_expect_tx(bar_idx, (uint32_t)(p.T * p.k * sizeof(int32_t)));
-    if (slice_bytes > 0) mbar_arrive_expect_tx(bar_stage, slice_bytes * (uint32_t)(p.T + p.E));
+    if (slice_bytes > 0) mbar_arrive_expect_tx(bar_stage, slice_bytes * (uint32_t)(p.T + p.E + (norm ? p.T : 0)));
   }
   __syncthreads();
   cluster_arrive_release();  // this CTA's barriers are initialised
@@ -544,14 +546,9 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   pdl_wait();
   pdl_launch_dependents();
   if (slice_bytes > 0) {
-    for (int r = tid; r < p.T; r += kRouteThreads)
+    for (int r = tid; r < p.T; r += kRouteThreads) {
       bulk_load(xs + (size_t)r * L.pitch, p.x + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
-  }
-  if (norm) {
-    // norm step: this CTA's range of every row (the same range cut every kernel uses)
-    for (int t = warp; t < p.T; t += kRouteWarps) {
-      const float ssq = norm_range_ssq(p.x + (size_t)t * p.H, p.norm.residual + (size_t)t * p.H, 2 * ks0, 2 * ks1);
-      if (lane == 0) norm_own[t] = ssq;
+      if (norm) bulk_load(rs + (size_t)r * L.pitch, p.norm.residual + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
     }
   }
   // rows the copies never touch: x rows past T, router rows past E
@@ -564,7 +561,16 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
   }
   if (slice_bytes > 0 && !mbar_wait_bounded(bar_stage, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
-  __syncthreads();  // zero rows and the bias written by other threads
+  if (norm) {
+    // norm step: this CTA's range of every row (the range cut every kernel uses)
+    for (int t = warp; t < p.T; t += kRouteWarps) {
+      const float ssq = norm_range_ssq(reinterpret_cast<const uint16_t*>(xs + (size_t)t * L.pitch),
+                                       reinterpret_cast<const uint16_t*>(rs + (size_t)t * L.pitch), 0,
+                                       2 * (ks1 - ks0));
+      if (lane == 0) norm_own[t] = ssq;
+    }
+  }
+  __syncthreads();  // zero rows, the bias and the range sums written by other threads
   cluster_wait_acquire();  // every peer's barriers are initialised: pushes may start
   if (norm) {
     // every CTA gets every range sum, adds them in range order (the same bits in
@@ -584,12 +590,12 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     }
     __syncthreads();
     const int nv = 2 * (ks1 - ks0);
-    const uint4* rres = reinterpret_cast<const uint4*>(p.norm.residual);
     const uint4* gam = reinterpret_cast<const uint4*>(p.norm.norm_w) + 2 * ks0;
     for (int i = tid; i < p.T * nv; i += kRouteThreads) {
       const int t = i / nv, v = i - t * nv;
       uint4* xp = reinterpret_cast<uint4*>(xs + (size_t)t * L.pitch) + v;
-      *xp = norm_apply8(*xp, __ldg(rres + (size_t)t * (p.H / 8) + 2 * ks0 + v), __ldg(gam + v), norm_rinv_s[t]);
+      *xp = norm_apply8(*xp, reinterpret_cast<const uint4*>(rs + (size_t)t * L.pitch)[v], __ldg(gam + v),
+                        norm_rinv_s[t]);
     }
     __syncthreads();
   }

@@ -34,10 +34,13 @@ __device__ __forceinline__ float quad_max(float v) {
 // them, or (scatter, in the layer's forward) the warp waits for routing and writes
 // its encoded values straight to the tile rows of the token's k assignments -- the
 // permute step without a launch of its own.
-// kNorm: the rows are y = RMSNorm(x + residual) (a separate instance: the norm's
-// loads need registers the plain encoding does not)
+// kNorm: the rows are y = RMSNorm(x + residual).  That instance runs one block per
+// token (a warp per 256-value chunk, at least kNormSlices warps): warp q < kNormSlices
+// sums range q of the row, and every warp forms the row's 1 / rms from the eight
+// sums (the same bits the router computes).
+constexpr int kEncodeNormMaxThreads = 1024;
 template <bool kNorm>
-__global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) {
+__global__ void __launch_bounds__(kNorm ? kEncodeNormMaxThreads : kAuxThreads) encode_x_kernel(EncodeXParams p) {
   // the previous kernel may still write x or read this call's buffers, unless the
   // launch before this one already waited for it.  Waiting at the end, this launch
   // also signals its dependents only after that wait: the GEMM after it reads the
@@ -47,24 +50,39 @@ __global__ void __launch_bounds__(kAuxThreads) encode_x_kernel(EncodeXParams p) 
     ptx::pdl_launch_dependents();
   }
   const int lane = threadIdx.x & 31;
-  const long long gw = ((long long)blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
   const int nvec_pad = ((p.H + 63) / 64) * 8;  // 8-value vectors per row, padded to 64 values
   const int nchunks = (nvec_pad + 31) / 32;
-  const int t = (int)(gw / nchunks);
-  if (t >= p.T) {
+  int t, chunk;
+  float rinv = 0.f;
+  if constexpr (kNorm) {
+    __shared__ float s_part[kNormSlices];
+    t = blockIdx.x;
+    chunk = threadIdx.x >> 5;
+    if (chunk < kNormSlices) {
+      const float ssq = norm_range_ssq(p.x + (size_t)t * p.H, p.norm.residual + (size_t)t * p.H,
+                                       norm_slice_vec(p.H, chunk), norm_slice_vec(p.H, chunk + 1));
+      if (lane == 0) s_part[chunk] = ssq;
+    }
+    __syncthreads();
+    float part[kNormSlices];
+#pragma unroll
+    for (int q = 0; q < kNormSlices; ++q) part[q] = s_part[q];
+    rinv = norm_rinv(part, p.H, p.norm.eps);
+  } else {
+    const long long gw = ((long long)blockIdx.x * kAuxThreads + threadIdx.x) >> 5;
+    t = (int)(gw / nchunks);
+    chunk = (int)(gw - (long long)t * nchunks);
+  }
+  if (t >= p.T || chunk >= nchunks) {
     if (p.wait_at_end) {
       ptx::pdl_wait();
       ptx::pdl_launch_dependents();
     }
     return;
   }
-  const int chunk = (int)(gw - (long long)t * nchunks);
   const int v = chunk * 32 + lane;
   const int nvec = p.H / 8;
   float f[8];
-  // with the norm step, the row's 1 / rms (the same bits the router computes)
-  const float rinv =
-      kNorm ? norm_row_rinv(p.x + (size_t)t * p.H, p.norm.residual + (size_t)t * p.H, p.H, p.norm.eps) : 0.f;
   if (v < nvec) {
     uint4 raw = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + v);
     if (kNorm)
@@ -148,8 +166,11 @@ cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream) {
   const int nvec_pad = ((p.H + 63) / 64) * 8;
   const long long warps = (long long)p.T * ((nvec_pad + 31) / 32);
   const int blocks = (int)((warps * 32 + kAuxThreads - 1) / kAuxThreads);
-  if (p.norm.norm_w)
-    return launch_pdl(encode_x_kernel<true>, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
+  if (p.norm.norm_w) {
+    const int nw = (nvec_pad + 31) / 32 > kNormSlices ? (nvec_pad + 31) / 32 : kNormSlices;
+    if (nw * 32 > kEncodeNormMaxThreads) return cudaErrorInvalidValue;
+    return launch_pdl(encode_x_kernel<true>, dim3(p.T > 0 ? p.T : 1), dim3(nw * 32), 0, stream, p);
+  }
   return launch_pdl(encode_x_kernel<false>, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
 }
 

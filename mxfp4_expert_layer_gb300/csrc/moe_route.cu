@@ -454,9 +454,12 @@ constexpr int kMmaIlp = 4;  // 8-expert column blocks per warp pass (one A fragm
 // item is (16-token row block, kMmaIlp column blocks); when there are fewer items
 // than warps, each item's K range is split over nsplit warps whose partial sums
 // meet in the split area.
+constexpr size_t kClusterSmemCap = 200 * 1024;  // dynamic shared memory of the cluster kernel
+
 struct ClusterRouteSmem {
   int mrows, erows, pitch;        // staged x rows (multiple of 16), router rows (multiple of 8), row bytes
   int nitems, nsplit;
+  int rs_staged;                  // norm step: residual slices staged beside x (else read from global)
   size_t x_off, w_off, rs_off, split_off, recv_off, lg_off, bias_off, idx_off, norm_off, bar_off, total;
 };
 static_assert(kClusterCtas == kNormSlices, "a cluster CTA sums one range of the norm's row cut");
@@ -474,7 +477,8 @@ __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int
   L.x_off = 0;
   L.w_off = L.x_off + (size_t)L.mrows * L.pitch;
   L.rs_off = L.w_off + (size_t)L.erows * L.pitch;  // norm step: residual slices, like x
-  L.split_off = L.rs_off + (norm ? (size_t)L.mrows * L.pitch : 0);
+  L.rs_staged = norm ? 1 : 0;
+  L.split_off = L.rs_off + (L.rs_staged ? (size_t)L.mrows * L.pitch : 0);
   const size_t split_bytes = L.nsplit > 1 ? sizeof(float) * (size_t)L.nsplit * L.mrows * L.erows : 0;
   L.recv_off = L.split_off + split_bytes;  // [kClusterCtas][kTokensPerGroup][erows] partials
   L.lg_off = L.recv_off + sizeof(float) * (size_t)kClusterCtas * kTokensPerGroup * L.erows;
@@ -485,6 +489,19 @@ __host__ __device__ inline ClusterRouteSmem cluster_route_smem(int T, int H, int
   const size_t norm_bytes = norm ? sizeof(float) * (size_t)(kClusterCtas + 2) * L.mrows : 0;
   L.bar_off = L.norm_off + norm_bytes;
   L.total = L.bar_off + 32;
+  if (L.rs_staged && L.total > kClusterSmemCap) {
+    // no room for the residual slices: the kernel reads them from global memory
+    const size_t rs_bytes = (size_t)L.mrows * L.pitch;
+    L.rs_staged = 0;
+    L.split_off -= rs_bytes;
+    L.recv_off -= rs_bytes;
+    L.lg_off -= rs_bytes;
+    L.bias_off -= rs_bytes;
+    L.idx_off -= rs_bytes;
+    L.norm_off -= rs_bytes;
+    L.bar_off -= rs_bytes;
+    L.total -= rs_bytes;
+  }
   return L;
 }
 
@@ -531,7 +548,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     if (norm) mbar_arrive_expect_tx(bar_norm, (uint32_t)(kClusterCtas * p.T * sizeof(float)));
     if (n_own > 0) mbar_arrive_expect_tx(bar_part, (uint32_t)(kClusterCtas * n_own * L.erows * sizeof(float)));
     if (builds) mbar_arrive_expect_tx(bar_idx, (uint32_t)(p.T * p.k * sizeof(int32_t)));
-    if (slice_bytes > 0) mbar_arrive_expect_tx(bar_stage, slice_bytes * (uint32_t)(p.T + p.E + (norm ? p.T : 0)));
+    if (slice_bytes > 0)
+      mbar_arrive_expect_tx(bar_stage, slice_bytes * (uint32_t)(p.T + p.E + (L.rs_staged ? p.T : 0)));
   }
   __syncthreads();
   cluster_arrive_release();  // this CTA's barriers are initialised
@@ -548,7 +566,8 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
   if (slice_bytes > 0) {
     for (int r = tid; r < p.T; r += kRouteThreads) {
       bulk_load(xs + (size_t)r * L.pitch, p.x + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
-      if (norm) bulk_load(rs + (size_t)r * L.pitch, p.norm.residual + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
+      if (L.rs_staged)
+        bulk_load(rs + (size_t)r * L.pitch, p.norm.residual + (size_t)r * p.H + ks0 * 16, slice_bytes, bar_stage);
     }
   }
   // rows the copies never touch: x rows past T, router rows past E
@@ -561,11 +580,15 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     *reinterpret_cast<uint4*>(wsm + (size_t)r * L.pitch + c * 16) = make_uint4(0, 0, 0, 0);
   }
   if (slice_bytes > 0 && !mbar_wait_bounded(bar_stage, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
+  // norm step: this CTA's slice of residual row t (shared or global memory)
+  auto res_slice = [&](int t) -> const uint16_t* {
+    return L.rs_staged ? reinterpret_cast<const uint16_t*>(rs + (size_t)t * L.pitch)
+                       : p.norm.residual + (size_t)t * p.H + ks0 * 16;
+  };
   if (norm) {
-    // norm step: this CTA's range of every row (the range cut every kernel uses)
+    // this CTA's range of every row (the range cut every kernel uses)
     for (int t = warp; t < p.T; t += kRouteWarps) {
-      const float ssq = norm_range_ssq(reinterpret_cast<const uint16_t*>(xs + (size_t)t * L.pitch),
-                                       reinterpret_cast<const uint16_t*>(rs + (size_t)t * L.pitch), 0,
+      const float ssq = norm_range_ssq(reinterpret_cast<const uint16_t*>(xs + (size_t)t * L.pitch), res_slice(t), 0,
                                        2 * (ks1 - ks0));
       if (lane == 0) norm_own[t] = ssq;
     }
@@ -594,8 +617,7 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     for (int i = tid; i < p.T * nv; i += kRouteThreads) {
       const int t = i / nv, v = i - t * nv;
       uint4* xp = reinterpret_cast<uint4*>(xs + (size_t)t * L.pitch) + v;
-      *xp = norm_apply8(*xp, reinterpret_cast<const uint4*>(rs + (size_t)t * L.pitch)[v], __ldg(gam + v),
-                        norm_rinv_s[t]);
+      *xp = norm_apply8(*xp, reinterpret_cast<const uint4*>(res_slice(t))[v], __ldg(gam + v), norm_rinv_s[t]);
     }
     __syncthreads();
   }
@@ -936,18 +958,18 @@ __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t
 static bool use_cluster_route(const RouteParams& p, size_t* smem_out) {
   if (p.from_logits || p.T > kClusterMaxTokens) return false;
   const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k, p.norm.norm_w != nullptr);
-  if (L.total > 200 * 1024) return false;
+  if (L.total > kClusterSmemCap) return false;
   static int state[64] = {};  // 0 unknown, 1 usable, -1 not
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
   if (state[dev] == 0) {
     state[dev] = -1;
-    if (cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024) ==
+    if (cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterSmemCap) ==
         cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(kClusterCtas);
       cfg.blockDim = dim3(kRouteThreads);
-      cfg.dynamicSmemBytes = 200 * 1024;
+      cfg.dynamicSmemBytes = kClusterSmemCap;
       int clusters = 0;
       if (cudaOccupancyMaxActiveClusters(&clusters, route_cluster_kernel, &cfg) == cudaSuccess && clusters > 0)
         state[dev] = 1;

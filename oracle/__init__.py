@@ -17,8 +17,11 @@ from .moe_oracle import (  # noqa: F401
     decode_e8m0,
     decode_mxfp4,
     expert_hidden,
+    expert_hidden_dense,
     expert_output,
+    expert_output_dense,
     moe_layer,
+    moe_layer_dense,
     moe_layer_norm,
     rmsnorm_residual,
     router_logits,

@@ -220,6 +220,36 @@ def expert_output(h_rows: np.ndarray, dn_codes_e, dn_scales_e, dtype=np.float32)
     return (np.asarray(h_rows, dtype=dtype) @ w.T).astype(dtype)
 
 
+def expert_hidden_dense(x_rows: np.ndarray, w_gateup_e_bits, I: int, dtype=np.float32):
+    """Gate/up of one expert with bf16 weights (gate rows [0, I), up rows [I, 2I)):
+    h = silu(x W_gate^T) * (x W_up^T); returns [n, I]."""
+    w = bf16_to_f32(w_gateup_e_bits).astype(dtype)
+    x_rows = np.asarray(x_rows, dtype=dtype)
+    g = x_rows @ w[:I].T
+    u = x_rows @ w[I:2 * I].T
+    return (silu(g) * u).astype(dtype)
+
+
+def expert_output_dense(h_rows: np.ndarray, w_down_e_bits, dtype=np.float32):
+    """Down projection of one expert with bf16 weights: y = h W_down^T; [n, H]."""
+    w = bf16_to_f32(w_down_e_bits).astype(dtype)
+    return (np.asarray(h_rows, dtype=dtype) @ w.T).astype(dtype)
+
+
+def moe_layer_dense(inp, dtype=np.float32, tokens=None, gating=None):
+    """The same layer with bf16 expert weights (no MX scales): "triton-kernels"
+    README, "Quick Start", "Fused MoE Dispatch (Mixtral / DeepSeek-V3 / Qwen2-MoE
+    style)" (router -> permute -> fused expert FFN -> unpermute, gate/up/down weights
+    [E, F, H] / [E, H, F], softmax gating over the top-k) and "MoE Dispatch
+    Results" (Mixtral-8x7B: 8 experts, top-2, hidden 4096, ffn 14336).  Routing,
+    gating and the combine are those of ``moe_layer``; ``inp`` carries ``w_gateup``
+    (bf16 bits [E, 2I, H], gate rows then up rows) and ``w_down`` ([E, H, I])."""
+    return moe_layer(inp, dtype=dtype, tokens=tokens,
+                     gating=GATING_SOFTMAX_TOPK if gating is None else gating,
+                     _experts=(lambda e, x: expert_hidden_dense(x, inp.w_gateup[e], inp.I, dtype),
+                               lambda e, h: expert_output_dense(h, inp.w_down[e], dtype)))
+
+
 def bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round to the nearest bf16 (ties to even) and return the bit patterns."""
     return (bf16_round(a).view(np.uint32) >> 16).astype(np.uint16)
@@ -264,7 +294,7 @@ def moe_layer_norm(inp, residual_bits: np.ndarray, gamma_bits: np.ndarray, eps: 
 
 
 def moe_layer(inp, dtype=np.float32, tokens=None, logits=None, return_hidden=False,
-              gating=GATING_SOFTMAX_TOPK):
+              gating=GATING_SOFTMAX_TOPK, _experts=None):
     """The whole layer on the tokens ``tokens`` (default: all).
 
     Router -> top-k + gating weights -> per expert: gate/up + SwiGLU, down -> per token
@@ -285,10 +315,13 @@ def moe_layer(inp, dtype=np.float32, tokens=None, logits=None, return_hidden=Fal
     n = tok.size
     y = np.zeros((n, k, H), dtype=dtype)
     h_all = np.zeros((n, k, I), dtype=dtype) if return_hidden else None
+    if _experts is None:  # MXFP4 experts
+        _experts = (lambda e, xr: expert_hidden(xr, inp.gu_codes[e], inp.gu_scales[e], I, dtype),
+                    lambda e, hr: expert_output(hr, inp.dn_codes[e], inp.dn_scales[e], dtype))
     for e in np.unique(idx):
         rows, slots = np.nonzero(idx == e)
-        h = expert_hidden(x_all[rows], inp.gu_codes[e], inp.gu_scales[e], I, dtype)
-        y[rows, slots] = expert_output(h, inp.dn_codes[e], inp.dn_scales[e], dtype)
+        h = _experts[0](e, x_all[rows])
+        y[rows, slots] = _experts[1](e, h)
         if return_hidden:
             h_all[rows, slots] = h
     acc = np.zeros((n, H), dtype=dtype)

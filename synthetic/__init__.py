@@ -8,11 +8,15 @@ can be fed from it without sharing any computation.
 
 from .gen import (  # noqa: F401
     CONFIGS,
+    DENSE_CONFIGS,
+    DenseLayerInputs,
     LayerInputs,
     bf16_bits_from_f32,
     bf16_bits_to_f32,
     make_layer,
     make_config,
+    make_dense_config,
+    make_dense_layer,
     make_norm_inputs,
     random_logits,
     random_topk_idx,

@@ -153,6 +153,57 @@ def make_norm_inputs(T: int, H: int, seed: int = 0):
     return residual, gamma, 1e-5
 
 
+@dataclass
+class DenseLayerInputs:
+    """The layer with bf16 expert weights: w_gateup [E, 2I, H] (gate rows, then up
+    rows), w_down [E, H, I], bf16 bit patterns."""
+    name: str
+    T: int
+    H: int
+    I: int
+    E: int
+    k: int
+    x: np.ndarray
+    w_router: np.ndarray
+    w_gateup: np.ndarray
+    w_down: np.ndarray
+    router_bias: Optional[np.ndarray] = None
+    meta: dict = field(default_factory=dict)
+
+
+def make_dense_layer(T, H, I, E, k, seed=0, w_std=0.02, name="custom_dense") -> DenseLayerInputs:
+    """x ~ N(0, 1); router weight ~ N(0, 0.02^2); expert weights ~ N(0, w_std^2), drawn
+    one expert at a time; all rounded to bf16."""
+    rng = np.random.Generator(np.random.PCG64(seed + 104729))
+    x = bf16_bits_from_f32(rng.standard_normal((T, H), dtype=np.float32))
+    w_router = bf16_bits_from_f32(0.02 * rng.standard_normal((E, H), dtype=np.float32))
+    w_gateup = np.empty((E, 2 * I, H), np.uint16)
+    w_down = np.empty((E, H, I), np.uint16)
+    for e in range(E):
+        w_gateup[e] = bf16_bits_from_f32(w_std * rng.standard_normal((2 * I, H), dtype=np.float32))
+        w_down[e] = bf16_bits_from_f32(w_std * rng.standard_normal((H, I), dtype=np.float32))
+    return DenseLayerInputs(name, T, H, I, E, k, x, w_router, w_gateup, w_down,
+                            meta={"seed": seed, "w_std": w_std})
+
+
+# bf16-weight workloads: Mixtral-8x7B expert shapes at the token counts of the
+# fused-MoE dispatch table, and a small case for quick parity
+DENSE_CONFIGS = {
+    "dense_tiny": dict(T=8, H=256, I=384, E=4, k=2),
+    "mixtral_t32": dict(T=32, H=4096, I=14336, E=8, k=2),
+    "mixtral_t128": dict(T=128, H=4096, I=14336, E=8, k=2),
+    "mixtral_t512": dict(T=512, H=4096, I=14336, E=8, k=2),
+    "mixtral_t2048": dict(T=2048, H=4096, I=14336, E=8, k=2),
+}
+
+
+def make_dense_config(name: str, seed: int = 0, T: Optional[int] = None) -> DenseLayerInputs:
+    c = dict(DENSE_CONFIGS[name])
+    if T is not None:
+        c["T"] = T
+    return make_dense_layer(seed=seed, name=name, **c)
+
+
 def random_logits(T: int, E: int, seed: int = 0, n_ties: int = 0) -> np.ndarray:
     """Router logits drawn N(0, 1) in float32.  ``n_ties`` tokens get an exact tie
     planted between two experts so tie-breaking is exercised."""

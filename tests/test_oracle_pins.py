@@ -244,3 +244,42 @@ def test_layer_norm_is_scale_free_and_routes_on_the_normalised_rows():
     # the router sees y: its logits are y @ W_r^T
     lg = _f(a["x_norm"]).astype(np.float64) @ _f(inp.w_router).astype(np.float64).T
     assert np.allclose(a["logits"], lg, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float64])
+def test_dense_layer_equals_mxfp4_layer_on_exactly_representable_weights(dtype):
+    # E2M1 values times a power of two have at most two significant bits, so the
+    # decoded MXFP4 weights are exact in bf16: the bf16-weight layer on those weights
+    # must reproduce the (separately pinned) MXFP4 layer bit for bit
+    from synthetic import DenseLayerInputs
+    inp = make_config("tiny")
+    wgu = np.stack([oracle.decode_mxfp4(inp.gu_codes[e], inp.gu_scales[e]) for e in range(inp.E)])
+    wd = np.stack([oracle.decode_mxfp4(inp.dn_codes[e], inp.dn_scales[e]) for e in range(inp.E)])
+    assert np.array_equal(oracle.bf16_round(wgu), wgu) and np.array_equal(oracle.bf16_round(wd), wd)
+    dense = DenseLayerInputs("tiny_dense", inp.T, inp.H, inp.I, inp.E, inp.k, inp.x, inp.w_router,
+                             oracle.bf16_bits(wgu), oracle.bf16_bits(wd))
+    a = oracle.moe_layer(inp, dtype=dtype)
+    b = oracle.moe_layer_dense(dense, dtype=dtype)
+    for key in ("idx", "w", "y", "out"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_dense_layer_against_python_loops():
+    from synthetic import make_dense_layer
+    inp = make_dense_layer(T=3, H=8, I=8, E=2, k=1, seed=4, w_std=0.5)
+    res = oracle.moe_layer_dense(inp, dtype=np.float64)
+    x = oracle.bf16_to_f32(inp.x).astype(np.float64)
+    wr = oracle.bf16_to_f32(inp.w_router).astype(np.float64)
+    wgu = oracle.bf16_to_f32(inp.w_gateup).astype(np.float64)
+    wd = oracle.bf16_to_f32(inp.w_down).astype(np.float64)
+    for t in range(inp.T):
+        logits = [sum(x[t, i] * wr[e, i] for i in range(inp.H)) for e in range(inp.E)]
+        e = max(range(inp.E), key=lambda q: (logits[q], -q))
+        h = []
+        for f in range(inp.I):
+            g = sum(x[t, i] * wgu[e, f, i] for i in range(inp.H))
+            u = sum(x[t, i] * wgu[e, inp.I + f, i] for i in range(inp.H))
+            h.append(g / (1.0 + np.exp(-g)) * u)
+        y = [sum(h[f] * wd[e, o, f] for f in range(inp.I)) for o in range(inp.H)]
+        assert res["idx"][t, 0] == e
+        assert np.allclose(res["out_unrounded"][t], y, rtol=1e-12, atol=1e-12)

@@ -217,6 +217,36 @@ int moe_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t
                      uint16_t* out, uint16_t* residual_out, int32_t* topk_idx_out, float* topk_w_out,
                      moe_stream_t stream);
 
+/* moe_forward_bf16: the same layer with bf16 expert weights instead of MXFP4.
+ * This is the "Fused MoE Dispatch" workload of the "triton-kernels" README
+ * ("Quick Start"; "MoE Dispatch Results": Mixtral-8x7B, 8 experts, top-2,
+ * hidden 4096, ffn 14336): router -> top-k softmax gating -> permute -> gate/up +
+ * SwiGLU -> down -> weighted combine + unpermute.
+ * Launches:
+ *   - routing: as moe_forward;
+ *   - permute: bf16 rows of x into tile order;
+ *   - gate/up and down: the grouped tcgen05 GEMMs with kind::f16 (bf16 x bf16,
+ *     f32 accumulate); h is rounded to bf16 between them;
+ *   - combine: as moe_forward.
+ * Arguments:
+ *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL;
+ *   w_gateup bf16 [E, 2I, H], gate rows [0, I) then up rows [I, 2I);
+ *   w_down bf16 [E, H, I].
+ *   Both weight tensors are used as stored (no preparation step); all pointers are
+ *   16-byte aligned.
+ *   workspace: moe_workspace_bytes(T, H, I, E, k) bytes, 256-byte aligned.
+ *   out bf16 [T, H].
+ *   topk_idx_out / topk_w_out: as moe_forward.
+ * Errors:
+ *   - MOE_ERR_UNSUPPORTED_SHAPE as moe_forward, and also unless H and I are
+ *     multiples of 64;
+ *   - MOE_ERR_INVALID_ARG for NULL or misaligned pointers;
+ *   - MOE_ERR_WORKSPACE_TOO_SMALL.                                                  */
+int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const uint16_t* w_gateup,
+                     const uint16_t* w_down, int T, int H, int I, int E, int k, void* workspace,
+                     size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                     moe_stream_t stream);
+
 /* moe_forward: the whole layer, out = MoE(x), on one stream with no host sync.
  *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL;
  *   w_gateup / w_down: prepared weights; out bf16 [T, H];

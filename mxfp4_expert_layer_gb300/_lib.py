@@ -46,6 +46,7 @@ SIGNATURES = {
     "moe_forward_gated": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P]),
     "moe_forward_norm": (_I, [_P, _P, _P, ctypes.c_float, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _S, _P, _P,
                               _P, _P, _P]),
+    "moe_forward_bf16": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P]),
     "moe_forward_timed": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P, _P]),
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I]),
     "moe_get_device_status": (_I, [_P, _S, ctypes.POINTER(_I), _P]),
@@ -105,6 +106,7 @@ moe_hidden_dequant = _call("moe_hidden_dequant")
 moe_forward = _call("moe_forward")
 moe_forward_gated = _call("moe_forward_gated")
 moe_forward_norm = _call("moe_forward_norm")
+moe_forward_bf16 = _call("moe_forward_bf16")
 moe_forward_timed = _call("moe_forward_timed")
 moe_forward_launches = _call("moe_forward_launches")
 moe_get_device_status = _call("moe_get_device_status")

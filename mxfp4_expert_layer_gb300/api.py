@@ -172,3 +172,47 @@ class MoELayer:
         st = ctypes.c_int(0)
         L.moe_get_device_status(ws.data_ptr(), ws.numel(), ctypes.byref(st), _stream())
         return st.value
+
+
+class MoELayerBF16:
+    """The same layer with bf16 expert weights (moe_forward_bf16): w_gateup [E, 2I, H]
+    (gate rows, then up rows) and w_down [E, H, I], used as stored."""
+
+    def __init__(self, w_router: torch.Tensor, w_gateup: torch.Tensor, w_down: torch.Tensor, k: int,
+                 router_bias: Optional[torch.Tensor] = None):
+        E, two_i, H = w_gateup.shape
+        self.w_router, self.w_gateup, self.w_down = w_router, w_gateup.contiguous(), w_down.contiguous()
+        self.router_bias = router_bias
+        self.H, self.I, self.E, self.k = H, two_i // 2, E, k
+        self._ws = {}
+
+    def workspace(self, T: int) -> torch.Tensor:
+        ws = self._ws.get(T)
+        if ws is None:
+            ws = workspace(T, self.H, self.I, self.E, self.k, self.w_router.device)
+            self._ws[T] = ws
+        return ws
+
+    def forward(self, x: torch.Tensor, out: Optional[torch.Tensor] = None, topk_idx=None, topk_w=None,
+                ws: Optional[torch.Tensor] = None) -> torch.Tensor:
+        _need_cuda(x)
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty(T, self.H, dtype=torch.bfloat16, device=x.device)
+        if ws is None:
+            ws = self.workspace(T)
+        L.check("moe_forward_bf16", L.moe_forward_bf16(
+            x.data_ptr(), self.w_router.data_ptr(), _ptr(self.router_bias), self.w_gateup.data_ptr(),
+            self.w_down.data_ptr(), T, self.H, self.I, self.E, self.k, ws.data_ptr(), ws.numel(), out.data_ptr(),
+            _ptr(topk_idx), _ptr(topk_w), _stream()))
+        return out
+
+    __call__ = forward
+
+    def device_status(self, T: int) -> int:
+        import ctypes
+        ws = self.workspace(T)
+        st = ctypes.c_int(0)
+        L.moe_get_device_status(ws.data_ptr(), ws.numel(), ctypes.byref(st), _stream())
+        return st.value
+

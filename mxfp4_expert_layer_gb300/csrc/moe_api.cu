@@ -124,6 +124,18 @@ bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P,
                   kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// bf16 weights of one family, row major [E * groups][rows per group][K], as a 3-D byte
+// map {2K bytes, rows per group, E * groups}: one box = 128 rows x 128 bytes (64
+// values, one pipeline stage) with the 128-byte swizzle; parts of a box past the
+// group's rows read as zero.
+bool weight_map16(CUtensorMap* out, const void* w, int E, int groups, int rows_per_group, int K) {
+  const cuuint64_t row_bytes = (cuuint64_t)K * 2;
+  cuuint64_t dims[3] = {row_bytes, (cuuint64_t)rows_per_group, (cuuint64_t)E * groups};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * rows_per_group};
+  cuuint32_t box[3] = {128, (cuuint32_t)kMTile, 1};
+  return make_map(out, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Records a caller event; while the stream is being captured the record is made an
@@ -536,6 +548,103 @@ int moe_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t
   norm.eps = eps;
   return forward_impl(x, w_router, router_bias, w_gateup, w_down, T, H, I, E, k, workspace, workspace_bytes, out,
                       topk_idx_out, topk_w_out, nullptr, stream, g, norm, residual_out);
+}
+
+int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const uint16_t* w_gateup,
+                     const uint16_t* w_down, int T, int H, int I, int E, int k, void* workspace,
+                     size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
+                     moe_stream_t stream) {
+  int st = check_shape(T, H, I, E, k);
+  if (st != MOE_OK) return st;
+  if (H % 64 || I % 64) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!x || !w_router || !w_gateup || !w_down || !workspace || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(out, 16) || !aligned(w_gateup, 16) ||
+      !aligned(w_down, 16) || !aligned(workspace, 256))
+    return MOE_ERR_INVALID_ARG;
+  const int bm = tile_rows_policy(T, k, E);
+  const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
+  if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void* ws = workspace;
+  int32_t* idx = topk_idx_out ? topk_idx_out : ws_ptr<int32_t>(ws, L.idx);
+  float* w = topk_w_out ? topk_w_out : ws_ptr<float>(ws, L.w);
+  int32_t* perm = ws_ptr<int32_t>(ws, L.perm);
+  TileEntry* tiles = ws_ptr<TileEntry>(ws, L.tiles);
+  int32_t* num_tiles = ws_ptr<int32_t>(ws, L.num_tiles);
+
+  // route + top-k + table: the same launch as the MXFP4 layer
+  RouteParams r = route_params(x, w_router, router_bias, T, H, E, k, ws_ptr<float>(ws, L.logits), 0, idx, w, ws, L);
+  r.build_table = 1;
+  r.bm = bm;
+  r.counts = ws_ptr<int32_t>(ws, L.counts);
+  r.offsets = ws_ptr<int32_t>(ws, L.offsets);
+  r.perm = perm;
+  r.inv_perm = ws_ptr<int32_t>(ws, L.inv_perm);
+  r.tiles = tiles;
+  r.num_tiles = num_tiles;
+  r.tile_first = ws_ptr<int32_t>(ws, L.tile_first);
+  if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // permute: bf16 rows of x into tile order
+  ScatterX16Params sx{};
+  sx.x = x;
+  sx.T = T; sx.H = H; sx.E = E; sx.k = k; sx.bm = bm; sx.max_tiles = L.max_tiles;
+  sx.topk_idx = idx;
+  sx.inv_perm = r.inv_perm;
+  sx.offsets = r.offsets;
+  sx.tile_first = r.tile_first;
+  sx.q_tile = ws_ptr<uint8_t>(ws, L.x_q);
+  if (launch_scatter_x16(sx, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // gate/up + SwiGLU (h in bf16, tile order), then down into the slots
+  GemmParams g{};
+  if (!weight_map16(&g.tm_w, w_gateup, E, 2, I, H)) return MOE_ERR_CUDA;
+  g.w16 = 1;
+  g.act_q = ws_ptr<uint8_t>(ws, L.x_q);
+  g.tiles = tiles;
+  g.num_tiles = num_tiles;
+  g.perm = perm;
+  g.T = T; g.H = H; g.I = I; g.E = E; g.k = k; g.bm = bm; g.max_tiles = L.max_tiles;
+  g.K = H;
+  g.kg = H / 64;
+  g.mt = ceil_div(I, kMTile);
+  g.rows_out = I;
+  g.w_groups = 2;
+  g.w_mt = g.mt;
+  g.group_tiles = bm >= 128 ? 32 : (bm >= 64 ? 16 : 1);
+  g.h_q = ws_ptr<uint8_t>(ws, L.h_q);
+  g.grid = persistent_ctas();
+  g.status = ws_ptr<uint32_t>(ws, L.status);
+  st = cuda_status(launch_gateup(g, s));
+  if (st != MOE_OK) return st;
+
+  GemmParams d{};
+  if (!weight_map16(&d.tm_w, w_down, E, 1, H, I)) return MOE_ERR_CUDA;
+  d.w16 = 1;
+  d.act_q = ws_ptr<uint8_t>(ws, L.h_q);
+  d.tiles = tiles;
+  d.num_tiles = num_tiles;
+  d.perm = perm;
+  d.T = T; d.H = H; d.I = I; d.E = E; d.k = k; d.bm = bm; d.max_tiles = L.max_tiles;
+  d.K = I;
+  d.kg = I / 64;
+  d.mt = ceil_div(H, kMTile);
+  d.rows_out = H;
+  d.w_groups = 1;
+  d.w_mt = d.mt;
+  d.m_pair = 0;
+  d.group_tiles = bm >= 128 ? 32 : (bm >= 64 ? 16 : 1);
+  d.topk_w = w;
+  d.slots = ws_ptr<float>(ws, L.slots);
+  d.grid = persistent_ctas();
+  d.status = ws_ptr<uint32_t>(ws, L.status);
+  st = cuda_status(launch_down(d, s));
+  if (st != MOE_OK) return st;
+  CombineParams c{};
+  c.slots = d.slots;
+  c.T = T; c.H = H; c.k = k;
+  c.out = out;
+  return cuda_status(launch_combine(c, s));
 }
 
 int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,

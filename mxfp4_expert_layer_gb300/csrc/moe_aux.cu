@@ -174,6 +174,33 @@ cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream) {
   return launch_pdl(encode_x_kernel<false>, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
 }
 
+__global__ void __launch_bounds__(kAuxThreads) scatter_x16_kernel(ScatterX16Params p) {
+  const int nv = p.H / 8;
+  const long long i = (long long)blockIdx.x * kAuxThreads + threadIdx.x;
+  const bool live = i < (long long)p.T * nv;
+  const int t = live ? (int)(i / nv) : 0, v = live ? (int)(i - (long long)t * nv) : 0;
+  uint4 val = make_uint4(0, 0, 0, 0);
+  if (live) val = __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)t * p.H) + v);
+  ptx::pdl_wait();  // routing has completed: its tile table is visible
+  ptx::pdl_launch_dependents();
+  if (!live) return;
+  for (int j = 0; j < p.k; ++j) {
+    const int a = t * p.k + j;
+    const int e = __ldcg(p.topk_idx + a);
+    if (e < 0 || e >= p.E) continue;
+    const int q = __ldcg(p.inv_perm + a) - __ldcg(p.offsets + e);
+    const int tile = __ldcg(p.tile_first + e) + q / p.bm, r = q % p.bm;
+    if (tile < 0 || tile >= p.max_tiles) continue;
+    *reinterpret_cast<uint4*>(p.q_tile + act16_offset(tile, r, 8 * v, p.max_tiles, p.bm)) = val;
+  }
+}
+
+cudaError_t launch_scatter_x16(const ScatterX16Params& p, cudaStream_t stream) {
+  const long long threads = (long long)p.T * (p.H / 8);
+  const int blocks = (int)((threads + kAuxThreads - 1) / kAuxThreads);
+  return launch_pdl(scatter_x16_kernel, dim3(blocks > 0 ? blocks : 1), dim3(kAuxThreads), 0, stream, p);
+}
+
 // The permute step: every (tile row, K group) copies its token's four encoded
 // 64-byte code runs and their exponent words from token order into the tile order
 // the gate/up GEMM loads by TMA.  Rows past a tile's last token are left as they

@@ -257,6 +257,15 @@ __host__ __device__ inline size_t act_offset(int tile, int t, int r, int k, int 
 }
 
 // Scale atom byte offset of (row r within a tile, MX block b within a K group).
+// bf16 activations (the bf16-weight GEMMs): one image per (64-value K stage, tile)
+// of bm rows x 128 bytes, 128-byte swizzled (16-byte chunk c of row r stored at
+// c ^ (r % 8)), so one bulk copy lands it in the layout the MMA reads:
+// [K / 64][max_tiles][bm][128 B].
+__host__ __device__ inline size_t act16_offset(int tile, int r, int k, int max_tiles, int bm) {
+  const int byte = (k % 64) * 2;
+  return (((size_t)(k / 64) * max_tiles + tile) * bm + r) * 128 + ((((byte >> 4) ^ (r & 7)) << 4) | (byte & 15));
+}
+
 __host__ __device__ inline int sf_atom_offset(int r, int b) {
   return (r >> 7) * kSfAtomBytes + (r & 31) * 16 + ((r >> 5) & 3) * 4 + b;
 }

@@ -41,22 +41,24 @@ constexpr uint64_t kWaitLimit = 1000000000ull;  // ns a bounded mbarrier wait ma
 
 // MPAIR (down only): two neighbouring 128-row M tiles per work unit, sharing each
 // stage's B tile, so a stage carries twice the weight bytes per activation byte.
-template <int BM, bool GATEUP, bool MPAIR>
+// W16: bf16 weights and activations (kind::f16, no scales, one term per token).
+template <int BM, bool GATEUP, bool MPAIR, bool W16 = false>
 struct GemmCfg {
   static constexpr int kA = (GATEUP || MPAIR) ? 2 : 1;       // weight tiles per stage (gate/up, or 2 M tiles)
-  static constexpr int kKStage = gemm_kstage(BM);            // K values per stage
-  static constexpr int kKBytes = kKStage / 2;                // bytes per operand row per stage
-  static constexpr int kAtoms = kKStage / kKGroup;           // scale atoms per 128 rows per stage
-  static constexpr int kKSteps = kKStage / 64;               // K = 64 MMA steps per stage
+  static constexpr int kKStage = W16 ? 64 : gemm_kstage(BM); // K values per stage
+  static constexpr int kKBytes = W16 ? 128 : kKStage / 2;    // bytes per operand row per stage
+  static constexpr int kAtoms = W16 ? 0 : kKStage / kKGroup; // scale atoms per 128 rows per stage
+  static constexpr int kKSteps = W16 ? kKStage / 16 : kKStage / 64;  // MMA K steps (32 bytes of every row)
   static constexpr int kATileBytes = kMTile * kKBytes;       // one 128-row weight tile of a stage
-  static constexpr bool kConcat = kTerms * BM <= 64;         // all terms in one MMA along N
+  static constexpr int kRowTerms = W16 ? 1 : kTerms;         // B rows per token
+  static constexpr bool kConcat = !W16 && kTerms * BM <= 64; // all terms in one MMA along N
   static constexpr int kN = kConcat ? kTerms * BM : BM;      // MMA N
   static constexpr int kAccN = kN;                           // accumulator columns per weight tile
   static constexpr int kAccCols = kA * kAccN;
   static constexpr int kVals = kA * BM;                      // values per row after summing terms
-  static constexpr int kBRows = kTerms * BM;                 // B tile rows (terms x token rows)
+  static constexpr int kBRows = kRowTerms * BM;              // B tile rows (terms x token rows)
   static constexpr int kBBytes = kBRows * kKBytes;
-  static constexpr int kNbAtoms = (kBRows + 127) / 128;      // B scale atoms per stage
+  static constexpr int kNbAtoms = W16 ? 0 : (kBRows + 127) / 128;  // B scale atoms per stage
   static constexpr int kSfBytes = (kA + kNbAtoms) * kAtoms * kSfAtomBytes;
   static constexpr int kStageRaw = kA * kATileBytes + kBBytes + kSfBytes;
   static constexpr int kStageBytes = (kStageRaw + 1023) / 1024 * 1024;
@@ -131,10 +133,10 @@ __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.f + __
 
 }  // namespace
 
-template <int BM, bool GATEUP, bool MPAIR>
-__global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
+template <int BM, bool GATEUP, bool MPAIR, bool W16>
+__global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using C = GemmCfg<BM, GATEUP, MPAIR>;
+  using C = GemmCfg<BM, GATEUP, MPAIR, W16>;
   extern __shared__ uint8_t gemm_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gemm_smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
@@ -215,7 +217,8 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
         const TileEntry te = load_tile(p.tiles + tile);
         expert = te.expert;
         // token-major tiles: only the real tokens' rows (kTerms per token) are loaded
-        b_rows = C::kConcat ? kTerms * max(1, min(te.n_rows, BM)) : C::kBRows;
+        // (the MMA's columns of rows never loaded are never read)
+        b_rows = (C::kConcat || W16) ? C::kRowTerms * max(1, min(te.n_rows, BM)) : C::kBRows;
       };
       auto advance = [&]() {
         if (++kk == kk1 && ++si < sch.nseg) open_seg();
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
           const int grp = GATEUP ? j : 0;
           tma_load_3d_hint(a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile,
                            expert * p.w_groups + grp, w_policy);
+          if constexpr (W16) continue;
           const int msf = min(mrow, p.w_mt - 1);
           const uint8_t* wsf =
               p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)p.kg_sf * kSfAtomBytes;
@@ -245,6 +249,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
         // the (stage, tile) image is contiguous and already swizzled: one bulk copy
         bulk_load(b_tile(s), p.act_q + ((size_t)b_kk * p.max_tiles + b_tile_idx) * (size_t)(C::kBRows * C::kKBytes),
                   (uint32_t)rows * (uint32_t)C::kKBytes, &full_bar[s]);
+        if constexpr (W16) return;
         // the stage's kAtoms K groups of scale atoms are adjacent
         bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * p.kg_sf + (size_t)b_kk * C::kAtoms) * (kSfAtomBytes * C::kNbAtoms),
                   C::kAtoms * C::kNbAtoms * kSfAtomBytes, &full_bar[s]);
@@ -327,6 +332,20 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
             break;
           }
           tc_fence_after();
+          if constexpr (W16) {
+            // bf16 x bf16: four K = 16 steps per 128-byte stage row, no scales
+            constexpr uint32_t idesc16 = idesc_bf16(kMTile, C::kN);
+            for (int ks = 0; ks < C::kKSteps; ++ks) {
+              const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(b_tile(s)) + 32 * ks);
+              const uint32_t acc = seg_first ? 0u : 1u;
+              for (int j = j0; j < j1; ++j)
+                mma_bf16(acc_base + j * C::kAccN, smem_desc_kmajor_sw128(smem_u32(a_tile(s, j)) + 32 * ks), bdesc,
+                         idesc16, acc);
+              seg_first = false;
+            }
+            mma_commit(&empty_bar[s]);
+            continue;
+          }
           const uint32_t sfc = tmem + sf_col0 + s * C::kSfColsPerStage;
           // this issuer's copy of the B scale atoms
           const uint32_t sfb0 = sfc + 4 * C::kA * C::kAtoms + issuer * 4 * C::kNbAtoms * C::kAtoms;
@@ -412,7 +431,33 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
 
       // the math of 16 token columns starting at c0, given g/u (gate/up) or y (down)
       auto consume = [&](int c0, const float* va, const float* vb) {
-        if constexpr (GATEUP) {
+        if constexpr (GATEUP && W16) {
+          // h = silu(g) * u -> shared memory (transposed), then bf16 rows of h in the
+          // down GEMM's B layout: thread (column j, 16 features qb) stores two 16-byte chunks
+          const bool fvalid = feat < p.I;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) s_xpose[j * kMTile + m] = fvalid ? silu_f(va[j]) * vb[j] : 0.f;
+          epi_bar();
+          const int j = et >> 3, qb = et & 7;
+          const int r = c0 + j, f0 = mt * kMTile + qb * 16;
+          if (r < nrows && f0 < p.I) {
+            const float4* src = reinterpret_cast<const float4*>(s_xpose + j * kMTile + qb * 16);
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float4 f4 = src[i];
+              w[2 * i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f4.x)) |
+                         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f4.y)) << 16);
+              w[2 * i + 1] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f4.z)) |
+                             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f4.w)) << 16);
+            }
+            *reinterpret_cast<uint4*>(p.h_q + act16_offset(tile, r, f0, p.max_tiles, BM)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(p.h_q + act16_offset(tile, r, f0 + 8, p.max_tiles, BM)) =
+                make_uint4(w[4], w[5], w[6], w[7]);
+          }
+          epi_bar();  // s_xpose reused by the next chunk
+        } else if constexpr (GATEUP) {
           // h = silu(g) * u -> shared memory, transposed so that one thread holds the 32
           // features of one MX block of one token column
           const bool fvalid = feat < p.I;
@@ -545,10 +590,10 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <int BM, bool GATEUP, bool MPAIR>
+template <int BM, bool GATEUP, bool MPAIR, bool W16>
 static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
-  using C = GemmCfg<BM, GATEUP, MPAIR>;
-  auto kern = moe_gemm_kernel<BM, GATEUP, MPAIR>;
+  using C = GemmCfg<BM, GATEUP, MPAIR, W16>;
+  auto kern = moe_gemm_kernel<BM, GATEUP, MPAIR, W16>;
   // the shared-memory opt-in is a per-device function attribute: set it once per device
   static bool configured[64] = {};
   int dev = 0;
@@ -562,19 +607,22 @@ static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
   return launch_pdl(kern, dim3(p.grid), dim3(C::kThreads), C::kSmemBytes, stream, p);
 }
 
-template <bool GATEUP, bool MPAIR>
+template <bool GATEUP, bool MPAIR, bool W16>
 static cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream) {
   switch (p.bm) {
-    case 16: return launch_gemm_t<16, GATEUP, MPAIR>(p, stream);
-    case 64: return launch_gemm_t<64, GATEUP, MPAIR>(p, stream);
-    case 128: return launch_gemm_t<128, GATEUP, MPAIR>(p, stream);
+    case 16: return launch_gemm_t<16, GATEUP, MPAIR, W16>(p, stream);
+    case 64: return launch_gemm_t<64, GATEUP, MPAIR, W16>(p, stream);
+    case 128: return launch_gemm_t<128, GATEUP, MPAIR, W16>(p, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream) { return launch_gemm<true, false>(p, stream); }
+cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream) {
+  return p.w16 ? launch_gemm<true, false, true>(p, stream) : launch_gemm<true, false, false>(p, stream);
+}
 cudaError_t launch_down(const GemmParams& p, cudaStream_t stream) {
-  return p.m_pair ? launch_gemm<false, true>(p, stream) : launch_gemm<false, false>(p, stream);
+  if (p.w16) return launch_gemm<false, false, true>(p, stream);  // bf16: no M-tile pairs
+  return p.m_pair ? launch_gemm<false, true, false>(p, stream) : launch_gemm<false, false, false>(p, stream);
 }
 
 }  // namespace moe

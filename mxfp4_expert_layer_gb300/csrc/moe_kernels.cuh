@@ -91,6 +91,20 @@ struct EncodeXParams {
 };
 cudaError_t launch_encode_x(const EncodeXParams& p, cudaStream_t stream);
 
+// The permute step of the bf16-weight layer: after routing, every token's bf16 row
+// goes to the tile rows of its k assignments (act16_offset layout).  Its x loads
+// are issued before the dependency wait (routing waited for earlier work).
+struct ScatterX16Params {
+  const uint16_t* x;          // bf16 [T, H]
+  int T, H, E, k, bm, max_tiles;
+  const int32_t* topk_idx;    // [T, k]
+  const int32_t* inv_perm;    // [T*k]
+  const int32_t* offsets;     // [E]
+  const int32_t* tile_first;  // [E]
+  uint8_t* q_tile;            // act16_offset layout
+};
+cudaError_t launch_scatter_x16(const ScatterX16Params& p, cudaStream_t stream);
+
 // The permute step: encoded x rows copied from token order into the tile order of
 // the gate/up GEMM's B operand.
 struct GatherXParams {
@@ -134,6 +148,7 @@ struct GemmParams {
   float* slots;            // f32 [T*k, H]: w_tj * y_tj per assignment
   int grid;                // persistent CTAs (<= kMaxCtas)
   uint32_t* status;
+  int w16;                 // bf16 weights and activations (act16_offset layout, no scales)
 };
 cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_down(const GemmParams& p, cudaStream_t stream);

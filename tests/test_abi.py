@@ -101,6 +101,13 @@ def test_host_argument_checks_return_codes(lib):
     assert fnorm(gating=3) == L.MOE_ERR_INVALID_ARG
     assert fnorm(rout=fake) == L.MOE_ERR_INVALID_ARG           # residual_out may not be out
     assert fnorm(rout=fake + 8) == L.MOE_ERR_INVALID_ARG       # misaligned residual_out
+    # the bf16-weight layer: H and I must be multiples of 64
+    def f16(H_=H, I_=I, x=fake, wgu=fake):
+        return L.moe_forward_bf16(x, fake, None, wgu, fake, T, H_, I_, E, k, fake, ws, fake, None, None, None)
+    assert f16(H_=2880 + 32) == L.MOE_ERR_UNSUPPORTED_SHAPE
+    assert f16(I_=2880 + 32) == L.MOE_ERR_UNSUPPORTED_SHAPE
+    assert f16(x=None) == L.MOE_ERR_INVALID_ARG
+    assert f16(wgu=fake + 8) == L.MOE_ERR_INVALID_ARG
     assert L.moe_build_tile_table(fake, T, k, E, 32, fake, fake, fake, fake, fake, fake, None) == \
         L.MOE_ERR_UNSUPPORTED_SHAPE                            # tile rows must be 16, 64 or 128
     assert L.moe_prepare_weights(fake, fake, E, 2 * I, H, 5, fake, 1 << 40, None) == L.MOE_ERR_UNSUPPORTED_SHAPE

@@ -20,7 +20,8 @@
  *    stream) and never synchronise the host, except moe_get_device_status.
  *  - The return value is a status: MOE_OK (0) or a negative MOE_ERR_* code.  On an
  *    error nothing has been launched unless the code is MOE_ERR_CUDA.
- *  - Shapes: 1 <= T, H % 32 == 0, I % 32 == 0, 1 <= k <= E <= 256, k <= 32.
+ *  - Shapes: 1 <= T, T * k <= 2^24, H % 32 == 0 with 32 <= H <= 8192, I % 32 == 0
+ *    with 32 <= I <= 16384, 1 <= k <= E <= 256, k <= 32.
  *  - bf16 arrays are raw bf16 bit patterns (uint16_t).
  *  - Expert weights: MXFP4 = FP4 E2M1 codes in blocks of 32 along K sharing one
  *    E8M0 scale, value = E2M1[code] * 2^(scale - 127) (OCP MX v1.0).  Raw layout:

@@ -17,11 +17,12 @@ namespace {
 // ------------------------------------------------------------------ checks
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-constexpr int kMaxDim = 8192;
+constexpr int kMaxDim = 8192;     // H (a routing row, an encoder block of the norm step)
+constexpr int kMaxInter = 16384;  // I (Mixtral-8x7B's is 14336)
 
 int check_shape(int T, int H, int I, int E, int k) {
   if (T < 1 || H < 32 || I < 32 || E < 1 || k < 1) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (H % 32 || I % 32 || H > kMaxDim || I > kMaxDim) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 32 || I % 32 || H > kMaxDim || I > kMaxInter) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (E > kMaxExperts || k > E || k > kMaxTopK) return MOE_ERR_UNSUPPORTED_SHAPE;
   if ((long long)T * k > (1LL << 24)) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;

@@ -106,6 +106,7 @@ def test_host_argument_checks_return_codes(lib):
         return L.moe_forward_bf16(x, fake, None, wgu, fake, T, H_, I_, E, k, fake, ws, fake, None, None, None)
     assert f16(H_=2880 + 32) == L.MOE_ERR_UNSUPPORTED_SHAPE
     assert f16(I_=2880 + 32) == L.MOE_ERR_UNSUPPORTED_SHAPE
+    assert f16(I_=16384 + 64) == L.MOE_ERR_UNSUPPORTED_SHAPE    # I above its limit
     assert f16(x=None) == L.MOE_ERR_INVALID_ARG
     assert f16(wgu=fake + 8) == L.MOE_ERR_INVALID_ARG
     assert L.moe_build_tile_table(fake, T, k, E, 32, fake, fake, fake, fake, fake, fake, None) == \

@@ -621,7 +621,7 @@ cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream) {
   return p.w16 ? launch_gemm<true, false, true>(p, stream) : launch_gemm<true, false, false>(p, stream);
 }
 cudaError_t launch_down(const GemmParams& p, cudaStream_t stream) {
-  if (p.w16) return launch_gemm<false, false, true>(p, stream);  // bf16: no M-tile pairs
+  if (p.w16) return p.m_pair ? launch_gemm<false, true, true>(p, stream) : launch_gemm<false, false, true>(p, stream);
   return p.m_pair ? launch_gemm<false, true, false>(p, stream) : launch_gemm<false, false, false>(p, stream);
 }
 

@@ -134,3 +134,89 @@ def test_truncating_bf16_fails_rounding_pin(monkeypatch):
 
     vals = np.array([1.0 + 3 * 2 ** -8], dtype=np.float32)
     assert not np.array_equal(trunc(vals), oracle.bf16_round(vals))
+
+
+# ---------------------------------------------------------------- RMSNorm + residual
+def _norm_variant(kind):
+    def f(x_bits, r_bits, gamma_bits, eps, dtype=np.float32):
+        x = mo.bf16_to_f32(x_bits)
+        r = mo.bf16_to_f32(r_bits)
+        exact = (x + r).astype(np.float32)
+        s = mo.bf16_round(exact)
+        sn = (exact if kind == "unrounded_stream" else (x if kind == "dropped_residual" else s)).astype(dtype)
+        gam = mo.bf16_to_f32(gamma_bits).astype(dtype)
+        msq = np.sum(sn * sn, axis=-1, keepdims=True) if kind == "sum_not_mean" else \
+            np.mean(sn * sn, axis=-1, keepdims=True)
+        if kind == "eps_outside_root":
+            y = sn / (np.sqrt(msq) + dtype(eps)) * gam
+        elif kind == "no_weight":
+            y = sn / np.sqrt(msq + dtype(eps))
+        elif kind == "one_plus_weight":
+            y = sn / np.sqrt(msq + dtype(eps)) * (1 + gam)
+        else:
+            y = sn / np.sqrt(msq + dtype(eps)) * gam
+        return mo.bf16_bits(s), mo.bf16_bits(y.astype(np.float32))
+    return f
+
+
+@pytest.mark.parametrize("kind", ["dropped_residual", "sum_not_mean", "eps_outside_root", "no_weight",
+                                  "one_plus_weight", "unrounded_stream"])
+def test_broken_rmsnorm_fails_pins(monkeypatch, kind):
+    from tests import test_oracle_pins as pins
+    monkeypatch.setattr(oracle, "rmsnorm_residual", _norm_variant(kind))
+    monkeypatch.setattr(mo, "rmsnorm_residual", _norm_variant(kind))
+    failed = 0
+    for pin in (lambda: pins.test_rmsnorm_residual_closed_forms(np.float64),
+                pins.test_rmsnorm_residual_rounds_the_stream_once,
+                pins.test_rmsnorm_residual_invariants,
+                pins.test_rmsnorm_residual_against_high_precision):
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, kind
+
+
+def test_unbroken_rmsnorm_variant_passes_pins(monkeypatch):
+    # the harness itself: the faithful restatement passes every pin
+    from tests import test_oracle_pins as pins
+    monkeypatch.setattr(oracle, "rmsnorm_residual", _norm_variant("faithful"))
+    pins.test_rmsnorm_residual_closed_forms(np.float64)
+    pins.test_rmsnorm_residual_rounds_the_stream_once()
+    pins.test_rmsnorm_residual_invariants()
+    pins.test_rmsnorm_residual_against_high_precision()
+
+
+# ---------------------------------------------------------------- bf16-weight experts
+def _dense_hidden_swapped(x_rows, w_e, I, dtype=np.float32):
+    w = mo.bf16_to_f32(w_e).astype(dtype)
+    x_rows = np.asarray(x_rows, dtype)
+    g, u = x_rows @ w[I:2 * I].T, x_rows @ w[:I].T
+    return (mo.silu(g) * u).astype(dtype)
+
+
+def _dense_hidden_no_silu(x_rows, w_e, I, dtype=np.float32):
+    w = mo.bf16_to_f32(w_e).astype(dtype)
+    x_rows = np.asarray(x_rows, dtype)
+    return ((x_rows @ w[:I].T) * (x_rows @ w[I:2 * I].T)).astype(dtype)
+
+
+def _dense_output_transposed(h_rows, w_e, dtype=np.float32):
+    w = mo.bf16_to_f32(w_e).astype(dtype)
+    return (np.asarray(h_rows, dtype) @ w).astype(dtype)
+
+
+@pytest.mark.parametrize("name,fn", [("expert_hidden_dense", _dense_hidden_swapped),
+                                     ("expert_hidden_dense", _dense_hidden_no_silu),
+                                     ("expert_output_dense", _dense_output_transposed)])
+def test_broken_dense_experts_fail_pins(monkeypatch, name, fn):
+    from tests import test_oracle_pins as pins
+    monkeypatch.setattr(mo, name, fn)
+    failed = 0
+    for pin in (lambda: pins.test_dense_layer_equals_mxfp4_layer_on_exactly_representable_weights(np.float32),
+                pins.test_dense_layer_against_python_loops):
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed > 0, name

@@ -283,3 +283,28 @@ def test_dense_layer_against_python_loops():
         y = [sum(h[f] * wd[e, o, f] for f in range(inp.I)) for o in range(inp.H)]
         assert res["idx"][t, 0] == e
         assert np.allclose(res["out_unrounded"][t], y, rtol=1e-12, atol=1e-12)
+
+
+def test_rmsnorm_residual_against_high_precision():
+    # y recomputed from the definition in 40-digit decimal arithmetic: the sum of two
+    # bf16 values is exact in a double, rounded to bf16 (the stream), the mean square
+    # is exact as a fraction, and the root and quotient are taken to 40 digits; y is then
+    # rounded once to bf16.  The oracle must agree bit for bit.
+    from decimal import Decimal, getcontext
+    from fractions import Fraction
+    getcontext().prec = 40
+    rng = np.random.Generator(np.random.PCG64(21))
+    T, H = 24, 16
+    x = oracle.bf16_bits(rng.standard_normal((T, H)).astype(np.float32) * 3)
+    r = oracle.bf16_bits((rng.standard_normal((T, H)) * np.exp2(rng.integers(-9, 2, (T, H)))).astype(np.float32))
+    g = oracle.bf16_bits((1 + 0.3 * rng.standard_normal(H)).astype(np.float32))
+    eps = 1e-5
+    s_bits, y_bits = oracle.rmsnorm_residual(x, r, g, eps, np.float64)
+    xf, rf, gf = _f(x).astype(np.float64), _f(r).astype(np.float64), _f(g).astype(np.float64)
+    s = oracle.bf16_round((xf + rf).astype(np.float32))  # x + r is exact in a double
+    assert np.array_equal(_f(s_bits), s)
+    for t in range(T):
+        ms = sum(Fraction(float(v)) ** 2 for v in s[t]) / H + Fraction(eps)
+        root = (Decimal(ms.numerator) / Decimal(ms.denominator)).sqrt()
+        want = [float(Decimal(float(s[t, i])) / root * Decimal(float(gf[i]))) for i in range(H)]
+        assert np.array_equal(_f(y_bits[t]), oracle.bf16_round(np.array(want, np.float32))), t

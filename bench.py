@@ -166,10 +166,13 @@ def cpu_baseline(inp, budget_s=12.0):
 
 # ---------------------------------------------------------------- distributed plumbing
 def dist_init(n):
+    """One process per GPU (torchrun env). NCCL on GPUs; gloo where there is no GPU
+    (the CPU tests of this plumbing). Replicas exchange only timings."""
     rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
     if world > 1:
+        import torch
         import torch.distributed as dist
-        dist.init_process_group("nccl")
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return rank, world
 
 
@@ -178,9 +181,16 @@ def max_over_ranks(v, world):
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_tokens_per_s(tokens_per_rank, ms_max, world):
+    """Whole-job throughput of `world` replicas: every rank's tokens over the slowest
+    rank's time per step."""
+    return world * tokens_per_rank / (ms_max * 1e-3)
 
 
 def barrier(world):
@@ -336,7 +346,7 @@ def main_dense(args):
                 "frac": ach / hbm, "peak_source": hbm_kind, "algorithmic_bytes_per_call": alg_bytes,
                 "traffic": None}
     line = {
-        "metric": "bf16-weight MoE layer (Mixtral-8x7B experts) tokens/s", "value": world * T / (ms * 1e-3),
+        "metric": "bf16-weight MoE layer (Mixtral-8x7B experts) tokens/s", "value": whole_job_tokens_per_s(T, ms, world),
         "unit": "tokens/s", "n_gpus": world, "steps": reps * step_calls, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
@@ -347,7 +357,7 @@ def main_dense(args):
         "us_per_call": ms * 1e3,
         "timing": f"CUDA graphs of {step_calls} consecutive layer calls, replayed",
         "roofline": roof,
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+        "e2e": {"value": whole_job_tokens_per_s(T, e2e_ms, world), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms},
         "gpu_launches": 5 * reps * step_calls,
         "clocks": clk,
@@ -610,7 +620,7 @@ def main():
         return
     us = ms * 1e3
     line = {
-        "metric": METRIC, "value": world * T / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "metric": METRIC, "value": whole_job_tokens_per_s(T, ms, world), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "mxfp4",
         "dtype_detail": "tcgen05 kind::mxf4: E2M1 weights x E2M1 activations (4 terms), E8M0 block scales, "
@@ -631,7 +641,7 @@ def main():
         "per_kernel_us": {n: v * 1e3 for n, v in zip(names, per_kernel)},
         "roofline": roof,
         "tensor_pipe": tensor_pipe,
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_tokens_per_s(T, e2e_ms, world), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2 * (2 if args.norm else 1),
                 "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms},
         "gpu_launches": launches * args.steps,

@@ -1,0 +1,66 @@
+"""The N > 1 plumbing of bench.py on CPU (gloo, world size 2): replicas exchange only
+their timings (max over ranks), and only rank 0 prints. The layer itself does not
+shard across GPUs ("replicas only"); these tests need no GPU."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank), MASTER_ADDR="127.0.0.1",
+                      MASTER_PORT=str(port))
+    sys.path.insert(0, ROOT)
+    import bench
+    import torch.distributed as dist
+    r, w = bench.dist_init(world)
+    assert (r, w) == (rank, world) and dist.get_backend() == "gloo"
+    # rank r took (r + 1.5) ms per step: the job's time is the slowest rank's
+    ms = bench.max_over_ranks(rank + 1.5, w)
+    bench.barrier(w)
+    q.put((rank, ms, bench.whole_job_tokens_per_s(64, ms, w)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_whole_job_value_gloo():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert [g[1] for g in got] == [2.5, 2.5]
+    # two replicas of 64 tokens in 2.5 ms: 51,200 tokens/s for the whole job
+    assert all(abs(g[2] - 2 * 64 / 2.5e-3) < 1e-6 for g in got)
+
+
+def test_reference_arm_under_torchrun_prints_once():
+    pytest.importorskip("numpy")
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+           "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"), "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "tiny"]
+    res = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [l for l in res.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

@@ -36,6 +36,7 @@ DOWN_FLOPS_PER_ROW = lambda H, I: 2 * H * I
 ACT_TERMS = 4                                            # E2M1 terms of the activation encoding
 MXFP4_OVER_BF16 = 13.5 / 2.25                            # nominal dense tensor-rate ratio
 DEFAULT_WORKLOAD = "gptoss20b_b1"
+NOMINAL_HBM_GBS = 7900.0                                 # GB300 HBM3e, nominal (context beside the measured peak)
 
 
 def parse():
@@ -638,6 +639,7 @@ def main():
         "eager_us_per_call": eager_ms * 1e3,
         "layer_hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "layer_roofline_frac": alg_bytes / (ms * 1e-3) / 1e9 / peak,
+        "layer_frac_of_nominal_hbm": alg_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
         "per_kernel_us": {n: v * 1e3 for n, v in zip(names, per_kernel)},
         "roofline": roof,
         "tensor_pipe": tensor_pipe,

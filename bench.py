@@ -122,12 +122,21 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- traffic from the committed ncu summary
+GEMM_HOST_MARKER = b"// ------------------------------------------------------------------ host launchers"
+
+
 def kernel_source_hash():
+    """Hash of the expert GEMM's device code: moe_gemm.cu up to its host launchers,
+    and the two headers it draws on.  A committed ncu summary is used only while
+    this matches the hash recorded with it."""
     import hashlib
     h = hashlib.sha256()
     for fn in ("moe_gemm.cu", "moe_common.cuh", "sm100_ptx.cuh"):
         with open(os.path.join(ROOT, "mxfp4_expert_layer_gb300", "csrc", fn), "rb") as f:
-            h.update(f.read())
+            data = f.read()
+        if fn == "moe_gemm.cu" and GEMM_HOST_MARKER in data:
+            data = data[:data.index(GEMM_HOST_MARKER)]
+        h.update(data)
     return h.hexdigest()[:16]
 
 

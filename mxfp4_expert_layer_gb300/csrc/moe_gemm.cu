@@ -590,6 +590,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
+// ------------------------------------------------------------------ host launchers
 template <int BM, bool GATEUP, bool MPAIR, bool W16>
 static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
   using C = GemmCfg<BM, GATEUP, MPAIR, W16>;

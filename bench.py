@@ -125,10 +125,18 @@ class ClockSampler:
 GEMM_HOST_MARKER = b"// ------------------------------------------------------------------ host launchers"
 
 
+def _code_only(src: bytes) -> bytes:
+    """C++ source with comments removed and whitespace collapsed (string literals in
+    these files hold no comment markers)."""
+    src = re.sub(rb"/\*.*?\*/", b" ", src, flags=re.S)
+    src = re.sub(rb"//[^\n]*", b" ", src)
+    return re.sub(rb"\s+", b" ", src).strip()
+
+
 def kernel_source_hash():
     """Hash of the expert GEMM's device code: moe_gemm.cu up to its host launchers,
-    and the two headers it draws on.  A committed ncu summary is used only while
-    this matches the hash recorded with it."""
+    and the two headers it draws on, comments and whitespace ignored.  A committed ncu
+    summary is used only while this matches the hash recorded with it."""
     import hashlib
     h = hashlib.sha256()
     for fn in ("moe_gemm.cu", "moe_common.cuh", "sm100_ptx.cuh"):
@@ -136,7 +144,7 @@ def kernel_source_hash():
             data = f.read()
         if fn == "moe_gemm.cu" and GEMM_HOST_MARKER in data:
             data = data[:data.index(GEMM_HOST_MARKER)]
-        h.update(data)
+        h.update(_code_only(data))
     return h.hexdigest()[:16]
 
 

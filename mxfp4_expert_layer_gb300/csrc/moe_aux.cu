@@ -1,6 +1,12 @@
 // Data movement kernels around the expert GEMMs:
 //  * encode_x: activation rows encoded once per token as four E2M1 terms with E8M0
-//    block scales (the tensor-core B operand, gathered by the gate/up GEMM);
+//    block scales (the tensor-core B operand).  In the forward it overlaps routing,
+//    then writes its rows straight into the tile order of the token's assignments
+//    (the permute); with the norm step it encodes y = RMSNorm(x + residual);
+//  * gather_x: the permute for the stage entry point (token order -> tile order);
+//  * scatter_x16: the permute of the bf16-weight layer (bf16 rows into tile order);
+//  * combine: weighted top-k sum of the down GEMM's slots, bf16 out, and the
+//    residual stream of the norm step;
 //  * prepare: one-time re-layout of the E8M0 scales of raw MXFP4 expert weights into
 //    the tensor-memory atom order ("MXFP4 MoE on tensor cores": weights permuted once
 //    at load; nothing is re-quantised; the codes stay row major);

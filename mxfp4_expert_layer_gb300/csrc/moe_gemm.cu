@@ -22,8 +22,14 @@
 //
 // Persistent CTAs (one per SM) take whole work units (expert tile x M tile)
 // round-robin.  Warp roles: warp 0 issues TMA loads into a ring of shared-memory
-// stages, warps 1 and 6 issue MMAs into one of two tensor-memory accumulators,
-// warps 2-5 run the epilogue of one unit while the MMAs of the next proceed.
+// stages, warps 1 and 6 issue MMAs into tensor-memory accumulators, warps 2-5 (and
+// 7-10 for 128-token tiles) run the epilogue of one unit while the MMAs of the next
+// proceed.
+//
+// The W16 instances run the same kernel on bf16 weights and activations
+// ("triton-kernels" README, "Fused MoE Dispatch": the Mixtral-style layer):
+// kind::f16 MMAs with K = 16, 64-value stages of the same 128-byte rows, no scales,
+// and bf16 h written by the gate/up epilogue.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
 #include "sm100_ptx.cuh"

@@ -7,13 +7,18 @@
 // kernel searching a tiles x experts grid); "triton-kernels" README, section
 // "Quick Start" (softmax gating + top-k, expert indices and weights returned).
 //
-// One launch does all three steps.  Many tokens: blocks of (8 tokens x a slice of
-// experts) compute logits; the last block to finish a token group (an integer
-// arrival count, no spinning) selects the top-k of those tokens; the last token
-// group to finish builds the tile table.  Few tokens (decode): one thread-block
-// cluster splits the hidden dimension, exchanges partial logits through
-// distributed shared memory and needs no global atomics.  Every result is computed by one fixed thread or
-// warp in a fixed order, so the outputs are bit-reproducible run to run.
+// One launch does all three steps.
+//  * Few tokens (decode): one thread-block cluster splits the hidden dimension,
+//    exchanges partial logits through distributed shared memory and needs no
+//    global atomics.
+//  * Many tokens: blocks of 32 tokens x all experts compute logits on the tensor
+//    cores, and the last block to finish (an integer arrival count, no spinning)
+//    builds the tile table.
+//  * Logits given: blocks of 8 tokens select the top-k.
+// With the norm step in front of the layer, both logit kernels normalise the rows
+// they stage (RMSNorm + residual, the range-sum order of moe_norm.cuh).  Every
+// result is computed by one fixed thread or warp in a fixed order, so the outputs
+// are bit-reproducible run to run.
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
 #include "sm100_ptx.cuh"

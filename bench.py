@@ -163,23 +163,26 @@ def committed_traffic(kernel: str, workload: str):
 
 
 # ---------------------------------------------------------------- CPU oracle baseline
-def cpu_baseline(inp, budget_s=12.0):
-    """The oracle as it stands, on the host cores, on a bounded sample of the workload."""
+def cpu_baseline(inp, budget_s=12.0, dense=False, max_tokens=8):
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload
+    (whole passes of the first min(T, max_tokens) tokens until the budget is spent)."""
     import numpy as np
     import oracle
     T = inp.T
-    n_tok = T if T <= 8 else 8
+    n_tok = min(T, max_tokens)
     tokens = np.arange(n_tok)
+    layer = oracle.moe_layer_dense if dense else oracle.moe_layer
     done, t0 = 0, time.perf_counter()
     while True:
-        oracle.moe_layer(inp, tokens=tokens)
+        layer(inp, tokens=tokens)
         done += n_tok
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
+    what = "bf16 experts" if dense else "MXFP4 decode of the touched experts"
     return {"value": done / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{done} tokens of {inp.name} ({n_tok} per pass, full layer incl. MXFP4 decode of the "
-                      f"touched experts) in {dt:.1f} s; numpy, BLAS threads up to {os.cpu_count()}"}
+            "sample": f"{done} tokens of {inp.name} ({n_tok} per pass, full layer incl. {what}) in {dt:.1f} s; "
+                      f"numpy, BLAS threads up to {os.cpu_count()}"}
 
 
 # ---------------------------------------------------------------- distributed plumbing
@@ -276,7 +279,8 @@ def main_dense(args):
     bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
     x, wr = bf(inp.x), bf(inp.w_router)
     layer = pkg.MoELayerBF16(wr, bf(inp.w_gateup), bf(inp.w_down), k=k)
-    del inp.w_gateup, inp.w_down
+    if args.no_cpu_baseline:
+        del inp.w_gateup, inp.w_down  # host copies are needed only by the CPU baseline
     idx = torch.empty(T, k, dtype=torch.int32, device=dev)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     layer(x, out=out, topk_idx=idx)
@@ -381,6 +385,8 @@ def main_dense(args):
         "clocks": clk,
         "device_status": status,
     }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, dense=True, max_tokens=2)
     print(json.dumps(line))
 
 

@@ -147,6 +147,96 @@ def check_topk(topk_softmax, T=64, E=16, k=4, seed=5):
     assert np.all(np.diff(sel, axis=1) <= 0)
 
 
+def brute_margin(row, k):
+    """(k-th largest) - ((k+1)-th largest) of a row by a Python full sort of its values,
+    in float64; +inf when the row has no (k+1)-th value (k = E)."""
+    vals = sorted((float(v) for v in row), reverse=True)
+    if k >= len(vals):
+        return math.inf
+    return vals[k - 1] - vals[k]
+
+
+def check_topk_margin(topk_margin, T=48, E=16, k=4, seed=8):
+    """The near-tie margin against a brute-force sort, on rows with exact ties planted
+    at positions (k-1, k) (margin exactly 0), inside the selection (k-2, k-1) and just
+    outside it (k, k+1); k = E gives +inf."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lg = rng.standard_normal((T, E)).astype(np.float32)
+    for t in range(T):
+        srt = np.argsort(-lg[t].astype(np.float64), kind="stable")
+        if t % 4 == 0:
+            lg[t, srt[k]] = lg[t, srt[k - 1]]
+        elif t % 4 == 1:
+            lg[t, srt[k - 2]] = lg[t, srt[k - 1]]
+        elif t % 4 == 2:
+            lg[t, srt[k + 1]] = lg[t, srt[k]]
+    got = np.asarray(topk_margin(lg, k), dtype=np.float64)
+    assert got.shape == (T,)
+    for t in range(T):
+        assert got[t] == brute_margin(lg[t], k), (t, got[t], brute_margin(lg[t], k))
+    assert np.all(got[0::4] == 0.0)
+    assert np.all(got[1::4] > 0.0) and np.all(got[2::4] > 0.0)
+    # a hand-written row: sorted values 5, 3, 2.5, 2.5, -1 -> margin(2) = 0.5, margin(3) = 0, margin(4) = 3.5
+    row = np.array([[2.5, -1.0, 5.0, 2.5, 3.0]], np.float32)
+    assert [float(topk_margin(row, kk)[0]) for kk in (1, 2, 3, 4)] == [2.0, 0.5, 0.0, 3.5]
+    # k = E: every expert is selected, no competitor
+    assert np.all(np.isinf(np.asarray(topk_margin(lg[:, :k], k))))
+
+
+def check_router_logits(router_logits, bf16_bits_of, seed=12):
+    """Router logits with a bias against closed forms: x = 0 gives the bias exactly;
+    a one-hot x row (x[t, h] = 1) gives column h of W_r plus the bias, one float32
+    rounding of an exact sum; and a small case against pure-Python float64 loops."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    E, H = 8, 64
+    w_bits = bf16_bits_of((0.02 * rng.standard_normal((E, H))).astype(np.float32))
+    w = (w_bits.astype(np.uint32) << 16).view(np.float32)
+    bias = (rng.standard_normal(E) * 3).astype(np.float32)
+    zero = np.zeros((3, H), np.uint16)
+    lg = router_logits(zero, w_bits, bias)
+    assert np.array_equal(lg, np.broadcast_to(bias, (3, E)))
+    assert np.array_equal(router_logits(zero, w_bits, None), np.zeros((3, E), np.float32))
+    hot = [0, 17, 63]
+    x1 = np.zeros((3, H), np.uint16)
+    for t, h in enumerate(hot):
+        x1[t, h] = 0x3F80  # bf16 1.0
+    lg = router_logits(x1, w_bits, bias)
+    for t, h in enumerate(hot):
+        for e in range(E):
+            want = np.float32(float(w[e, h]) + float(bias[e]))  # exact sum of two floats, rounded once
+            assert lg[t, e] == want, (t, e, lg[t, e], want)
+    assert np.array_equal(router_logits(x1, w_bits, None), w[:, hot].T)
+    # brute force: float64 loops over h, the bias added last
+    x_bits = bf16_bits_of(rng.standard_normal((5, H)).astype(np.float32))
+    x = (x_bits.astype(np.uint32) << 16).view(np.float32)
+    lg = router_logits(x_bits, w_bits, bias, np.float64)
+    for t in range(5):
+        for e in range(E):
+            want = sum(float(x[t, h]) * float(w[e, h]) for h in range(H)) + float(bias[e])
+            assert abs(lg[t, e] - want) <= 1e-12 * (1 + abs(want)), (t, e)
+
+
+# tokens-per-expert -> tile rows, worked by hand from the rule "16 if m <= 16, 64 if
+# m <= 64, else 128" with m = T*k/E (both boundaries included in the smaller tile)
+TILE_ROWS_CASES = [
+    (1, 4, 32, 16),      # m = 0.125
+    (128, 4, 32, 16),    # m = 16 exactly
+    (129, 4, 32, 64),    # m = 16.125
+    (200, 2, 16, 64),    # m = 25
+    (512, 4, 32, 64),    # m = 64 exactly
+    (513, 4, 32, 128),   # m = 64.125
+    (64, 4, 128, 16),    # m = 2
+    (4096, 4, 128, 128),  # m = 128
+    (13, 3, 3, 16),      # m = 13
+    (17, 1, 1, 64),      # m = 17
+]
+
+
+def check_tile_rows_policy(tile_rows_policy):
+    for T, k, E, want in TILE_ROWS_CASES:
+        assert tile_rows_policy(T, k, E) == want, (T, k, E, tile_rows_policy(T, k, E), want)
+
+
 def brute_tile_table(idx, E, bm):
     """Counting sort by hand with Python lists."""
     flat = [int(v) for v in np.asarray(idx).reshape(-1)]

@@ -42,6 +42,15 @@ def test_error_strings(lib):
         assert L.moe_error_string(code)
 
 
+def test_library_tile_policy_matches_worked_values(lib):
+    # the host-side policy of the C ABI against the values worked by hand for the
+    # oracle's pin (no GPU involved: moe_tile_rows is host arithmetic)
+    from mxfp4_expert_layer_gb300 import _lib as L
+    from tests.oracle_checks import TILE_ROWS_CASES
+    for T, k, E, want in TILE_ROWS_CASES:
+        assert L.moe_tile_rows(T, k, E) == want, (T, k, E)
+
+
 def test_sizes_and_policy(lib):
     from mxfp4_expert_layer_gb300 import _lib as L
     import oracle

@@ -220,3 +220,70 @@ def test_broken_dense_experts_fail_pins(monkeypatch, name, fn):
         except AssertionError:
             failed += 1
     assert failed > 0, name
+
+
+# ---------------------------------------------------------------- margin, router bias, tile policy
+def _margin_off_by_one_low(logits, k):
+    lg = np.sort(np.asarray(logits, np.float64), axis=1)[:, ::-1]
+    if k >= lg.shape[1]:
+        return np.full(lg.shape[0], np.inf)
+    return lg[:, max(k - 2, 0)] - lg[:, k - 1]
+
+
+def _margin_off_by_one_high(logits, k):
+    lg = np.sort(np.asarray(logits, np.float64), axis=1)[:, ::-1]
+    if k + 1 >= lg.shape[1]:
+        return np.full(lg.shape[0], np.inf)
+    return lg[:, k - 1] - lg[:, k + 1]
+
+
+def _margin_no_inf(logits, k):
+    lg = np.sort(np.asarray(logits, np.float64), axis=1)[:, ::-1]
+    return lg[:, k - 1] - lg[:, min(k, lg.shape[1] - 1)]
+
+
+@pytest.mark.parametrize("bad", [_margin_off_by_one_low, _margin_off_by_one_high, _margin_no_inf])
+def test_broken_margin_fails_pin(bad):
+    with pytest.raises(AssertionError):
+        oc.check_topk_margin(bad)
+
+
+def _logits_variant(kind):
+    def f(x_bits, w_router_bits, bias=None, dtype=np.float32):
+        x = mo.bf16_to_f32(x_bits).astype(dtype)
+        w = mo.bf16_to_f32(w_router_bits).astype(dtype)
+        lg = x @ w.T
+        if bias is not None and kind != "dropped":
+            b = np.asarray(bias, dtype)[None, :]
+            lg = lg + (2 * b if kind == "twice" else (-b if kind == "negated" else b))
+        if kind == "transposed_w":
+            lg = (x @ w.reshape(w.shape[1], w.shape[0])).astype(dtype)
+        return lg.astype(dtype)
+    return f
+
+
+@pytest.mark.parametrize("kind", ["dropped", "twice", "negated", "transposed_w"])
+def test_broken_router_bias_fails_pin(kind):
+    from synthetic import bf16_bits_from_f32
+    with pytest.raises(AssertionError):
+        oc.check_router_logits(_logits_variant(kind), bf16_bits_from_f32)
+
+
+def test_faithful_router_variant_passes_pin():
+    from synthetic import bf16_bits_from_f32
+    oc.check_router_logits(_logits_variant("faithful"), bf16_bits_from_f32)
+
+
+def _policy_strict(T, k, E):
+    m = T * k / E
+    return 16 if m < 16 else (64 if m < 64 else 128)
+
+
+def _policy_no_middle(T, k, E):
+    return 16 if T * k / E <= 16 else 128
+
+
+@pytest.mark.parametrize("bad", [_policy_strict, _policy_no_middle])
+def test_broken_tile_policy_fails_pin(bad):
+    with pytest.raises(AssertionError):
+        oc.check_tile_rows_policy(bad)

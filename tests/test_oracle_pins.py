@@ -98,6 +98,21 @@ def test_gating_variants_closed_forms():
     np.testing.assert_allclose(w4, 0.25, rtol=1e-15)
 
 
+def test_topk_margin_against_full_sort():
+    oc.check_topk_margin(oracle.topk_margin)
+    oc.check_topk_margin(oracle.topk_margin, T=20, E=128, k=4, seed=9)
+    oc.check_topk_margin(oracle.topk_margin, T=12, E=8, k=2, seed=10)
+
+
+def test_router_logits_bias_closed_forms():
+    from synthetic import bf16_bits_from_f32
+    oc.check_router_logits(oracle.router_logits, bf16_bits_from_f32)
+
+
+def test_tile_rows_policy_worked_values():
+    oc.check_tile_rows_policy(oracle.tile_rows_policy)
+
+
 def test_tile_table_brute_force_and_invariants():
     cases = []
     for (T, E, k, bm, skew, seed) in [(4, 8, 2, 16, 0, 0), (1, 32, 4, 16, 0, 1),

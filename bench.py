@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="default workload only: skip the batch-64, 120b and prefill lines of the `workloads` block")
     ap.add_argument("--norm", action="store_true",
                     help="RMSNorm + residual fused in front of the layer (moe_forward_norm)")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of CUDA-graph replays")
@@ -62,17 +64,6 @@ def measured_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
-
-
-def mxfp4_peak_tflops():
-    """Dense MXFP4 tensor peak: the measured bf16 GEMM burst rate times the nominal
-    MXFP4/bf16 ratio (no MXFP4 GEMM rate is measured on this machine)."""
-    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(p):
-        with open(p) as f:
-            d = json.load(f)
-        return float(d["bf16_tflops"]) * MXFP4_OVER_BF16, "measured bf16 x nominal mxfp4/bf16 ratio (6)"
-    return 1900.0 * MXFP4_OVER_BF16, "fallback bf16 x nominal mxfp4/bf16 ratio (6)"
 
 
 # ---------------------------------------------------------------- clocks
@@ -390,17 +381,42 @@ def main_dense(args):
     print(json.dumps(line))
 
 
-def main():
-    args = parse()
-    if args.workload.startswith("mixtral") or args.workload.startswith("dense"):
-        if args.impl == "reference":
-            print(json.dumps({"impl": "reference", "unavailable": "the bf16-weight workloads have no reference "
-                              "arm; their parity is checked against the oracle in tests/test_gpu_dense.py"}))
-            return
-        return main_dense(args)
-    if args.impl == "reference":
-        return run_reference(args)
-    rank, world = dist_init(args.gpus)
+STAGE_NAMES = ["route_topk_table", "encode_x", "gateup_swiglu", "down", "combine"]  # MOE_FORWARD_STAGES launches
+SIDE_WORKLOADS = ["gptoss20b_b64", "gptoss120b_b64", "gptoss120b_prefill4096"]
+
+
+def tensor_peaks(L, stream):
+    """The measured kind::mxf4 and kind::f16 MMA rates of this GPU (moe_tensor_peak),
+    and the rule's MXFP4 figure: the measured bf16 GEMM burst rate times the nominal
+    MXFP4/bf16 ratio."""
+    import ctypes
+    out = {}
+    for kind, name in ((L.MOE_PEAK_MXF4, "mxf4_mma_tflops"), (L.MOE_PEAK_BF16, "bf16_mma_tflops")):
+        v = ctypes.c_double(0.0)
+        st = L.moe_tensor_peak(kind, 20000, ctypes.byref(v), stream)
+        out[name] = v.value if st == 0 else None
+    bf16, kind = bf16_peak_tflops(sustained=False)
+    out["bf16_gemm_tflops"] = bf16
+    out["mxf4_rule_tflops"] = bf16 * MXFP4_OVER_BF16
+    out["rule_source"] = f"{kind} cuBLAS bf16 burst x nominal mxfp4/bf16 ratio ({MXFP4_OVER_BF16:g})"
+    return out
+
+
+def stage_bytes_and_flops(T, H, I, E, k, touched):
+    """Algorithmic bytes (and FLOPs) of each launch of one layer call."""
+    b = {"route_topk_table": E * H * 2 + T * H * 2,
+         "encode_x": T * H * 2 + T * k * H * (ACT_TERMS // 2 + 1 / 8),
+         "gateup_swiglu": touched * GATEUP_BYTES_PER_EXPERT(H, I),
+         "down": touched * DOWN_BYTES_PER_EXPERT(H, I),
+         "combine": T * k * H * 4 + T * H * 2}
+    f = {"gateup_swiglu": GATEUP_FLOPS_PER_ROW(H, I) * T * k, "down": DOWN_FLOPS_PER_ROW(H, I) * T * k}
+    return b, f
+
+
+def measure_layer(args, wl, rank, world, dev, stream_peaks, headline, steps):
+    """Everything measured for one MXFP4 workload: the graph-timed layer, eager
+    launches, the per-launch split, the roofline of the dominant launch, the tensor
+    pipe of the expert GEMMs and (headline only) the end-to-end number."""
     import numpy as np
     import torch
 
@@ -408,13 +424,7 @@ def main():
     from mxfp4_expert_layer_gb300 import _lib as L
     from synthetic import make_config
 
-    local = int(os.environ.get("LOCAL_RANK", 0))
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    pkg.build()
-    L.load()
-
-    inp = make_config(args.workload, seed=rank)
+    inp = make_config(wl, seed=rank)
     T, H, I, E, k = inp.T, inp.H, inp.I, inp.E, inp.k
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     x = to(inp.x.view(np.int16)).view(torch.bfloat16)
@@ -422,6 +432,8 @@ def main():
     bias = None if inp.router_bias is None else to(inp.router_bias)
     layer = pkg.MoELayer.from_mxfp4(wr, to(inp.gu_codes), to(inp.gu_scales), to(inp.dn_codes), to(inp.dn_scales),
                                     k=k, router_bias=bias)
+    if not headline or args.no_cpu_baseline:
+        del inp.gu_codes, inp.gu_scales, inp.dn_codes, inp.dn_scales  # only the CPU baseline reads them
     # routing of the workload (same for every call): touched experts give the algorithmic bytes
     idx = torch.empty(T, k, dtype=torch.int32, device=dev)
     wts = torch.empty(T, k, dtype=torch.float32, device=dev)
@@ -429,15 +441,15 @@ def main():
     layer(x, out=out, topk_idx=idx, topk_w=wts)
     torch.cuda.synchronize()
     touched = int(torch.unique(idx).numel())
-    gu_bytes = touched * GATEUP_BYTES_PER_EXPERT(H, I)
-    dn_bytes = touched * DOWN_BYTES_PER_EXPERT(H, I)
-    alg_bytes = gu_bytes + dn_bytes
+    sbytes, sflops = stage_bytes_and_flops(T, H, I, E, k, touched)
+    alg_bytes = sbytes["gateup_swiglu"] + sbytes["down"]
 
     # rotate copies of the whole layer input (expert weights, router weight, x) so the
     # touched experts of every call come from HBM and nothing a real model would not
     # find in L2 (another layer's router, another step's activations) is found there
     copies = max(1, min(16, math.ceil(4 * L2_BYTES / max(alg_bytes, 1))))
-    if args.norm:
+    norm = args.norm and headline
+    if norm:
         from synthetic import make_norm_inputs
         r_np, g_np, eps = make_norm_inputs(T, H, seed=rank)
         resid = to(r_np.view(np.int16)).view(torch.bfloat16)
@@ -450,11 +462,11 @@ def main():
         for _ in range(copies - 1)]
     ws = layer.workspace(T)
 
-    def call(i, events=None, norm=args.norm):
+    def call(i, events=None, with_norm=norm):
         wgu, wd, wr_i, x_i, r_i = wsets[i % copies]
         b = None if bias is None else bias.data_ptr()
         cs = torch.cuda.current_stream().cuda_stream
-        if norm and events is None:
+        if with_norm and events is None:
             st = L.moe_forward_norm(x_i.data_ptr(), r_i.data_ptr(), gamma.data_ptr(), eps, wr_i.data_ptr(), b,
                                     wgu.data_ptr(), wd.data_ptr(), T, H, I, E, k, 0, ws.data_ptr(), ws.numel(),
                                     out.data_ptr(), res_out.data_ptr(), None, None, cs)
@@ -469,30 +481,27 @@ def main():
 
     launches = L.moe_forward_launches(T, H, I, E, k)
     if args.profile:
-        for s_ in range(args.warmup + args.steps):
+        for s_ in range(args.warmup + steps):
             call(s_)
         torch.cuda.synchronize()
-        print(json.dumps({"profile_run": inp.name, "calls": args.warmup + args.steps,
-                          "status": layer.device_status(T)}))
-        return
+        return {"profile_run": inp.name, "calls": args.warmup + steps, "status": layer.device_status(T)}
 
     # the layer runs inside a captured decode step in the pages' engine: one CUDA
     # graph holds the calls of every weight copy in sequence (consecutive layers of
     # a step, each with its own weights), so a layer's first launch overlaps the
     # previous layer's last as it would in that step.  Single-call graphs serve the
-    # remainder of K steps and the per-stage split; --eager times plain launches.
-    nk = 4  # stages bracketed by moe_forward_timed's events (MOE_FORWARD_STAGES)
+    # remainder of K steps and the per-launch split; --eager times plain launches.
+    nk = len(STAGE_NAMES)
     step_calls = copies * math.ceil(8 / copies)  # layer calls per step graph: >= 8, whole rotations
-    names = ["route_topk_table", "encode_x", "gateup_swiglu", "down_combine"]
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
-    graphs, tgraphs, tevents = [], [], []
-    hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
-    hx.copy_(x.cpu())
-    hr = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
-    hr.copy_(resid.cpu())
-    hout = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
-    e2e_graphs = []
+    graphs, tgraphs, tevents, e2e_graphs = [], [], [], []
+    if headline:
+        hx = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+        hx.copy_(x.cpu())
+        hr = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
+        hr.copy_(resid.cpu())
+        hout = torch.empty(T, H, dtype=torch.bfloat16, pin_memory=True)
     with torch.cuda.stream(side):
         call(0)
         torch.cuda.synchronize()
@@ -510,24 +519,25 @@ def main():
                 call(j, ctypes_array(evs))
             tgraphs.append(tg)
             tevents.append(evs)
-            eg = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(eg, stream=side):
-                wsets[j][3].copy_(hx, non_blocking=True)
-                if args.norm:
-                    wsets[j][4].copy_(hr, non_blocking=True)
-                call(j)
-                hout.copy_(out, non_blocking=True)
-            e2e_graphs.append(eg)
+            if headline:
+                eg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(eg, stream=side):
+                    wsets[j][3].copy_(hx, non_blocking=True)
+                    if norm:
+                        wsets[j][4].copy_(hr, non_blocking=True)
+                    call(j)
+                    hout.copy_(out, non_blocking=True)
+                e2e_graphs.append(eg)
         step_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(step_graph, stream=side):
             for j in range(step_calls):
                 call(j)
-        if args.norm:
+        if norm:
             # the same step without the norm step, for its cost
             plain_graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(plain_graph, stream=side):
                 for j in range(step_calls):
-                    call(j, norm=False)
+                    call(j, with_norm=False)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -548,7 +558,6 @@ def main():
         for s_ in range(n % step_calls):
             graphs[s_ % copies].replay()
 
-    clocks = ClockSampler(local)
     # pre-warm: bring clocks up (~0.5 s of steps), then the W warm-up steps
     t_end = time.perf_counter() + 0.5
     i = 0
@@ -562,86 +571,147 @@ def main():
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    run_steps(args.steps)
+    run_steps(steps)
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = ev0.elapsed_time(ev1) / steps
     ms = max_over_ranks(ms, world)
-    i += args.steps
+    i += steps
 
-    plain_us = None
-    if args.norm:
+    res = {"inp": inp, "T": T, "H": H, "I": I, "E": E, "k": k, "touched": touched, "copies": copies,
+           "step_calls": step_calls, "alg_bytes": alg_bytes, "ms": ms, "launches": launches}
+    if norm:
         torch.cuda.synchronize()
-        reps_p = max(1, args.steps // step_calls)
+        reps_p = max(1, steps // step_calls)
         ev0.record(stream)
         for _ in range(reps_p):
             plain_graph.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-        plain_us = ev0.elapsed_time(ev1) * 1e3 / (reps_p * step_calls)
+        res["plain_us"] = ev0.elapsed_time(ev1) * 1e3 / (reps_p * step_calls)
 
     # eager launches, for reference (host launch overhead included)
     torch.cuda.synchronize()
     ev0.record(stream)
-    for s_ in range(args.steps):
+    for s_ in range(steps):
         call(i + s_)
     ev1.record(stream)
     torch.cuda.synchronize()
-    eager_ms = ev0.elapsed_time(ev1) / args.steps
+    res["eager_ms"] = ev0.elapsed_time(ev1) / steps
 
-    # per-kernel split: graphs with events between the launches
+    # per-launch split: single-call graphs with an event between consecutive launches
+    # (the event breaks the programmatic-launch overlap, so each launch is timed alone)
     per_kernel = [0.0] * nk
-    reps = max(1, args.steps // copies)
+    reps = max(1, steps // copies)
     for r in range(reps):
         for j in range(copies):
             tgraphs[j].replay()
             torch.cuda.synchronize()
             for q in range(nk):
                 per_kernel[q] += tevents[j][q].elapsed_time(tevents[j][q + 1])
-    per_kernel = [v / (reps * copies) for v in per_kernel]
-    alg = {"gateup_swiglu": gu_bytes, "down_combine": dn_bytes}
-    flops = {"gateup_swiglu": GATEUP_FLOPS_PER_ROW(H, I) * T * k, "down_combine": DOWN_FLOPS_PER_ROW(H, I) * T * k}
-    dom = max(alg, key=lambda n: per_kernel[names.index(n)])
-    dom_ms = per_kernel[names.index(dom)]
-    peak, peak_kind = measured_peaks()
-    mx_peak, mx_peak_kind = mxfp4_peak_tflops()
-    # which roof binds the dominant kernel: its weight bytes at the HBM peak, or the
-    # tensor-pipe work it issues (kTerms MMAs per product) at the MXFP4 peak
-    t_hbm = alg[dom] / (peak * 1e9)
-    t_tc = flops[dom] * ACT_TERMS / (mx_peak * 1e12)
-    tensor_bound = t_tc > t_hbm
-    if tensor_bound:
-        achieved = flops[dom] / (dom_ms * 1e-3) / 1e12
-        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": mx_peak, "unit": "TFLOP/s",
-                "frac": achieved / mx_peak, "peak_source": mx_peak_kind,
-                "algorithmic_flops_per_launch": flops[dom], "traffic": committed_traffic(dom, inp.name)}
+    per_kernel = {n: v / (reps * copies) for n, v in zip(STAGE_NAMES, per_kernel)}
+    res["per_kernel_ms"] = per_kernel
+
+    hbm, hbm_kind = measured_peaks()
+    mx = stream_peaks["mxf4_mma_tflops"] or stream_peaks["mxf4_rule_tflops"]
+    mx_src = "measured kind::mxf4 MMA rate (moe_tensor_peak)" if stream_peaks["mxf4_mma_tflops"] else \
+        stream_peaks["rule_source"]
+    # the dominant launch (longest single-launch time) and the roof that binds it: its
+    # algorithmic bytes at the HBM peak, or (expert GEMMs) the MMAs it issues
+    # (ACT_TERMS per product) at the measured MXFP4 rate
+    dom = max(per_kernel, key=per_kernel.get)
+    dom_ms = per_kernel[dom]
+    t_hbm = sbytes[dom] / (hbm * 1e9)
+    t_tc = sflops.get(dom, 0) * ACT_TERMS / (mx * 1e12)
+    if t_tc > t_hbm:
+        achieved = sflops[dom] / (dom_ms * 1e-3) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": mx, "unit": "TFLOP/s",
+                "frac": achieved / mx, "peak_source": mx_src,
+                "frac_of_bf16_x6": achieved / stream_peaks["mxf4_rule_tflops"],
+                "issued_frac": achieved * ACT_TERMS / mx,
+                "algorithmic_flops_per_launch": sflops[dom], "launch_us": dom_ms * 1e3,
+                "traffic": committed_traffic(dom, inp.name)}
     else:
-        achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": peak_kind,
-                "algorithmic_bytes_per_launch": alg[dom], "traffic": committed_traffic(dom, inp.name)}
-    gemm_ms = sum(per_kernel[names.index(n)] for n in alg)
-    tensor_pipe = {"algorithmic_tflops": sum(flops.values()) / (gemm_ms * 1e-3) / 1e12,
-                   "issued_tflops": ACT_TERMS * sum(flops.values()) / (gemm_ms * 1e-3) / 1e12,
-                   "mxfp4_peak_tflops": mx_peak, "peak_source": mx_peak_kind,
-                   "issued_frac": ACT_TERMS * sum(flops.values()) / (gemm_ms * 1e-3) / 1e12 / mx_peak,
-                   "note": f"expert GEMMs only; each product is issued as {ACT_TERMS} E2M1-term MMAs"}
+        achieved = sbytes[dom] / (dom_ms * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": hbm_kind,
+                "algorithmic_bytes_per_launch": sbytes[dom], "launch_us": dom_ms * 1e3,
+                "traffic": committed_traffic(dom, inp.name)}
+    res["roofline"] = roof
+    gemm_ms = per_kernel["gateup_swiglu"] + per_kernel["down"]
+    fl = sum(sflops.values())
+    res["tensor_pipe"] = {"algorithmic_tflops": fl / (gemm_ms * 1e-3) / 1e12,
+                          "issued_tflops": ACT_TERMS * fl / (gemm_ms * 1e-3) / 1e12,
+                          "mxf4_peak_tflops": mx, "peak_source": mx_src,
+                          "algorithmic_frac": fl / (gemm_ms * 1e-3) / 1e12 / mx,
+                          "issued_frac": ACT_TERMS * fl / (gemm_ms * 1e-3) / 1e12 / mx,
+                          "algorithmic_frac_of_bf16_x6": fl / (gemm_ms * 1e-3) / 1e12 / stream_peaks["mxf4_rule_tflops"],
+                          "note": f"expert GEMMs (gate/up + down launches); each product is issued as {ACT_TERMS} "
+                                  f"E2M1-term MMAs"}
+
+    if headline:
+        # end to end through the C ABI: pinned host input -> device, layer, device -> pinned host
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s_ in range(steps):
+            e2e_graphs[(i + s_) % copies].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        res["e2e_ms"] = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    res["status"] = layer.device_status(T)
+    return res
+
+
+def main():
+    args = parse()
+    if args.workload.startswith("mixtral") or args.workload.startswith("dense"):
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the bf16-weight workloads have no reference "
+                              "arm; their parity is checked against the oracle in tests/test_gpu_dense.py"}))
+            return
+        return main_dense(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    rank, world = dist_init(args.gpus)
+    import torch
+
+    import mxfp4_expert_layer_gb300 as pkg
+    from mxfp4_expert_layer_gb300 import _lib as L
+
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pkg.build()
+    L.load()
+    peaks = tensor_peaks(L, torch.cuda.current_stream().cuda_stream)
+    if args.profile:
+        print(json.dumps(measure_layer(args, args.workload, rank, world, dev, peaks, True, args.steps)))
+        return
+    clocks = ClockSampler(local)
+    r = measure_layer(args, args.workload, rank, world, dev, peaks, True, args.steps)
+    side = {}
+    if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+        for wl in SIDE_WORKLOADS:
+            torch.cuda.empty_cache()
+            w = measure_layer(args, wl, rank, world, dev, peaks, False, min(args.steps, 100))
+            side[wl] = {"us_per_call": w["ms"] * 1e3,
+                        "tokens_per_s": whole_job_tokens_per_s(w["T"], w["ms"], world),
+                        "touched_experts": w["touched"],
+                        "layer_hbm_gbs": w["alg_bytes"] / (w["ms"] * 1e-3) / 1e9,
+                        "layer_roofline_frac": w["alg_bytes"] / (w["ms"] * 1e-3) / 1e9 / measured_peaks()[0],
+                        "per_kernel_us": {n: v * 1e3 for n, v in w["per_kernel_ms"].items()},
+                        "roofline": w["roofline"], "tensor_pipe": w["tensor_pipe"], "device_status": w["status"],
+                        "timing": f"CUDA graphs of {w['step_calls']} consecutive layer calls cycling over "
+                                  f"{w['copies']} weight copies, replayed; {min(args.steps, 100)} calls"}
+            del w
     clk = clocks.stop()
-
-    # end to end through the C ABI: pinned host input -> device, layer, device -> pinned host
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for s_ in range(args.steps):
-        e2e_graphs[(i + s_) % copies].replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
-
-    status = layer.device_status(T)
     if rank != 0:
         return
+    inp, T, H, I, E, k = r["inp"], r["T"], r["H"], r["I"], r["E"], r["k"]
+    ms, alg_bytes, copies, step_calls = r["ms"], r["alg_bytes"], r["copies"], r["step_calls"]
+    peak, peak_kind = measured_peaks()
     us = ms * 1e3
     line = {
         "metric": METRIC, "value": whole_job_tokens_per_s(T, ms, world), "unit": "tokens/s", "n_gpus": world,
@@ -651,7 +721,7 @@ def main():
                         "f32 accumulate, bf16 out",
         "data": "synthetic",
         "config": {"workload": inp.name, "T": T, "H": H, "I": I, "E": E, "k": k,
-                   "tile_rows": L.moe_tile_rows(T, k, E), "touched_experts": touched,
+                   "tile_rows": L.moe_tile_rows(T, k, E), "touched_experts": r["touched"],
                    "l2": f"{copies} rotating copies of weights, router weight and x "
                          f"({copies * alg_bytes / 1e6:.0f} MB of experts touched per rotation > 4x L2)",
                    "parallelism": f"replicas x{world}"},
@@ -659,23 +729,28 @@ def main():
         "timing": "eager launches" if args.eager else
                   f"CUDA graphs of {step_calls} consecutive layer calls cycling over {copies} weight "
                   f"copies, replayed",
-        "eager_us_per_call": eager_ms * 1e3,
+        "eager_us_per_call": r["eager_ms"] * 1e3,
         "layer_hbm_gbs": alg_bytes / (ms * 1e-3) / 1e9,
         "layer_roofline_frac": alg_bytes / (ms * 1e-3) / 1e9 / peak,
         "layer_frac_of_nominal_hbm": alg_bytes / (ms * 1e-3) / 1e9 / NOMINAL_HBM_GBS,
-        "per_kernel_us": {n: v * 1e3 for n, v in zip(names, per_kernel)},
-        "roofline": roof,
-        "tensor_pipe": tensor_pipe,
-        "e2e": {"value": whole_job_tokens_per_s(T, e2e_ms, world), "unit": "tokens/s",
+        "per_kernel_us": {n: v * 1e3 for n, v in r["per_kernel_ms"].items()},
+        "per_kernel_note": "each launch timed alone: single-call graphs with an event between consecutive "
+                           "launches, which removes the programmatic-launch overlap the layer runs with",
+        "roofline": r["roofline"],
+        "tensor_pipe": r["tensor_pipe"],
+        "tensor_peaks": peaks,
+        "e2e": {"value": whole_job_tokens_per_s(T, r["e2e_ms"], world), "unit": "tokens/s",
                 "h2d_bytes_per_step": T * H * 2 * (2 if args.norm else 1),
-                "d2h_bytes_per_step": T * H * 2, "ms_per_step": e2e_ms},
-        "gpu_launches": launches * args.steps,
+                "d2h_bytes_per_step": T * H * 2, "ms_per_step": r["e2e_ms"]},
+        "gpu_launches": r["launches"] * args.steps,
         "clocks": clk,
-        "device_status": status,
+        "device_status": r["status"],
     }
+    if side:
+        line["workloads"] = side
     if args.norm:
         line["config"]["norm"] = "RMSNorm + residual fused in front of the layer (moe_forward_norm)"
-        line["norm_step"] = {"us_per_call_without_norm": plain_us, "added_us": us - plain_us,
+        line["norm_step"] = {"us_per_call_without_norm": r["plain_us"], "added_us": us - r["plain_us"],
                              "per_kernel_note": "per_kernel_us and roofline come from the layer's timed "
                                                 "graphs without the norm step"}
     if not args.no_cpu_baseline:

@@ -17,7 +17,8 @@
  *  - Pointers are DEVICE pointers owned by the caller unless stated otherwise.  The
  *    library never allocates or frees device memory on these paths.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
- *    stream) and never synchronise the host, except moe_get_device_status.
+ *    stream) and never synchronise the host, except moe_prepare_weights,
+ *    moe_get_device_status, moe_route_noalloc_status and moe_tensor_peak.
  *  - The return value is a status: MOE_OK (0) or a negative MOE_ERR_* code.  On an
  *    error nothing has been launched unless the code is MOE_ERR_CUDA.
  *  - Shapes: 1 <= T, T * k <= 2^24, H % 32 == 0 with 32 <= H <= 8192, I % 32 == 0
@@ -130,12 +131,24 @@ int moe_route(const uint16_t* x, const uint16_t* w_router, const float* router_b
  *   T must be <= 8192: larger T returns MOE_ERR_UNSUPPORTED_SHAPE.
  *   The first call on a device looks up the array's device address for that
  *   device (once per device, with it current); make that first call before any
- *   stream capture.  Each call clears the counters it uses on `stream` before
- *   launching, so it neither allocates nor needs initialised memory.
+ *   stream capture.  The array is zero when the library loads and every call
+ *   leaves its counters at zero again, so no call clears anything before it
+ *   launches.
  *   All calls share the one array: calls that overlap on the GPU (on different
- *   streams, or from several threads) race and must be serialised by the caller. */
+ *   streams, or from several threads) race and must be serialised by the caller.
+ *   A bounded device wait that gives up sets the array's status word; read it with
+ *   moe_route_noalloc_status (a routing whose status is non-zero is not reliable). */
 int moe_route_noalloc(const uint16_t* x, const uint16_t* w_router, const float* router_bias, int T, int H, int E,
                       int k, float* logits, int flags, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/* moe_route_noalloc_status: the device status of moe_route_noalloc on the current
+ * device.  The pages have no counterpart of it; it is moe_get_device_status for the
+ * fixed array.  Synchronises `stream`, reads the array's status word into *status
+ * (bits as in moe_get_device_status; 0 = healthy) and, when it is non-zero, clears
+ * the whole array, status word and arrival counters alike.  Returns MOE_OK,
+ * MOE_ERR_DEVICE_TIMEOUT when a bit was set, MOE_ERR_INVALID_ARG for a NULL
+ * status, or MOE_ERR_CUDA.  Not for the hot path.                                 */
+int moe_route_noalloc_status(int* status, moe_stream_t stream);
 
 /* moe_build_tile_table: the per-expert tile table of a routing ("Per-expert
  * routing tile table": each expert writes its own tiles).  Atomic-free counting
@@ -260,13 +273,14 @@ int moe_forward(const uint16_t* x, const uint16_t* w_router, const float* router
 /* moe_forward_timed: moe_forward that also records caller-created CUDA events
  * (cudaEvent_t, passed as void*) on `stream` around its MOE_FORWARD_STAGES stages:
  * events[i] just before stage i and events[MOE_FORWARD_STAGES] after the last one.
- * The stages are route + top-k + tile table, the per-token encoding of x (which
- * waits for routing and writes the tile order itself: the permute step), the
- * gate/up + SwiGLU GEMM, and down + combine (two launches).  It gives the
- * per-stage time split ("Where the
- * time went": per-section times of a decode step).  events must hold
- * MOE_FORWARD_STAGES + 1 valid events.                                            */
-#define MOE_FORWARD_STAGES 4
+ * The stages are its five launches: route + top-k + tile table, the per-token
+ * encoding of x (which waits for routing and writes the tile order itself: the
+ * permute step), the gate/up + SwiGLU GEMM, the down GEMM, and the combine.  It
+ * gives the per-launch time split ("Where the time went": per-section times of a
+ * decode step); an event between two launches also separates them, so the
+ * programmatic-launch overlap of consecutive kernels is lost in this form.
+ * events must hold MOE_FORWARD_STAGES + 1 valid events.                          */
+#define MOE_FORWARD_STAGES 5
 int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* router_bias, const void* w_gateup,
                       const void* w_down, int T, int H, int I, int E, int k, void* workspace,
                       size_t workspace_bytes, uint16_t* out, int32_t* topk_idx_out, float* topk_w_out,
@@ -275,6 +289,22 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
 /* Number of kernels moe_forward launches for a shape (for launch accounting):
  * route + top-k + table, encode + permute x, gate/up, down, combine.             */
 int moe_forward_launches(int T, int H, int I, int E, int k);
+
+/* moe_tensor_peak: the measured dense tensor-pipe rate of this GPU, in TFLOP/s, for
+ * one of the MMA forms the expert GEMMs issue, as the roofline peak of the
+ * compute-bound (many-token) workloads.  The pages give no tensor peak for this
+ * hardware; the 4096-token prefill case is to be reported against the MXFP4 rate.
+ *   kind MOE_PEAK_MXF4: tcgen05 kind::mxf4 block-scaled (E2M1 x E2M1, E8M0 scales,
+ *        K = 64 per instruction), the MXFP4 layer's GEMMs;
+ *   kind MOE_PEAK_BF16: kind::f16 (bf16 x bf16, K = 16), the bf16-weight layer.
+ * One CTA per SM issues mmas_per_sm (8 .. 2^24) MMAs of M = 128, N = 256 back to
+ * back into tensor memory; the call times that launch with CUDA events on
+ * `stream`, synchronises it and writes 2*M*N*K*mmas*SMs / time to *tflops.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_CUDA, or MOE_ERR_DEVICE_TIMEOUT when
+ * the bounded completion wait gave up.  Not for the hot path.                      */
+#define MOE_PEAK_MXF4 0
+#define MOE_PEAK_BF16 1
+int moe_tensor_peak(int kind, int mmas_per_sm, double* tflops, moe_stream_t stream);
 
 /* Synchronises `stream`, reads the workspace's device status word into *status
  * (bit 0: main-loop wait timed out, bit 1: epilogue wait timed out, bit 2:

@@ -24,6 +24,8 @@ MOE_WEIGHTS_DOWN = 1
 MOE_ROUTE_FROM_LOGITS = 1
 MOE_ROUTE_GATING_SOFTMAX_ALL = 2
 MOE_ROUTE_GATING_SIGMOID = 4
+MOE_PEAK_MXF4 = 0
+MOE_PEAK_BF16 = 1
 
 # every symbol the header declares, with its C signature
 _P = ctypes.c_void_p
@@ -38,6 +40,7 @@ SIGNATURES = {
     "moe_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P, _S, _P]),
     "moe_route_noalloc": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _I, _P, _P, _P]),
+    "moe_route_noalloc_status": (_I, [ctypes.POINTER(_I), _P]),
     "moe_build_tile_table": (_I, [_P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P]),
     "moe_mxfp4_gateup_swiglu": (_I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _P, _S, _P]),
     "moe_mxfp4_down_combine": (_I, [_P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P]),
@@ -50,6 +53,7 @@ SIGNATURES = {
     "moe_forward_timed": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _S, _P, _P, _P, _P, _P]),
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I]),
     "moe_get_device_status": (_I, [_P, _S, ctypes.POINTER(_I), _P]),
+    "moe_tensor_peak": (_I, [_I, _I, ctypes.POINTER(ctypes.c_double), _P]),
 }
 
 _lib = None
@@ -99,6 +103,7 @@ moe_max_tiles = _call("moe_max_tiles")
 moe_workspace_bytes = _call("moe_workspace_bytes")
 moe_route = _call("moe_route")
 moe_route_noalloc = _call("moe_route_noalloc")
+moe_route_noalloc_status = _call("moe_route_noalloc_status")
 moe_build_tile_table = _call("moe_build_tile_table")
 moe_mxfp4_gateup_swiglu = _call("moe_mxfp4_gateup_swiglu")
 moe_mxfp4_down_combine = _call("moe_mxfp4_down_combine")
@@ -110,3 +115,4 @@ moe_forward_bf16 = _call("moe_forward_bf16")
 moe_forward_timed = _call("moe_forward_timed")
 moe_forward_launches = _call("moe_forward_launches")
 moe_get_device_status = _call("moe_get_device_status")
+moe_tensor_peak = _call("moe_tensor_peak")

@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libmoe_mxfp4.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 
-SOURCES = ["moe_route.cu", "moe_gemm.cu", "moe_aux.cu", "moe_api.cu", "moe_noalloc.cu"]
+SOURCES = ["moe_route.cu", "moe_gemm.cu", "moe_aux.cu", "moe_api.cu", "moe_noalloc.cu", "moe_peak.cu"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "--expt-relaxed-constexpr"]

@@ -150,17 +150,21 @@ cudaError_t record_event(void* ev, cudaStream_t s) {
   return cudaEventRecord(reinterpret_cast<cudaEvent_t>(ev), s);
 }
 
-// One persistent GEMM CTA per SM of the current device (cached per device).
+// One persistent GEMM CTA per SM of the current device (cached per device; every
+// thread computes the same value, so publishing it needs no lock).
 int persistent_ctas() {
-  static int cached[64] = {};
+  static std::atomic<int> cached[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kMaxCtas;
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c) return c;
+  }
   int sms = kMaxCtas;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = kMaxCtas;
   if (sms > kMaxCtas) sms = kMaxCtas;
   if (sms < 1) sms = 1;
-  if (dev >= 0 && dev < 64) cached[dev] = sms;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev].store(sms, std::memory_order_relaxed);
   return sms;
 }
 
@@ -239,9 +243,12 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   return cuda_status(launch_gateup(g, stream));
 }
 
+// The down GEMM (w * y into the slots), then the combine; `between` (may be null) is
+// called after the GEMM's launch and before the combine's.
+template <typename Between>
 int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_tiles, int bm, const float* topk_w,
              const void* w_down, int T, int H, int I, int E, int k, void* ws, const WsLayout& L, uint16_t* out,
-             cudaStream_t stream, const uint16_t* x = nullptr, const uint16_t* residual = nullptr,
+             cudaStream_t stream, Between between, const uint16_t* x = nullptr, const uint16_t* residual = nullptr,
              uint16_t* residual_out = nullptr) {
   const PreparedLayout P = make_prepared_layout(E, H, I, 1);
   GemmParams g{};
@@ -269,6 +276,8 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   g.status = ws_ptr<uint32_t>(ws, L.status);
   int st = cuda_status(launch_down(g, stream));
   if (st != MOE_OK) return st;
+  st = between();
+  if (st != MOE_OK) return st;
   CombineParams c{};
   c.slots = g.slots;
   c.T = T; c.H = H; c.k = k;
@@ -278,6 +287,19 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   c.residual_out = residual_out;
   return cuda_status(launch_combine(c, stream));
 }
+
+}  // namespace
+
+int moe::read_and_clear_status(void* word, size_t clear_bytes, cudaStream_t stream, int* status) {
+  uint32_t h = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&h, word, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (h && cudaMemset(word, 0, clear_bytes) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = (int)h;
+  return h ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+namespace {
 
 static_assert(MOE_ROUTE_FROM_LOGITS == kRouteFlagFromLogits && MOE_ROUTE_GATING_SOFTMAX_ALL == kRouteFlagSoftmaxAll &&
                   MOE_ROUTE_GATING_SIGMOID == kRouteFlagSigmoid,
@@ -434,7 +456,7 @@ int moe_mxfp4_down_combine(const int32_t* perm, const int32_t* tiles, const int3
   const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   return run_down(perm, reinterpret_cast<const TileEntry*>(tiles), num_tiles, bm, topk_w, w_down, T, H, I, E, k,
-                  workspace, L, out, reinterpret_cast<cudaStream_t>(stream));
+                  workspace, L, out, reinterpret_cast<cudaStream_t>(stream), [] { return MOE_OK; });
 }
 
 int moe_hidden_dequant(const int32_t* perm, const int32_t* tiles, const int32_t* num_tiles, int tile_rows, int T,
@@ -498,8 +520,8 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
     if (events && record_event(events[i], s) != cudaSuccess) ev_ok = false;
   };
   // stages: [0] route + top-k + tile table, [1] encode + permute x, [2] gate/up,
-  // [3] down + combine.  Routing goes first (it waits for the previous kernel); the
-  // encoding overlaps it, waits for it at its end and writes the tile order.
+  // [3] down, [4] combine.  Routing goes first (it waits for the previous kernel);
+  // the encoding overlaps it, waits for it at its end and writes the tile order.
   mark(0);
   if (!ev_ok) return MOE_ERR_INVALID_ARG;
   if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -510,9 +532,13 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   st = run_gateup(perm, tiles, num_tiles, bm, w_gateup, T, H, I, E, k, ws, L, s);
   if (st != MOE_OK) return st;
   mark(3);
-  st = run_down(perm, tiles, num_tiles, bm, w, w_down, T, H, I, E, k, ws, L, out, s, x, norm.residual,
-                residual_out);
-  mark(4);
+  st = run_down(perm, tiles, num_tiles, bm, w, w_down, T, H, I, E, k, ws, L, out, s,
+                [&] {
+                  mark(4);
+                  return ev_ok ? MOE_OK : MOE_ERR_INVALID_ARG;
+                },
+                x, norm.residual, residual_out);
+  mark(5);
   return st;
 }
 
@@ -672,13 +698,7 @@ int moe_forward_launches(int T, int H, int I, int E, int k) {
 
 int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream) {
   if (!workspace || !status || workspace_bytes < 256) return MOE_ERR_INVALID_ARG;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint32_t h = 0;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemcpy(&h, workspace, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (h && cudaMemset(workspace, 0, 256) != cudaSuccess) return MOE_ERR_CUDA;
-  *status = (int)h;
-  return h ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+  return read_and_clear_status(workspace, 256, reinterpret_cast<cudaStream_t>(stream), status);
 }
 
 }  // extern "C"

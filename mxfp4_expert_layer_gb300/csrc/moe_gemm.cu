@@ -601,16 +601,9 @@ template <int BM, bool GATEUP, bool MPAIR, bool W16>
 static cudaError_t launch_gemm_t(const GemmParams& p, cudaStream_t stream) {
   using C = GemmCfg<BM, GATEUP, MPAIR, W16>;
   auto kern = moe_gemm_kernel<BM, GATEUP, MPAIR, W16>;
-  // the shared-memory opt-in is a per-device function attribute: set it once per device
-  static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemOptIn opt_in;
+  const cudaError_t e = opt_in.ensure(kern, C::kSmemBytes);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
   return launch_pdl(kern, dim3(p.grid), dim3(C::kThreads), C::kSmemBytes, stream, p);
 }
 

@@ -3,10 +3,40 @@
 
 #include <cuda.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "moe_common.cuh"
 #include "moe_norm.cuh"
 
 namespace moe {
+
+constexpr int kMaxDevices = 64;  // devices with a per-device host-side cache entry
+
+// Raises a kernel's dynamic shared-memory limit on the current device to at least
+// `bytes`.  The limit is a per-device function attribute, so it is set once per
+// device and increase.  Host threads making their first calls at the same time are
+// serialised by a lock; later calls read the published value without it.
+class SmemOptIn {
+ public:
+  template <typename Kern>
+  cudaError_t ensure(Kern kern, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (done_[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done_[dev].store(bytes, std::memory_order_release);
+    return e;
+  }
+
+ private:
+  std::atomic<int> done_[kMaxDevices] = {};
+  std::mutex mu_;
+};
 
 // Launches `kern` with programmatic stream serialization: it may begin while the
 // previous kernel on the stream finishes; the kernel itself waits (pdl_wait) before
@@ -26,6 +56,12 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
+
+// Synchronises `stream`, reads the device status word at `word` (a device address)
+// into *status and, when it is non-zero, zero-fills `clear_bytes` bytes from `word`
+// (the word itself and whatever the timed-out kernels may have left behind).
+// Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a bit was set) or MOE_ERR_CUDA.
+int read_and_clear_status(void* word, size_t clear_bytes, cudaStream_t stream, int* status);
 
 // Route flags (the public MOE_ROUTE_* values) -> gating variant, or -1 for a bad set.
 constexpr int kRouteFlagFromLogits = 1, kRouteFlagSoftmaxAll = 2, kRouteFlagSigmoid = 4;

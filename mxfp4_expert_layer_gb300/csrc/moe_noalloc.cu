@@ -10,7 +10,10 @@
 // library instead, so the caller passes only inputs and outputs.
 //
 // The array lives in every GPU that loads the library, for the life of the
-// process: kNoAllocScratchBytes bytes, enough for T <= kNoAllocMaxTokens.
+// process: kNoAllocScratchBytes bytes, enough for T <= kNoAllocMaxTokens.  It is
+// zero when the library is loaded; every routing call leaves its counters at zero
+// again, and moe_route_noalloc_status clears the whole array after a reported
+// timeout (a kernel that gave up may have left a counter behind).
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -21,7 +24,6 @@
 namespace {
 
 constexpr int kNoAllocMaxTokens = 8192;
-constexpr int kNoAllocMaxDevices = 64;
 // status word (256 bytes) + one arrival counter per group of 8 tokens + the table counter
 constexpr size_t kNoAllocScratchBytes = 256 + sizeof(uint32_t) * (kNoAllocMaxTokens / 8 + 1);
 
@@ -31,13 +33,13 @@ static __device__ __align__(256) uint8_t g_route_scratch[kNoAllocScratchBytes];
 // code the name g_route_scratch is only a host-side stand-in for the symbol; the
 // kernel must be given the address cudaGetSymbolAddress returns for the current
 // device.
-void* g_scratch_addr[kNoAllocMaxDevices] = {};
+void* g_scratch_addr[moe::kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
 int scratch_for_current_device(uint8_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (dev < 0 || dev >= moe::kMaxDevices) return MOE_ERR_UNSUPPORTED_SHAPE;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
@@ -69,9 +71,8 @@ extern "C" int moe_route_noalloc(const uint16_t* x, const uint16_t* w_router, co
   int st = scratch_for_current_device(&scratch);
   if (st != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // every call shares the array: the arrival counters must start at zero
-  const size_t used = 256 + sizeof(uint32_t) * (size_t)(ceil_div(T, 8) + 1);
-  if (cudaMemsetAsync(scratch, 0, used, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // The arrival counters are zero here: zero at load, and reset by the last arriver
+  // of every call (after a timeout, moe_route_noalloc_status clears them).
   RouteParams r{};
   r.x = x;
   r.w_router = w_router;
@@ -87,4 +88,12 @@ extern "C" int moe_route_noalloc(const uint16_t* x, const uint16_t* w_router, co
   r.status = reinterpret_cast<uint32_t*>(scratch);
   r.build_table = 0;
   return launch_route(r, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" int moe_route_noalloc_status(int* status, moe_stream_t stream) {
+  if (!status) return MOE_ERR_INVALID_ARG;
+  uint8_t* scratch = nullptr;
+  const int st = scratch_for_current_device(&scratch);
+  if (st != MOE_OK) return st;
+  return moe::read_and_clear_status(scratch, kNoAllocScratchBytes, reinterpret_cast<cudaStream_t>(stream), status);
 }

@@ -964,25 +964,34 @@ static bool use_cluster_route(const RouteParams& p, size_t* smem_out) {
   if (p.from_logits || p.T > kClusterMaxTokens) return false;
   const ClusterRouteSmem L = cluster_route_smem(p.T, p.H, p.E, p.k, p.norm.norm_w != nullptr);
   if (L.total > kClusterSmemCap) return false;
-  static int state[64] = {};  // 0 unknown, 1 usable, -1 not
+  // per device: 0 not probed yet, 1 usable, -1 not.  The probe runs under a lock and
+  // its result is published once, so concurrent first calls all see the same answer.
+  static std::atomic<int> state[kMaxDevices] = {};
+  static std::mutex mu;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  if (state[dev] == 0) {
-    state[dev] = -1;
-    if (cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterSmemCap) ==
-        cudaSuccess) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(kClusterCtas);
-      cfg.blockDim = dim3(kRouteThreads);
-      cfg.dynamicSmemBytes = kClusterSmemCap;
-      int clusters = 0;
-      if (cudaOccupancyMaxActiveClusters(&clusters, route_cluster_kernel, &cfg) == cudaSuccess && clusters > 0)
-        state[dev] = 1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  int st = state[dev].load(std::memory_order_acquire);
+  if (st == 0) {
+    std::lock_guard<std::mutex> lock(mu);
+    st = state[dev].load(std::memory_order_relaxed);
+    if (st == 0) {
+      st = -1;
+      if (cudaFuncSetAttribute(route_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kClusterSmemCap) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kClusterCtas);
+        cfg.blockDim = dim3(kRouteThreads);
+        cfg.dynamicSmemBytes = kClusterSmemCap;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, route_cluster_kernel, &cfg) == cudaSuccess && clusters > 0)
+          st = 1;
+      }
+      cudaGetLastError();  // a refused query leaves no sticky error
+      state[dev].store(st, std::memory_order_release);
     }
-    cudaGetLastError();  // a refused query leaves no sticky error
   }
   *smem_out = L.total;
-  return state[dev] == 1;
+  return st == 1;
 }
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
@@ -992,15 +1001,9 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
   if (!p.from_logits) {
     // many tokens: tensor-core logits, 32 tokens per block
     const MmaRouteSmem L = mma_route_smem(p.E, p.norm.norm_w != nullptr);
-    static int configured[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    static SmemOptIn opt_in;
+    const cudaError_t e = opt_in.ensure(route_mma_kernel, (int)L.total);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || configured[dev] < (int)L.total) {
-      e = cudaFuncSetAttribute(route_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
-      if (e != cudaSuccess) return e;
-      if (dev >= 0 && dev < 64) configured[dev] = (int)L.total;
-    }
     return launch_pdl(route_mma_kernel, dim3(ceil_div(p.T, kMmaTokens)), dim3(kRouteThreads), L.total, stream, p);
   }
   const int groups = ceil_div(p.T, kTokensPerGroup);
@@ -1008,16 +1011,10 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t stream) {
   const size_t smem = p.from_logits ? 0 : (size_t)kTokensPerGroup * p.H * sizeof(uint16_t);
   // static (tile-table scratch) + dynamic (activation tile) shared memory may exceed
   // the 48 KB default window
-  static int configured_smem[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemOptIn opt_in12, opt_in4;
+  cudaError_t e = opt_in12.ensure(route_kernel<12>, (int)smem);
+  if (e == cudaSuccess) e = opt_in4.ensure(route_kernel<4>, (int)smem);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64 || configured_smem[dev] < (int)smem) {
-    e = cudaFuncSetAttribute(route_kernel<12>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(route_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured_smem[dev] = (int)smem;
-  }
   if (p.T <= 64) return launch_pdl(route_kernel<12>, grid, dim3(kRouteThreads), smem, stream, p);
   return launch_pdl(route_kernel<4>, grid, dim3(kRouteThreads), smem, stream, p);
 }

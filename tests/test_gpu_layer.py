@@ -9,7 +9,8 @@ import pytest
 
 import oracle
 from synthetic import make_config, make_layer, make_norm_inputs
-from tests.gpu_helpers import TOL_MAX_ABS, TOL_REL_FROB, bf16_bits_to_f32, bf16_to_np, build_layer, errors, to_dev
+from tests.gpu_helpers import (TOL_MAX_ABS, TOL_REL_FROB, bf16_bits_to_f32, bf16_to_np, build_layer, errors,
+                               logit_band, tile_edge_tokens, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -91,17 +92,22 @@ def run_layer(inp, tokens=None, gating=0):
 GATING_OF_FLAG = {0: 0, 2: 1, 4: 2}  # MOE_ROUTE_GATING_* flag -> oracle gating variant
 
 
-def check_layer(inp, tokens=None, margin=1e-4, gating=0):
+def check_layer(inp, tokens=None, gating=0, band=None, min_kept=0.9):
+    """The layer's output and routing against the oracle on `tokens` (default all).
+    Tokens whose oracle top-k margin lies inside the near-tie band are left out of
+    the comparison; the band comes from the router logit error measured on this
+    input (gpu_helpers.logit_band) unless one is given."""
     layer, out, idx, w = run_layer(inp, gating=gating)
     ref = oracle.moe_layer(inp, tokens=tokens, gating=GATING_OF_FLAG[gating])
     tok = ref["tokens"]
-    # compare tokens whose routing is not a near tie under fp32 logit rounding
-    keep = oracle.topk_margin(ref["logits"], inp.k) > margin
-    assert keep.mean() > 0.9
+    if band is None:
+        band, _ = logit_band(inp)
+    keep = oracle.topk_margin(ref["logits"], inp.k) > band
+    assert keep.mean() >= min_kept, (keep.mean(), band)
     assert np.array_equal(idx[tok][keep], ref["idx"][keep])
     rel, mx = errors(out[tok][keep], ref["out"][keep])
     assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)
-    return rel, mx
+    return rel, mx, idx
 
 
 def test_layer_tiny():
@@ -126,13 +132,63 @@ def test_layer_gptoss120b_b1():
     check_layer(make_config("gptoss120b_b1"))
 
 
-def test_layer_gptoss120b_b64_sampled():
-    check_layer(make_config("gptoss120b_b64"), tokens=np.arange(0, 64, 4))
+def test_layer_gptoss120b_b64():
+    check_layer(make_config("gptoss120b_b64"))
 
 
-def test_layer_gptoss120b_prefill4096_sampled():
+def test_layer_gptoss120b_prefill4096_every_tile():
+    """4096 tokens with the Zipf router bias: the oracle checks the tokens at the
+    first and the last row of every tile the GPU's routing produced (hot experts'
+    full 128-row tiles and every partial last tile), plus a random sample."""
     inp = make_config("gptoss120b_prefill4096")
-    check_layer(inp, tokens=np.random.default_rng(0).choice(inp.T, 24, replace=False))
+    layer, out, idx, w = run_layer(inp)
+    bm = oracle.tile_rows_policy(inp.T, inp.k, inp.E)
+    tab = oracle.tile_table(idx, inp.E, bm)
+    assert tab["num_tiles"] > inp.E // 2 and np.max(tab["counts"]) > 4 * bm  # skewed: several hot experts
+    tokens = np.union1d(tile_edge_tokens(idx, inp.E, bm), np.random.default_rng(0).choice(inp.T, 32, replace=False))
+    ref = oracle.moe_layer(inp, tokens=tokens)
+    band, _ = logit_band(inp)
+    keep = oracle.topk_margin(ref["logits"], inp.k) > band
+    assert keep.mean() >= 0.9, (keep.mean(), band)
+    assert np.array_equal(idx[tokens][keep], ref["idx"][keep])
+    # every tile keeps at least one compared token at one of its edges
+    kept = set(tokens[keep].tolist())
+    for e, s0, n, _ in tab["tiles"]:
+        edge = {int(tab["perm"][s0]) // inp.k, int(tab["perm"][s0 + n - 1]) // inp.k}
+        assert edge & kept, (e, s0, n)
+    rel, mx = errors(out[tokens][keep], ref["out"][keep])
+    assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)
+
+
+def with_outliers(inp, factors=(100.0, 1000.0), fixed_channels=False, seed=0):
+    """x with a heavy tail: in every 32-value block of every row, one element scaled
+    by each of `factors` -- at random positions, or (fixed_channels) at the same
+    channels for every token, as massive activations sit in fixed channels."""
+    import dataclasses
+    from synthetic import bf16_bits_from_f32
+    rng = np.random.default_rng(seed)
+    x = oracle.bf16_to_f32(inp.x).copy()
+    T, H = x.shape
+    for b in range(H // 32):
+        fixed = rng.choice(32, len(factors), replace=False)
+        for t in range(T):
+            pos = fixed if fixed_channels else rng.choice(32, len(factors), replace=False)
+            for f, q in zip(factors, pos):
+                x[t, b * 32 + q] *= f
+    return dataclasses.replace(inp, x=bf16_bits_from_f32(x))
+
+
+@pytest.mark.parametrize("name", ["tiny", "gptoss20b_b64"])
+@pytest.mark.parametrize("fixed", [False, True], ids=["random_positions", "fixed_channels"])
+def test_layer_heavy_tailed_activations(name, fixed):
+    """One x100 and one x1000 element in every 32-value block.  Each E2M1 term of the
+    activation encoding is scaled to its block's largest residual, so the other values
+    of such a block keep less relative precision (about 1e-2 of their block's
+    non-outlier maximum after four terms, against about 1e-4 without outliers); with
+    the expert weights as drawn the outliers dominate every dot product and the layer
+    stays within the tolerance."""
+    rel, mx, _ = check_layer(with_outliers(make_config(name), fixed_channels=fixed))
+    print(f"{name} heavy-tailed x ({'fixed channels' if fixed else 'random positions'}): rel {rel:.2e} max {mx:.2e}")
 
 
 @pytest.mark.parametrize("T,H,I,E,k", [(200, 256, 256, 16, 2),    # 64-row tiles, ragged tails
@@ -212,7 +268,7 @@ def test_consecutive_calls_with_new_routing(name):
     assert layer.device_status(base.T) == 0
     for inp, out in zip(inps, outs):
         ref = oracle.moe_layer(inp)
-        keep = oracle.topk_margin(ref["logits"], inp.k) > 1e-4
+        keep = oracle.topk_margin(ref["logits"], inp.k) > logit_band(inp)[0]
         rel, mx = errors(bf16_bits_to_f32(bf16_to_np(out))[keep], ref["out"][keep])
         assert rel <= TOL_REL_FROB and mx <= TOL_MAX_ABS, (rel, mx)
 
@@ -237,7 +293,8 @@ def test_layer_norm_residual(name, T):
     ref = oracle.moe_layer_norm(inp, r, g, eps)
     assert np.array_equal(bf16_to_np(res_out), ref["residual_out"])
     got = bf16_bits_to_f32(bf16_to_np(out))
-    keep = oracle.topk_margin(ref["logits"], inp.k) > 1e-4
+    # the router's input is y: the band comes from the router error measured on the oracle's y
+    keep = oracle.topk_margin(ref["logits"], inp.k) > logit_band(inp, x_bits=ref["x_norm"])[0]
     assert keep.mean() > 0.9
     assert np.array_equal(idx.cpu().numpy()[keep], ref["idx"][keep])
     rel, mx = errors(got[keep], ref["out"][keep])

@@ -71,9 +71,10 @@ def test_router_logits_and_selection(api, name, T):
     wa = np.abs(oracle.bf16_to_f32(inp.w_router)).astype(np.float64)
     bound = inp.H * 2.0 ** -24 * (xa @ wa.T) + 1e-6
     assert np.all(np.abs(got - ref) <= bound)
-    # selections agree wherever the top-k margin exceeds the logit error
+    # selections agree wherever the top-k margin exceeds twice the largest logit error
+    # (band: four times the error measured here, at least 1e-6)
     margin = oracle.topk_margin(ref, inp.k)
-    ok = margin > 1e-4
+    ok = margin > max(4.0 * float(np.abs(got.astype(np.float64) - ref).max()), 1e-6)
     ref_idx, ref_w = oracle.topk_softmax(ref, inp.k)
     assert np.array_equal(idx.cpu().numpy()[ok], ref_idx[ok])
     np.testing.assert_allclose(w.cpu().numpy()[ok], ref_w[ok], rtol=1e-4, atol=1e-6)

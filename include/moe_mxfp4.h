@@ -309,7 +309,9 @@ int moe_tensor_peak(int kind, int mmas_per_sm, double* tflops, moe_stream_t stre
 /* Synchronises `stream`, reads the workspace's device status word into *status
  * (bit 0: main-loop wait timed out, bit 1: epilogue wait timed out, bit 2:
  * producer wait timed out; 0 = healthy) and clears it.  Returns MOE_OK, or
- * MOE_ERR_DEVICE_TIMEOUT when any bit was set.  Not for the hot path.              */
+ * MOE_ERR_DEVICE_TIMEOUT when any bit was set.  After a timeout the call's outputs
+ * are not reliable and the workspace's arrival counters may be left non-zero:
+ * zero-fill the workspace again before its next use.  Not for the hot path.        */
 int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream);
 
 #ifdef __cplusplus

@@ -60,7 +60,14 @@ struct GemmCfg {
   static constexpr bool kConcat = !W16 && kTerms * BM <= 64; // all terms in one MMA along N
   static constexpr int kN = kConcat ? kTerms * BM : BM;      // MMA N
   static constexpr int kAccN = kN;                           // accumulator columns per weight tile
-  static constexpr int kAccCols = kA * kAccN;
+  // Decode stages that carry one weight tile (the unpaired down GEMM, 16-row tiles):
+  // the stage's two K groups go to two MMA-issuing threads, each with its own scale
+  // copies and its own accumulator slice, and the epilogue adds the two slices.  One
+  // thread then issues half the tcgen05 instructions of a stage; at these shapes the
+  // issuing thread, not the tensor pipe or the copies, sets the stage rate.
+  static constexpr bool kSplitK = !W16 && kA == 1 && kConcat;
+  static constexpr int kAccSlices = kSplitK ? 2 : kA;       // accumulator slices per buffer
+  static constexpr int kAccCols = kAccSlices * kAccN;
   static constexpr int kVals = kA * BM;                      // values per row after summing terms
   static constexpr int kBRows = kRowTerms * BM;              // B tile rows (terms x token rows)
   static constexpr int kBBytes = kBRows * kKBytes;
@@ -86,9 +93,10 @@ struct GemmCfg {
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
   static constexpr uint32_t kTxNoB = kA * kATileBytes + kSfBytes;                // all but the B codes
   // MMA issuers: with two weight tiles per stage each of two threads issues one
-  // tile's MMAs (its own accumulator, scale copies and B scale columns)
-  static constexpr int kIssuers = kA;
-  static constexpr int kSfColsPerStage = 4 * (kA + kIssuers * kNbAtoms) * kAtoms;
+  // tile's MMAs (its own accumulator, scale copies and B scale columns); with split K
+  // groups each issues one K group's (the B scale atoms are then not duplicated)
+  static constexpr int kIssuers = kSplitK ? 2 : kA;
+  static constexpr int kSfColsPerStage = 4 * (kA + (kSplitK ? 1 : kIssuers) * kNbAtoms) * kAtoms;
   static constexpr int kSfCols = kStages * kSfColsPerStage;
   static constexpr int kNumAcc = (2 * kAccCols + kSfCols <= 512) ? 2 : 1;
   static constexpr int kTmemNeed = kNumAcc * kAccCols + kSfCols;
@@ -310,9 +318,23 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
     pdl_wait();
     const int issuer = warp == 1 ? 0 : 1;
     if (lane == 0 && issuer < C::kIssuers) {
-      // this thread's weight tiles j in [j0, j1)
-      const int j0 = C::kIssuers == 2 ? issuer : 0, j1 = C::kIssuers == 2 ? issuer + 1 : C::kA;
+      // this thread's weight tiles [j0, j1) and K steps [ks0, ks1) of every stage
+      constexpr bool kTilePerIssuer = C::kIssuers == 2 && !C::kSplitK;
+      const int j0 = kTilePerIssuer ? issuer : 0, j1 = kTilePerIssuer ? issuer + 1 : C::kA;
+      const int ks0 = C::kSplitK ? issuer * (C::kKSteps / 2) : 0;
+      const int ks1 = C::kSplitK ? ks0 + C::kKSteps / 2 : C::kKSteps;
+      const int at0 = ks0 >> 1, at1 = (ks1 + 1) >> 1;  // K groups (scale atoms) of those steps
+      const uint32_t acc_slice = C::kSplitK ? issuer * C::kAccN : 0u;
       const uint32_t sf_col0 = C::kNumAcc * C::kAccCols;
+      // shared-memory addresses of stage 0's parts; stage s adds s * kStageBytes
+      const uint32_t a_addr0 = smem_u32(a_tile(0, 0));
+      const uint32_t b_addr0 = smem_u32(b_tile(0));
+      const uint32_t sfa_addr0 = smem_u32(sf_a(0, 0));
+      const uint32_t sfb_addr0 = smem_u32(sf_b(0));
+      // operand rows are kKBytes long (64-byte swizzle for 64, 128-byte for 128)
+      auto kdesc = [](uint32_t saddr) {
+        return C::kKBytes == 128 ? smem_desc_kmajor_sw128(saddr) : smem_desc_kmajor_sw64(saddr);
+      };
       int g = 0;
       bool err = false;
       for (int si = 0; si < sch.nseg && !err; ++si) {
@@ -326,7 +348,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t acc_base = tmem + b * C::kAccCols;
+        const uint32_t acc_base = tmem + b * C::kAccCols + acc_slice;
         bool seg_first = true;
         for (int kk = kk0; kk < kk1; ++kk, ++g) {
           const int s = g % C::kStages;
@@ -338,52 +360,52 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
             break;
           }
           tc_fence_after();
+          const uint32_t so = (uint32_t)s * C::kStageBytes;
           if constexpr (W16) {
             // bf16 x bf16: four K = 16 steps per 128-byte stage row, no scales
             constexpr uint32_t idesc16 = idesc_bf16(kMTile, C::kN);
             for (int ks = 0; ks < C::kKSteps; ++ks) {
-              const uint64_t bdesc = smem_desc_kmajor_sw128(smem_u32(b_tile(s)) + 32 * ks);
+              const uint64_t bdesc = smem_desc_kmajor_sw128(b_addr0 + so + 32 * ks);
               const uint32_t acc = seg_first ? 0u : 1u;
               for (int j = j0; j < j1; ++j)
-                mma_bf16(acc_base + j * C::kAccN, smem_desc_kmajor_sw128(smem_u32(a_tile(s, j)) + 32 * ks), bdesc,
-                         idesc16, acc);
+                mma_bf16(acc_base + j * C::kAccN, smem_desc_kmajor_sw128(a_addr0 + so + j * C::kATileBytes + 32 * ks),
+                         bdesc, idesc16, acc);
               seg_first = false;
             }
             mma_commit(&empty_bar[s]);
             continue;
           }
           const uint32_t sfc = tmem + sf_col0 + s * C::kSfColsPerStage;
-          // this issuer's copy of the B scale atoms
-          const uint32_t sfb0 = sfc + 4 * C::kA * C::kAtoms + issuer * 4 * C::kNbAtoms * C::kAtoms;
+          // this issuer's copy of the B scale atoms (one shared copy with split K groups)
+          const uint32_t sfb0 = sfc + 4 * C::kA * C::kAtoms + (C::kSplitK ? 0 : issuer * 4 * C::kNbAtoms * C::kAtoms);
           // scale atoms -> tensor memory (32 rows x 16 bytes, replicated to 4 lane quarters):
           // A tile j, K group a at columns 4 (j kAtoms + a); B atom (a, q) at 4 (a kNbAtoms + q)
-          for (int i = j0 * C::kAtoms; i < j1 * C::kAtoms; ++i)
-            tmem_cp_32x128b_warpx4(sfc + 4 * i, smem_desc(smem_u32(sf_a(s, 0)) + i * kSfAtomBytes, 0, 128, 0));
-          for (int i = 0; i < C::kAtoms * C::kNbAtoms; ++i)
-            tmem_cp_32x128b_warpx4(sfb0 + 4 * i, smem_desc(smem_u32(sf_b(s)) + i * kSfAtomBytes, 0, 128, 0));
-          // operand rows are kKBytes long (64-byte swizzle for 64, 128-byte for 128)
-          auto kdesc = [&](uint32_t saddr) {
-            return C::kKBytes == 128 ? smem_desc_kmajor_sw128(saddr) : smem_desc_kmajor_sw64(saddr);
-          };
-          for (int ks = 0; ks < C::kKSteps; ++ks) {  // K = 64 steps: 32 bytes of every operand row
+          for (int j = j0; j < j1; ++j)
+            for (int a = at0; a < at1; ++a) {
+              const int i = j * C::kAtoms + a;
+              tmem_cp_32x128b_warpx4(sfc + 4 * i, smem_desc(sfa_addr0 + so + i * kSfAtomBytes, 0, 128, 0));
+            }
+          for (int i = at0 * C::kNbAtoms; i < at1 * C::kNbAtoms; ++i)
+            tmem_cp_32x128b_warpx4(sfb0 + 4 * i, smem_desc(sfb_addr0 + so + i * kSfAtomBytes, 0, 128, 0));
+          for (int ks = ks0; ks < ks1; ++ks) {  // K = 64 steps: 32 bytes of every operand row
             if (kk * (C::kKStage / kMxBlock) + 2 * ks >= kblocks) break;  // both MX blocks are padding
             const int a = ks >> 1;                    // K group (scale atom) of this step
             const uint32_t idesc = idesc_mxf4(kMTile, C::kN, 2 * (ks & 1), 2 * (ks & 1));
             if constexpr (C::kConcat) {
-              const uint64_t bdesc = kdesc(smem_u32(b_tile(s)) + 32 * ks);
+              const uint64_t bdesc = kdesc(b_addr0 + so + 32 * ks);
               const uint32_t acc = seg_first ? 0u : 1u;
               for (int j = j0; j < j1; ++j) {
-                const uint64_t adesc = kdesc(smem_u32(a_tile(s, j)) + 32 * ks);
+                const uint64_t adesc = kdesc(a_addr0 + so + j * C::kATileBytes + 32 * ks);
                 mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
                          sfb0 + 4 * a * C::kNbAtoms, acc);
               }
             } else {
               for (int t = 0; t < kTerms; ++t) {
-                const uint64_t bdesc = kdesc(smem_u32(b_tile(s)) + t * BM * C::kKBytes + 32 * ks);
+                const uint64_t bdesc = kdesc(b_addr0 + so + t * BM * C::kKBytes + 32 * ks);
                 const uint32_t sfb = sfb0 + 4 * a * C::kNbAtoms + (t * BM) / 32;
                 const uint32_t acc = (seg_first && t == 0) ? 0u : 1u;
                 for (int j = j0; j < j1; ++j) {
-                  const uint64_t adesc = kdesc(smem_u32(a_tile(s, j)) + 32 * ks);
+                  const uint64_t adesc = kdesc(a_addr0 + so + j * C::kATileBytes + 32 * ks);
                   mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a), sfb, acc);
                 }
               }
@@ -408,6 +430,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
     auto epi_bar = [eg]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + eg) : "memory"); };
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int i_pad = (p.I + 63) / 64 * 64;  // h features written (zeros past I)
+    const bool split_live = p.K > 2 * 2 * kMxBlock;  // the second issuer's K group holds data
     for (int si = 0; si < sch.nseg; ++si) {
       int u, kk0, kk1, tile, mt;
       bool whole;
@@ -553,13 +576,19 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         for (int j = 0; j < C::kA; ++j)
 #pragma unroll
           for (int c = 0; c < BM; ++c) {
+            // split K groups: the two slices hold partial sums of the same products (the
+            // second one only when K reaches past the first K group of 128)
+            auto col = [&](int i) {
+              return C::kSplitK ? acc[j * C::kAccN + i] + (split_live ? acc[C::kAccN + i] : 0.f)
+                                : acc[j * C::kAccN + i];
+            };
             float v;
             if constexpr (C::kConcat) {
-              v = acc[j * C::kAccN + kTerms * c];
+              v = col(kTerms * c);
 #pragma unroll
-              for (int t = 1; t < kTerms; ++t) v += acc[j * C::kAccN + kTerms * c + t];
+              for (int t = 1; t < kTerms; ++t) v += col(kTerms * c + t);
             } else {
-              v = acc[j * C::kAccN + c];
+              v = col(c);
             }
             vals[j * BM + c] = v;
           }

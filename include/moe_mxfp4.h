@@ -306,6 +306,17 @@ int moe_forward_launches(int T, int H, int I, int E, int k);
 #define MOE_PEAK_BF16 1
 int moe_tensor_peak(int kind, int mmas_per_sm, double* tflops, moe_stream_t stream);
 
+/* moe_set_wait_limit_ns: how long (ns) each pipeline wait of the expert GEMMs may
+ * take before it gives up, for launches made after the call (process-wide; 0
+ * restores the default of 1 s; at most 10 s, else MOE_ERR_INVALID_ARG).  A wait
+ * that gives up sets a bit of the workspace status word (moe_get_device_status), the
+ * kernel drops its remaining work, waits (up to 1 s) for the copies and tensor-core
+ * operations it has already issued, frees its tensor memory and exits: no trap, and
+ * the context stays usable.  A limit shorter than the pipeline's own latency (a few
+ * microseconds) makes waits give up on ordinary calls; that is how failure detection
+ * is tested.  The pages have no counterpart of it.                                 */
+int moe_set_wait_limit_ns(unsigned long long ns);
+
 /* Synchronises `stream`, reads the workspace's device status word into *status
  * (bit 0: main-loop wait timed out, bit 1: epilogue wait timed out, bit 2:
  * producer wait timed out; 0 = healthy) and clears it.  Returns MOE_OK, or

@@ -54,6 +54,7 @@ SIGNATURES = {
     "moe_forward_launches": (_I, [_I, _I, _I, _I, _I]),
     "moe_get_device_status": (_I, [_P, _S, ctypes.POINTER(_I), _P]),
     "moe_tensor_peak": (_I, [_I, _I, ctypes.POINTER(ctypes.c_double), _P]),
+    "moe_set_wait_limit_ns": (_I, [ctypes.c_ulonglong]),
 }
 
 _lib = None
@@ -116,3 +117,4 @@ moe_forward_timed = _call("moe_forward_timed")
 moe_forward_launches = _call("moe_forward_launches")
 moe_get_device_status = _call("moe_get_device_status")
 moe_tensor_peak = _call("moe_tensor_peak")
+moe_set_wait_limit_ns = _call("moe_set_wait_limit_ns")

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -240,6 +241,7 @@ int run_gateup(const int32_t* perm, const TileEntry* tiles, const int32_t* num_t
   g.kg_out = L.kg_i;
   g.grid = persistent_ctas();
   g.status = ws_ptr<uint32_t>(ws, L.status);
+  g.wait_ns = gemm_wait_limit_ns();
   return cuda_status(launch_gateup(g, stream));
 }
 
@@ -274,6 +276,7 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
   g.slots = ws_ptr<float>(ws, L.slots);
   g.grid = persistent_ctas();
   g.status = ws_ptr<uint32_t>(ws, L.status);
+  g.wait_ns = gemm_wait_limit_ns();
   int st = cuda_status(launch_down(g, stream));
   if (st != MOE_OK) return st;
   st = between();
@@ -289,6 +292,13 @@ int run_down(const int32_t* perm, const TileEntry* tiles, const int32_t* num_til
 }
 
 }  // namespace
+
+namespace {
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+}  // namespace
+
+uint64_t moe::gemm_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
 int moe::read_and_clear_status(void* word, size_t clear_bytes, cudaStream_t stream, int* status) {
   uint32_t h = 0;
@@ -642,6 +652,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
   g.h_q = ws_ptr<uint8_t>(ws, L.h_q);
   g.grid = persistent_ctas();
   g.status = ws_ptr<uint32_t>(ws, L.status);
+  g.wait_ns = gemm_wait_limit_ns();
   st = cuda_status(launch_gateup(g, s));
   if (st != MOE_OK) return st;
 
@@ -673,6 +684,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
   d.slots = ws_ptr<float>(ws, L.slots);
   d.grid = persistent_ctas();
   d.status = ws_ptr<uint32_t>(ws, L.status);
+  d.wait_ns = gemm_wait_limit_ns();
   st = cuda_status(launch_down(d, s));
   if (st != MOE_OK) return st;
   CombineParams c{};
@@ -694,6 +706,12 @@ int moe_forward_timed(const uint16_t* x, const uint16_t* w_router, const float* 
 int moe_forward_launches(int T, int H, int I, int E, int k) {
   if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
   return 5;  // route + table, encode + permute x, gate/up, down, combine
+}
+
+int moe_set_wait_limit_ns(unsigned long long ns) {
+  if (ns > 10ull * kDefaultWaitNs) return MOE_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns ? (uint64_t)ns : kDefaultWaitNs, std::memory_order_relaxed);
+  return MOE_OK;
 }
 
 int moe_get_device_status(void* workspace, size_t workspace_bytes, int* status, moe_stream_t stream) {

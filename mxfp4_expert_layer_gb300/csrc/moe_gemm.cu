@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
   uint64_t* empty_bar = full_bar + C::kStages;
   uint64_t* accf_bar = empty_bar + C::kStages;   // [2] accumulator ready
   uint64_t* acce_bar = accf_bar + 2;             // [2] accumulator drained
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce_bar + 2);
+  uint64_t* drain_bar = acce_bar + 2;            // every MMA issuer's tensor-core work has completed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   int* s_flags = reinterpret_cast<int*>(tmem_slot + 4);  // [0] error, [1] unit finisher
   // per epilogue group: h transpose [16][128], row assignment [128], its top-k weight [128]
   uint8_t* epi_smem = smem + C::kStages * C::kStageBytes + C::kBarBytes;
@@ -176,6 +177,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
       mbar_init(&accf_bar[b], C::kIssuers);
       mbar_init(&acce_bar[b], 128 * C::kEpiGroups);
     }
+    mbar_init(drain_bar, C::kIssuers);
     s_flags[0] = 0;
     fence_mbar_init();
   }
@@ -198,6 +200,12 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
   // the immediately preceding kernel and is only touched after pdl_wait().  Routing
   // outputs are read through L2 only (ld.global.cg): kernels overlap their
   // neighbours, so nothing may come from an L1 line left by an earlier call.
+  // With single-tile raster groups a CTA's first unit is (tile blockIdx / mt, M unit
+  // blockIdx % mt) whatever the tile count, so its tile entry is loaded together with
+  // the count instead of after it (one L2 round trip less before the first copy).
+  const int first_tile = (int)blockIdx.x / p.mt;
+  const bool first_known = p.group_tiles == 1 && first_tile < p.max_tiles;
+  const int4 first_te = first_known ? __ldcg(reinterpret_cast<const int4*>(p.tiles + first_tile)) : make_int4(0, 0, 0, 0);
   const int num_tiles = __ldcg(p.num_tiles);
   const int KG = p.kg;
   const int U = num_tiles * p.mt;
@@ -219,99 +227,107 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      // iterator over this CTA's (segment, K group) iterations
-      int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0, b_rows = C::kBRows;
-      auto open_seg = [&]() {
-        int u, kk0;
-        bool whole;
-        sch.seg(si, u, kk0, kk1, whole);
-        kk = kk0;
-        map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
-        const TileEntry te = load_tile(p.tiles + tile);
-        expert = te.expert;
-        // token-major tiles: only the real tokens' rows (kTerms per token) are loaded
-        // (the MMA's columns of rows never loaded are never read)
-        b_rows = (C::kConcat || W16) ? C::kRowTerms * max(1, min(te.n_rows, BM)) : C::kBRows;
-      };
-      auto advance = [&]() {
-        if (++kk == kk1 && ++si < sch.nseg) open_seg();
-      };
-      // bytes the stage's barrier expects for the current tile
-      auto tx_bytes = [&]() -> uint32_t { return C::kTxNoB + (uint32_t)b_rows * (uint32_t)C::kKBytes; };
-      // Weights are read once per call.  When more units than CTAs stream them, mark
-      // them evict-first so that the activation tiles every unit of a tile re-reads
-      // stay in L2; a single wave keeps the normal policy (faster there).
-      const uint64_t w_policy = U > grid ? l2_policy_evict_first() : l2_policy_evict_normal();
-      auto load_a = [&](int s) {
-        for (int j = 0; j < C::kA; ++j) {
-          // gate/up: group j of M tile mt; down: M tile mt (or 2 mt + j), group 0.  An M
-          // tile past the matrix reads zeros (TMA fill) and scales of the last tile.
-          const int mrow = GATEUP ? mt : (MPAIR ? 2 * mt + j : mt);
-          const int grp = GATEUP ? j : 0;
-          tma_load_3d_hint(a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile,
-                           expert * p.w_groups + grp, w_policy);
-          if constexpr (W16) continue;
-          const int msf = min(mrow, p.w_mt - 1);
-          const uint8_t* wsf =
-              p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)p.kg_sf * kSfAtomBytes;
-          bulk_load_hint(sf_a(s, j), wsf + (size_t)kk * C::kAtoms * kSfAtomBytes, C::kAtoms * kSfAtomBytes,
-                         &full_bar[s], w_policy);
-        }
-      };
-      auto load_b = [&](int s, int b_tile_idx, int b_kk, int rows) {
-        // the (stage, tile) image is contiguous and already swizzled: one bulk copy
-        bulk_load(b_tile(s), p.act_q + ((size_t)b_kk * p.max_tiles + b_tile_idx) * (size_t)(C::kBRows * C::kKBytes),
-                  (uint32_t)rows * (uint32_t)C::kKBytes, &full_bar[s]);
-        if constexpr (W16) return;
-        // the stage's kAtoms K groups of scale atoms are adjacent
-        bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * p.kg_sf + (size_t)b_kk * C::kAtoms) * (kSfAtomBytes * C::kNbAtoms),
-                  C::kAtoms * C::kNbAtoms * kSfAtomBytes, &full_bar[s]);
-      };
-      int g = 0;
-      bool err = false;
-      if (sch.nseg > 0) {
-        open_seg();
-        // weights of the first stages depend only on the routing: stream them while
-        // the previous kernel finishes
-        int pre_tile[C::kStages], pre_kk[C::kStages], pre_rows[C::kStages];
-        int npre = 0;
-        while (npre < C::kStages && si < sch.nseg) {
-          mbar_arrive_expect_tx(&full_bar[npre], tx_bytes());  // fresh stages: no wait
-          load_a(npre);
-          pre_tile[npre] = tile;
-          pre_kk[npre] = kk;
-          pre_rows[npre] = b_rows;
-          ++npre;
-          advance();
-        }
-        pdl_wait();
-        for (int i = 0; i < npre; ++i) load_b(i, pre_tile[i], pre_kk[i], pre_rows[i]);
-        g = npre;
-        for (; si < sch.nseg; ++g) {
-          const int s = g % C::kStages;
-          const uint32_t ph = (g / C::kStages) & 1;
-          if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1, kWaitLimit)) {
-            report_status(p.status, kStatusTimeoutProducer);
-            s_flags[0] = 1;
-            err = true;
-            break;
-          }
-          mbar_arrive_expect_tx(&full_bar[s], tx_bytes());
-          load_a(s);
-          load_b(s, tile, kk, b_rows);
-          advance();
-        }
+    // Lane 0 issues every weight copy and runs the ring; after the dependency wait the
+    // activation copies of the stages it issued before the wait go out from one lane
+    // each, in parallel.
+    __shared__ int s_pre[3][C::kStages];  // pre-issued stages: tile, K group, B rows
+    // iterator over this CTA's (segment, K group) iterations (lane 0)
+    int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0, b_rows = C::kBRows;
+    auto open_seg = [&]() {
+      int u, kk0;
+      bool whole;
+      sch.seg(si, u, kk0, kk1, whole);
+      kk = kk0;
+      map_unit(u, num_tiles, p.mt, p.group_tiles, tile, mt);
+      TileEntry te;
+      if (si == 0 && first_known) {
+        te.expert = first_te.x;
+        te.n_rows = first_te.z;
       } else {
-        pdl_wait();
+        te = load_tile(p.tiles + tile);
       }
-      // on an error, wait (bounded) for the copies already issued to land
-      if (err) {
-        for (int gg = max(0, g - C::kStages); gg < g; ++gg)
-          mbar_wait_bounded(&full_bar[gg % C::kStages], (gg / C::kStages) & 1, kWaitLimit);
+      expert = te.expert;
+      // token-major tiles: only the real tokens' rows (kTerms per token) are loaded
+      // (the MMA's columns of rows never loaded are never read)
+      b_rows = (C::kConcat || W16) ? C::kRowTerms * max(1, min(te.n_rows, BM)) : C::kBRows;
+    };
+    auto advance = [&]() {
+      if (++kk == kk1 && ++si < sch.nseg) open_seg();
+    };
+    // bytes the stage's barrier expects for the current tile
+    auto tx_bytes = [&]() -> uint32_t { return C::kTxNoB + (uint32_t)b_rows * (uint32_t)C::kKBytes; };
+    // Weights are read once per call.  When more units than CTAs stream them, mark
+    // them evict-first so that the activation tiles every unit of a tile re-reads
+    // stay in L2; a single wave keeps the normal policy (faster there).
+    const uint64_t w_policy = U > grid ? l2_policy_evict_first() : l2_policy_evict_normal();
+    auto load_a = [&](int s) {
+      for (int j = 0; j < C::kA; ++j) {
+        // gate/up: group j of M tile mt; down: M tile mt (or 2 mt + j), group 0.  An M
+        // tile past the matrix reads zeros (TMA fill) and scales of the last tile.
+        const int mrow = GATEUP ? mt : (MPAIR ? 2 * mt + j : mt);
+        const int grp = GATEUP ? j : 0;
+        tma_load_3d_hint(a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile,
+                         expert * p.w_groups + grp, w_policy);
+        if constexpr (W16) continue;
+        const int msf = min(mrow, p.w_mt - 1);
+        const uint8_t* wsf =
+            p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)p.kg_sf * kSfAtomBytes;
+        bulk_load_hint(sf_a(s, j), wsf + (size_t)kk * C::kAtoms * kSfAtomBytes, C::kAtoms * kSfAtomBytes,
+                       &full_bar[s], w_policy);
       }
-    } else {
-      pdl_wait();
+    };
+    auto load_b = [&](int s, int b_tile_idx, int b_kk, int rows) {
+      // the (stage, tile) image is contiguous and already swizzled: one bulk copy
+      bulk_load(b_tile(s), p.act_q + ((size_t)b_kk * p.max_tiles + b_tile_idx) * (size_t)(C::kBRows * C::kKBytes),
+                (uint32_t)rows * (uint32_t)C::kKBytes, &full_bar[s]);
+      if constexpr (W16) return;
+      // the stage's kAtoms K groups of scale atoms are adjacent
+      bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * p.kg_sf + (size_t)b_kk * C::kAtoms) * (kSfAtomBytes * C::kNbAtoms),
+                C::kAtoms * C::kNbAtoms * kSfAtomBytes, &full_bar[s]);
+    };
+    int npre = 0;
+    if (lane == 0 && sch.nseg > 0) {
+      open_seg();
+      // weights of the first stages depend only on the routing: stream them while
+      // the previous kernel finishes
+      while (npre < C::kStages && si < sch.nseg) {
+        mbar_arrive_expect_tx(&full_bar[npre], tx_bytes());  // fresh stages: no wait
+        load_a(npre);
+        s_pre[0][npre] = tile;
+        s_pre[1][npre] = kk;
+        s_pre[2][npre] = b_rows;
+        ++npre;
+        advance();
+      }
+    }
+    npre = __shfl_sync(0xffffffffu, npre, 0);
+    __syncwarp();  // s_pre written by lane 0 is visible to the warp
+    pdl_wait();
+    if (lane < npre) load_b(lane, s_pre[0][lane], s_pre[1][lane], s_pre[2][lane]);
+    __syncwarp();
+    if (lane == 0) {
+      int g = npre;
+      bool err = false;
+      for (; si < sch.nseg; ++g) {
+        const int s = g % C::kStages;
+        const uint32_t ph = (g / C::kStages) & 1;
+        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1, p.wait_ns)) {
+          report_status(p.status, kStatusTimeoutProducer);
+          s_flags[0] = 1;
+          err = true;
+          break;
+        }
+        mbar_arrive_expect_tx(&full_bar[s], tx_bytes());
+        load_a(s);
+        load_b(s, tile, kk, b_rows);
+        advance();
+      }
+      // Before the CTA exits and its shared memory is reused, every copy issued into it
+      // has landed: wait (bounded by the long limit, whatever the call's wait limit) for
+      // the last ring's worth of stages.  On the normal path they were consumed already.
+      (void)err;
+      for (int gg = max(0, g - C::kStages); gg < g; ++gg)
+        mbar_wait_bounded(&full_bar[gg % C::kStages], (gg / C::kStages) & 1, kWaitLimit);
     }
   } else if (warp == 1 || warp == kSecondIssuerWarp) {
     // ------------------------------------------------------------ MMA issuers
@@ -342,7 +358,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         bool whole;
         sch.seg(si, u, kk0, kk1, whole);
         const int b = si % C::kNumAcc;
-        if (!mbar_wait_bounded(&acce_bar[b], ((si / C::kNumAcc) & 1) ^ 1, kWaitLimit)) {
+        if (!mbar_wait_bounded(&acce_bar[b], ((si / C::kNumAcc) & 1) ^ 1, p.wait_ns)) {
           report_status(p.status, kStatusTimeoutMain);
           s_flags[0] = 1;
           break;
@@ -353,7 +369,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         for (int kk = kk0; kk < kk1; ++kk, ++g) {
           const int s = g % C::kStages;
           const uint32_t ph = (g / C::kStages) & 1;
-          if (!mbar_wait_bounded(&full_bar[s], ph, kWaitLimit)) {
+          if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_ns)) {
             report_status(p.status, kStatusTimeoutMain);
             s_flags[0] = 1;
             err = true;
@@ -416,6 +432,10 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         }
         if (!err) mma_commit(&accf_bar[b]);
       }
+      // every tensor-core operation this thread issued (MMAs, scale copies) completes
+      // before the CTA frees its tensor memory and exits (long limit, as above)
+      mma_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, kWaitLimit);
     }
   } else if ((warp >= 2 && warp < 6) || (C::kEpiGroups == 2 && warp >= 7 && warp < 11)) {
     // ------------------------------------------------------------ epilogue
@@ -448,7 +468,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
           s_roww[et] = __ldcg(p.topk_w + a);
         }
       }
-      const bool ok = mbar_wait_bounded(&accf_bar[b], (si / C::kNumAcc) & 1, kWaitLimit);
+      const bool ok = mbar_wait_bounded(&accf_bar[b], (si / C::kNumAcc) & 1, p.wait_ns);
       if (!ok) {
         report_status(p.status, kStatusTimeoutEpi);
         s_flags[0] = 1;

@@ -185,7 +185,12 @@ struct GemmParams {
   int grid;                // persistent CTAs (<= kMaxCtas)
   uint32_t* status;
   int w16;                 // bf16 weights and activations (act16_offset layout, no scales)
+  uint64_t wait_ns;        // limit of each pipeline wait (ns); teardown drains wait up to 1 s
 };
+
+// Limit of the expert GEMMs' pipeline waits for launches made from now on (ns; the
+// default is 1 s), set by moe_set_wait_limit_ns.
+uint64_t gemm_wait_limit_ns();
 cudaError_t launch_gateup(const GemmParams& p, cudaStream_t stream);
 cudaError_t launch_down(const GemmParams& p, cudaStream_t stream);
 

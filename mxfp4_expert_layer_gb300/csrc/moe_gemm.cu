@@ -30,6 +30,8 @@
 // ("triton-kernels" README, "Fused MoE Dispatch": the Mixtral-style layer):
 // kind::f16 MMAs with K = 16, 64-value stages of the same 128-byte rows, no scales,
 // and bf16 h written by the gate/up epilogue.
+#include <type_traits>
+
 #include "moe_common.cuh"
 #include "moe_kernels.cuh"
 #include "sm100_ptx.cuh"
@@ -507,58 +509,78 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
           }
           epi_bar();  // s_xpose reused by the next chunk
         } else if constexpr (GATEUP) {
-          // h = silu(g) * u -> shared memory, transposed so that one thread holds the 32
-          // features of one MX block of one token column
+          // h = silu(g) * u -> shared memory, transposed so that threads hold runs of
+          // features of one token column (only the tile's real tokens are computed)
           const bool fvalid = feat < p.I;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) s_xpose[j * kMTile + m] = fvalid ? silu_f(va[j]) * vb[j] : 0.f;
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < nrows) s_xpose[j * kMTile + m] = fvalid ? silu_f(va[j]) * vb[j] : 0.f;
           epi_bar();
-          // 16 columns x 4 MX blocks, two threads per block (16 values each): threads
-          // 8j..8j+7 hold column j, the pair (2qb, 2qb+1) block qb
-          const int j = et >> 3, qb = (et >> 1) & 3, hf = et & 1;
-          const int r = c0 + j;
-          float vv[16];
-          const float4* src = reinterpret_cast<const float4*>(s_xpose + j * kMTile + qb * 32 + hf * 16);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 f4 = src[i];
-            vv[4 * i] = f4.x;
-            vv[4 * i + 1] = f4.y;
-            vv[4 * i + 2] = f4.z;
-            vv[4 * i + 3] = f4.w;
-          }
-          const int feat0 = mt * kMTile + qb * 32 + hf * 16;
+          // Each column's 4 MX blocks of 32 features are encoded by 128 / V threads, V
+          // values each (32 / V threads per block), with V the smallest of 4, 8 and 16
+          // whose 128-thread cover reaches the chunk's real columns: a tile with few
+          // tokens gives each thread a shorter dependent chain of terms.
+          const int live = min(16, nrows - c0);
           uint8_t* sf = p.h_sf + ((size_t)tile * p.kg_out + mt) * (kSfAtomBytes * act_sf_atoms(BM));
+          auto encode = [&](auto v_tag) {
+            constexpr int V = decltype(v_tag)::value;
+            constexpr int kTpb = 32 / V;    // threads per MX block
+            constexpr int kTpc = 4 * kTpb;  // threads per column
+            const int j = et / kTpc, qb = (et % kTpc) / kTpb, sub = et % kTpb;
+            const int r = c0 + j;
+            float vv[V];
+            const float4* src = reinterpret_cast<const float4*>(s_xpose + j * kMTile + qb * 32 + sub * V);
 #pragma unroll
-          for (int t = 0; t < kTerms; ++t) {
-            float amax = 0.f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(vv[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            const int pe = mx_e2m1_exponent(amax);
-            const float inv = pow2_int(-pe), sc = pow2_int(pe);
-            uint32_t w[2] = {0, 0};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const uint32_t pair = f32x2_to_e2m1x2(vv[2 * i] * inv, vv[2 * i + 1] * inv);
-              const float2 q = e2m1x2_to_f32x2(pair);
-              vv[2 * i] -= q.x * sc;
-              vv[2 * i + 1] -= q.y * sc;
-              w[i >> 2] |= pair << (8 * (i & 3));
+            for (int i = 0; i < V / 4; ++i) {
+              const float4 f4 = src[i];
+              vv[4 * i] = f4.x;
+              vv[4 * i + 1] = f4.y;
+              vv[4 * i + 2] = f4.z;
+              vv[4 * i + 3] = f4.w;
             }
-            // the 4 MX blocks of a column sit in lanes 8j'..8j'+7 (even lanes): pack exponents
-            const uint32_t e8 = static_cast<uint32_t>(pe + 127);
-            const int base = lane & ~7;
-            const uint32_t word = __shfl_sync(0xffffffffu, e8, base) | (__shfl_sync(0xffffffffu, e8, base + 2) << 8) |
-                                  (__shfl_sync(0xffffffffu, e8, base + 4) << 16) |
-                                  (__shfl_sync(0xffffffffu, e8, base + 6) << 24);
-            if (r < nrows) {
-              if (feat0 < i_pad)
-                *reinterpret_cast<uint2*>(p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM)) =
-                    make_uint2(w[0], w[1]);
-              if ((et & 7) == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(t, r, BM), 0)) = word;
+            const int feat0 = mt * kMTile + qb * 32 + sub * V;
+#pragma unroll
+            for (int t = 0; t < kTerms; ++t) {
+              float amax = 0.f;
+#pragma unroll
+              for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(vv[i]));
+#pragma unroll
+              for (int d = 1; d < kTpb; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+              const int pe = mx_e2m1_exponent(amax);
+              const float inv = pow2_int(-pe), sc = pow2_int(pe);
+              uint32_t w[(V + 7) / 8] = {};
+#pragma unroll
+              for (int i = 0; i < V / 2; ++i) {
+                const uint32_t pair = f32x2_to_e2m1x2(vv[2 * i] * inv, vv[2 * i + 1] * inv);
+                const float2 q = e2m1x2_to_f32x2(pair);
+                vv[2 * i] -= q.x * sc;
+                vv[2 * i + 1] -= q.y * sc;
+                w[i >> 2] |= pair << (8 * (i & 3));
+              }
+              // the column's 4 blocks start at lanes base, base + kTpb, ...: pack the exponents
+              const uint32_t e8 = static_cast<uint32_t>(pe + 127);
+              const int base = lane & ~(kTpc - 1);
+              const uint32_t word = __shfl_sync(0xffffffffu, e8, base) |
+                                    (__shfl_sync(0xffffffffu, e8, base + kTpb) << 8) |
+                                    (__shfl_sync(0xffffffffu, e8, base + 2 * kTpb) << 16) |
+                                    (__shfl_sync(0xffffffffu, e8, base + 3 * kTpb) << 24);
+              if (r < nrows) {
+                if (feat0 < i_pad) {
+                  uint8_t* dst = p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM);
+                  if constexpr (V == 16) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                  else if constexpr (V == 8) *reinterpret_cast<uint32_t*>(dst) = w[0];
+                  else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w[0]);
+                }
+                if (et % kTpc == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(t, r, BM), 0)) = word;
+              }
             }
-          }
+          };
+          if (live <= 4)
+            encode(std::integral_constant<int, 4>{});
+          else if (live <= 8)
+            encode(std::integral_constant<int, 8>{});
+          else
+            encode(std::integral_constant<int, 16>{});
           epi_bar();  // s_xpose reused by the next chunk
         } else {
           // output features: M tile mt, or the pair 2 mt, 2 mt + 1 (va, vb)

@@ -189,6 +189,89 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
   }
 }
 
+// The same table for at most 32 assignments, built by one warp with no block
+// barrier (the decode shapes): lane a holds assignment a, lanes with equal experts
+// count themselves into one shared histogram row (__match_any_sync, no atomics), and
+// the scan, offsets, tiles and the stable scatter are those of the block version, so
+// the bits are identical.
+template <bool kSharedIdx = false>
+__device__ void build_tile_table_warp(const int32_t* __restrict__ idx, int Tk, int E, int bm, int32_t* counts,
+                                      int32_t* offsets, int32_t* perm, int32_t* inv_perm, TileEntry* tiles,
+                                      int32_t* num_tiles, uint32_t* status, int32_t* tile_first = nullptr) {
+  __shared__ int whist[kMaxExperts];
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int e = lane; e < E; e += 32) whist[e] = 0;
+  int ea = -1;
+  if (lane < Tk) {
+    ea = kSharedIdx ? idx[lane] : __ldcg(idx + lane);
+    if (ea < 0 || ea >= E) {
+      report_status(status, kStatusBadIndex);
+      ea = -1;
+    }
+  }
+  const unsigned grp = __match_any_sync(0xffffffffu, ea);
+  __syncwarp();
+  if (ea >= 0 && (grp & lt_mask) == 0) whist[ea] = __popc(grp);
+  __syncwarp();
+  // lane l owns experts [l*per, l*per + per): counts, then one warp scan of the packed
+  // (rows, tiles) pairs gives each expert's first sorted row and first tile
+  const int lgbm = __ffs(bm) - 1;
+  const int per = (E + 31) >> 5;
+  const int e0 = lane * per;
+  int cnt[kMaxExperts / 32];
+  int rows = 0, ntl = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    const int c = (i < per && e0 + i < E) ? whist[e0 + i] : 0;
+    cnt[i] = c;
+    rows += c;
+    ntl += (c + bm - 1) >> lgbm;
+  }
+  int packed = rows | (ntl << 16);  // at most 32 rows and 32 tiles
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, packed, d);
+    if (lane >= d) packed += o;
+  }
+  const int rows_incl = packed & 0xFFFF, ntl_incl = (int)((unsigned)packed >> 16);
+  int off = rows_incl - rows, t0 = ntl_incl - ntl;
+  __syncwarp();  // every lane has read whist before it becomes the row offsets
+#pragma unroll
+  for (int i = 0; i < kMaxExperts / 32; ++i) {
+    const int e = e0 + i;
+    if (i >= per || e >= E) break;
+    const int c = cnt[i];
+    counts[e] = c;
+    offsets[e] = off;
+    if (tile_first) tile_first[e] = t0;
+    whist[e] = off;
+    const int nt = (c + bm - 1) >> lgbm;
+    for (int q = 0; q < nt; ++q) {
+      TileEntry te;
+      te.expert = e;
+      te.row_begin = off + (q << lgbm);
+      te.n_rows = min(bm, c - (q << lgbm));
+      te.pad_row = (t0 + q) << lgbm;
+      tiles[t0 + q] = te;
+    }
+    off += c;
+    t0 += nt;
+  }
+  if (lane == 31) {
+    offsets[E] = rows_incl;
+    *num_tiles = ntl_incl;
+  }
+  __syncwarp();
+  // stable scatter: an assignment's sorted row is its expert's first row plus the
+  // number of lower lanes with the same expert
+  if (ea >= 0) {
+    const int pos = whist[ea] + __popc(grp & lt_mask);
+    perm[pos] = lane;
+    inv_perm[lane] = pos;
+  }
+}
+
 // Top-k of one token by one warp: each lane holds logits e = lane + 32*i; k rounds
 // of a warp arg-max on (value desc, index asc).  Weights by `gating` (MoeGating):
 // softmax over the k selected (exponentials relative to the largest, summed in
@@ -726,6 +809,14 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     }
   }
   if (!builds) return;
+  if (p.T * p.k <= 32) {
+    // few assignments: one warp builds the table
+    if (warp != 0) return;
+    if (!mbar_wait_cluster_bounded(bar_idx, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
+    build_tile_table_warp<true>(sidx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
+                                p.num_tiles, p.status, p.tile_first);
+    return;
+  }
   if (!mbar_wait_cluster_bounded(bar_idx, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
   build_tile_table_block<true>(sidx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
                                p.num_tiles, p.status, p.tile_first);
@@ -955,6 +1046,10 @@ __global__ void __launch_bounds__(kRouteThreads) tile_table_kernel(const int32_t
                                                                    int32_t* counts, int32_t* offsets, int32_t* perm,
                                                                    int32_t* inv_perm, TileEntry* tiles,
                                                                    int32_t* num_tiles) {
+  if (Tk <= 32) {
+    if (threadIdx.x < 32) build_tile_table_warp(idx, Tk, E, bm, counts, offsets, perm, inv_perm, tiles, num_tiles, nullptr);
+    return;
+  }
   build_tile_table_block(idx, Tk, E, bm, counts, offsets, perm, inv_perm, tiles, num_tiles, nullptr);
 }
 

@@ -103,7 +103,10 @@ def test_router_many_tokens(api, T, H, E, k, zipf):
 
 CASES = [(4, 8, 2, 16, 0.0), (1, 32, 4, 16, 0.0), (64, 32, 4, 16, 0.0), (64, 128, 4, 16, 0.0),
          (4096, 128, 4, 128, 1.1), (4096, 128, 4, 64, 0.0), (777, 16, 2, 64, 1.5), (300, 1, 1, 128, 0.0),
-         (50, 256, 8, 16, 0.7), (2048, 8, 8, 128, 0.0)]
+         (50, 256, 8, 16, 0.7), (2048, 8, 8, 128, 0.0),
+         # at most 32 assignments (the one-warp builder): at the limit, k = E, one expert, skewed
+         (8, 256, 4, 16, 0.0), (32, 64, 1, 16, 1.5), (5, 3, 3, 16, 0.0), (3, 1, 1, 16, 0.0), (6, 200, 5, 64, 0.0),
+         (33, 64, 1, 16, 0.0)]
 
 
 @pytest.mark.parametrize("T,E,k,bm,skew", CASES)

@@ -229,11 +229,13 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    // Lane 0 issues every weight copy and runs the ring; after the dependency wait the
-    // activation copies of the stages it issued before the wait go out from one lane
+    // The whole warp runs the ring in step with identical values (uniform control
+    // flow); lane 0 alone issues each copy, through a predicate.  After the dependency
+    // wait the activation copies of the stages issued before it go out from one lane
     // each, in parallel.
     __shared__ int s_pre[3][C::kStages];  // pre-issued stages: tile, K group, B rows
-    // iterator over this CTA's (segment, K group) iterations (lane 0)
+    const bool leader = lane == 0;
+    // iterator over this CTA's (segment, K group) iterations
     int si = 0, kk = 0, kk1 = 0, tile = 0, mt = 0, expert = 0, b_rows = C::kBRows;
     auto open_seg = [&]() {
       int u, kk0;
@@ -268,75 +270,80 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         // tile past the matrix reads zeros (TMA fill) and scales of the last tile.
         const int mrow = GATEUP ? mt : (MPAIR ? 2 * mt + j : mt);
         const int grp = GATEUP ? j : 0;
-        tma_load_3d_hint(a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile,
-                         expert * p.w_groups + grp, w_policy);
+        tma_load_3d_hint_if(leader, a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile,
+                            expert * p.w_groups + grp, w_policy);
         if constexpr (W16) continue;
         const int msf = min(mrow, p.w_mt - 1);
         const uint8_t* wsf =
             p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)p.kg_sf * kSfAtomBytes;
-        bulk_load_hint(sf_a(s, j), wsf + (size_t)kk * C::kAtoms * kSfAtomBytes, C::kAtoms * kSfAtomBytes,
-                       &full_bar[s], w_policy);
+        bulk_load_hint_if(leader, sf_a(s, j), wsf + (size_t)kk * C::kAtoms * kSfAtomBytes, C::kAtoms * kSfAtomBytes,
+                          &full_bar[s], w_policy);
       }
     };
-    auto load_b = [&](int s, int b_tile_idx, int b_kk, int rows) {
-      // the (stage, tile) image is contiguous and already swizzled: one bulk copy
-      bulk_load(b_tile(s), p.act_q + ((size_t)b_kk * p.max_tiles + b_tile_idx) * (size_t)(C::kBRows * C::kKBytes),
-                (uint32_t)rows * (uint32_t)C::kKBytes, &full_bar[s]);
+    // the (stage, tile) image of the activations is contiguous and already swizzled:
+    // one bulk copy, and one for the stage's adjacent K groups of scale atoms
+    auto load_b = [&](bool issue, int s, int b_tile_idx, int b_kk, int rows) {
+      bulk_load_if(issue, b_tile(s),
+                   p.act_q + ((size_t)b_kk * p.max_tiles + b_tile_idx) * (size_t)(C::kBRows * C::kKBytes),
+                   (uint32_t)rows * (uint32_t)C::kKBytes, &full_bar[s]);
       if constexpr (W16) return;
-      // the stage's kAtoms K groups of scale atoms are adjacent
-      bulk_load(sf_b(s), p.act_sf + ((size_t)b_tile_idx * p.kg_sf + (size_t)b_kk * C::kAtoms) * (kSfAtomBytes * C::kNbAtoms),
-                C::kAtoms * C::kNbAtoms * kSfAtomBytes, &full_bar[s]);
+      bulk_load_if(issue, sf_b(s),
+                   p.act_sf + ((size_t)b_tile_idx * p.kg_sf + (size_t)b_kk * C::kAtoms) * (kSfAtomBytes * C::kNbAtoms),
+                   C::kAtoms * C::kNbAtoms * kSfAtomBytes, &full_bar[s]);
+    };
+    auto wait_warp = [](uint64_t* bar, uint32_t parity, uint64_t limit) {
+      return __shfl_sync(0xffffffffu, mbar_wait_bounded(bar, parity, limit) ? 1 : 0, 0) != 0;
     };
     int npre = 0;
-    if (lane == 0 && sch.nseg > 0) {
+    if (sch.nseg > 0) {
       open_seg();
       // weights of the first stages depend only on the routing: stream them while
       // the previous kernel finishes
       while (npre < C::kStages && si < sch.nseg) {
-        mbar_arrive_expect_tx(&full_bar[npre], tx_bytes());  // fresh stages: no wait
+        mbar_arrive_expect_tx_if(leader, &full_bar[npre], tx_bytes());  // fresh stages: no wait
         load_a(npre);
-        s_pre[0][npre] = tile;
-        s_pre[1][npre] = kk;
-        s_pre[2][npre] = b_rows;
+        if (leader) {
+          s_pre[0][npre] = tile;
+          s_pre[1][npre] = kk;
+          s_pre[2][npre] = b_rows;
+        }
         ++npre;
         advance();
       }
     }
-    npre = __shfl_sync(0xffffffffu, npre, 0);
     __syncwarp();  // s_pre written by lane 0 is visible to the warp
     pdl_wait();
-    if (lane < npre) load_b(lane, s_pre[0][lane], s_pre[1][lane], s_pre[2][lane]);
+    if (lane < npre) load_b(true, lane, s_pre[0][lane], s_pre[1][lane], s_pre[2][lane]);
     __syncwarp();
-    if (lane == 0) {
-      int g = npre;
-      bool err = false;
-      for (; si < sch.nseg; ++g) {
-        const int s = g % C::kStages;
-        const uint32_t ph = (g / C::kStages) & 1;
-        if (!mbar_wait_bounded(&empty_bar[s], ph ^ 1, p.wait_ns)) {
-          report_status(p.status, kStatusTimeoutProducer);
-          s_flags[0] = 1;
-          err = true;
-          break;
-        }
-        mbar_arrive_expect_tx(&full_bar[s], tx_bytes());
-        load_a(s);
-        load_b(s, tile, kk, b_rows);
-        advance();
+    int g = npre;
+    for (; si < sch.nseg; ++g) {
+      const int s = g % C::kStages;
+      const uint32_t ph = (g / C::kStages) & 1;
+      if (!wait_warp(&empty_bar[s], ph ^ 1, p.wait_ns)) {
+        if (leader) report_status(p.status, kStatusTimeoutProducer);
+        s_flags[0] = 1;
+        break;
       }
-      // Before the CTA exits and its shared memory is reused, every copy issued into it
-      // has landed: wait (bounded by the long limit, whatever the call's wait limit) for
-      // the last ring's worth of stages.  On the normal path they were consumed already.
-      (void)err;
-      for (int gg = max(0, g - C::kStages); gg < g; ++gg)
-        mbar_wait_bounded(&full_bar[gg % C::kStages], (gg / C::kStages) & 1, kWaitLimit);
+      mbar_arrive_expect_tx_if(leader, &full_bar[s], tx_bytes());
+      load_a(s);
+      load_b(leader, s, tile, kk, b_rows);
+      advance();
     }
+    // Before the CTA exits and its shared memory is reused, every copy issued into it
+    // has landed: wait (bounded by the long limit, whatever the call's wait limit) for
+    // the last ring's worth of stages.  On the normal path they were consumed already.
+    for (int gg = max(0, g - C::kStages); gg < g; ++gg)
+      wait_warp(&full_bar[gg % C::kStages], (gg / C::kStages) & 1, kWaitLimit);
   } else if (warp == 1 || warp == kSecondIssuerWarp) {
     // ------------------------------------------------------------ MMA issuers
     pdl_wait();
     const int issuer = warp == 1 ? 0 : 1;
-    if (lane == 0 && issuer < C::kIssuers) {
-      // this thread's weight tiles [j0, j1) and K steps [ks0, ks1) of every stage
+    if (issuer < C::kIssuers) {
+      // The whole warp runs this loop in step with identical values (its control flow
+      // is warp-uniform, so descriptors and addresses can live in uniform registers);
+      // lane 0 alone issues each tcgen05 instruction, through a predicate.
+      const bool leader = lane == 0;
+      // this warp's weight tiles [j0, j1) and K steps [ks0, ks1) of every stage
       constexpr bool kTilePerIssuer = C::kIssuers == 2 && !C::kSplitK;
       const int j0 = kTilePerIssuer ? issuer : 0, j1 = kTilePerIssuer ? issuer + 1 : C::kA;
       const int ks0 = C::kSplitK ? issuer * (C::kKSteps / 2) : 0;
@@ -353,6 +360,10 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
       auto kdesc = [](uint32_t saddr) {
         return C::kKBytes == 128 ? smem_desc_kmajor_sw128(saddr) : smem_desc_kmajor_sw64(saddr);
       };
+      // a bounded wait whose outcome the whole warp shares
+      auto wait_warp = [](uint64_t* bar, uint32_t parity, uint64_t limit) {
+        return __shfl_sync(0xffffffffu, mbar_wait_bounded(bar, parity, limit) ? 1 : 0, 0) != 0;
+      };
       int g = 0;
       bool err = false;
       for (int si = 0; si < sch.nseg && !err; ++si) {
@@ -360,8 +371,8 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         bool whole;
         sch.seg(si, u, kk0, kk1, whole);
         const int b = si % C::kNumAcc;
-        if (!mbar_wait_bounded(&acce_bar[b], ((si / C::kNumAcc) & 1) ^ 1, p.wait_ns)) {
-          report_status(p.status, kStatusTimeoutMain);
+        if (!wait_warp(&acce_bar[b], ((si / C::kNumAcc) & 1) ^ 1, p.wait_ns)) {
+          if (leader) report_status(p.status, kStatusTimeoutMain);
           s_flags[0] = 1;
           break;
         }
@@ -371,8 +382,8 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         for (int kk = kk0; kk < kk1; ++kk, ++g) {
           const int s = g % C::kStages;
           const uint32_t ph = (g / C::kStages) & 1;
-          if (!mbar_wait_bounded(&full_bar[s], ph, p.wait_ns)) {
-            report_status(p.status, kStatusTimeoutMain);
+          if (!wait_warp(&full_bar[s], ph, p.wait_ns)) {
+            if (leader) report_status(p.status, kStatusTimeoutMain);
             s_flags[0] = 1;
             err = true;
             break;
@@ -386,11 +397,11 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
               const uint64_t bdesc = smem_desc_kmajor_sw128(b_addr0 + so + 32 * ks);
               const uint32_t acc = seg_first ? 0u : 1u;
               for (int j = j0; j < j1; ++j)
-                mma_bf16(acc_base + j * C::kAccN, smem_desc_kmajor_sw128(a_addr0 + so + j * C::kATileBytes + 32 * ks),
-                         bdesc, idesc16, acc);
+                mma_bf16_if(leader, acc_base + j * C::kAccN,
+                            smem_desc_kmajor_sw128(a_addr0 + so + j * C::kATileBytes + 32 * ks), bdesc, idesc16, acc);
               seg_first = false;
             }
-            mma_commit(&empty_bar[s]);
+            mma_commit_if(leader, &empty_bar[s]);
             continue;
           }
           const uint32_t sfc = tmem + sf_col0 + s * C::kSfColsPerStage;
@@ -401,10 +412,10 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
           for (int j = j0; j < j1; ++j)
             for (int a = at0; a < at1; ++a) {
               const int i = j * C::kAtoms + a;
-              tmem_cp_32x128b_warpx4(sfc + 4 * i, smem_desc(sfa_addr0 + so + i * kSfAtomBytes, 0, 128, 0));
+              tmem_cp_32x128b_warpx4_if(leader, sfc + 4 * i, smem_desc(sfa_addr0 + so + i * kSfAtomBytes, 0, 128, 0));
             }
           for (int i = at0 * C::kNbAtoms; i < at1 * C::kNbAtoms; ++i)
-            tmem_cp_32x128b_warpx4(sfb0 + 4 * i, smem_desc(sfb_addr0 + so + i * kSfAtomBytes, 0, 128, 0));
+            tmem_cp_32x128b_warpx4_if(leader, sfb0 + 4 * i, smem_desc(sfb_addr0 + so + i * kSfAtomBytes, 0, 128, 0));
           for (int ks = ks0; ks < ks1; ++ks) {  // K = 64 steps: 32 bytes of every operand row
             if (kk * (C::kKStage / kMxBlock) + 2 * ks >= kblocks) break;  // both MX blocks are padding
             const int a = ks >> 1;                    // K group (scale atom) of this step
@@ -414,8 +425,8 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
               const uint32_t acc = seg_first ? 0u : 1u;
               for (int j = j0; j < j1; ++j) {
                 const uint64_t adesc = kdesc(a_addr0 + so + j * C::kATileBytes + 32 * ks);
-                mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
-                         sfb0 + 4 * a * C::kNbAtoms, acc);
+                mma_mxf4_if(leader, acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
+                            sfb0 + 4 * a * C::kNbAtoms, acc);
               }
             } else {
               for (int t = 0; t < kTerms; ++t) {
@@ -424,20 +435,21 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
                 const uint32_t acc = (seg_first && t == 0) ? 0u : 1u;
                 for (int j = j0; j < j1; ++j) {
                   const uint64_t adesc = kdesc(a_addr0 + so + j * C::kATileBytes + 32 * ks);
-                  mma_mxf4(acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a), sfb, acc);
+                  mma_mxf4_if(leader, acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
+                              sfb, acc);
                 }
               }
             }
             seg_first = false;
           }
-          mma_commit(&empty_bar[s]);  // frees the stage once both issuers' MMAs have read it
+          mma_commit_if(leader, &empty_bar[s]);  // frees the stage once both issuers' MMAs have read it
         }
-        if (!err) mma_commit(&accf_bar[b]);
+        if (!err) mma_commit_if(leader, &accf_bar[b]);
       }
-      // every tensor-core operation this thread issued (MMAs, scale copies) completes
+      // every tensor-core operation this warp issued (MMAs, scale copies) completes
       // before the CTA frees its tensor memory and exits (long limit, as above)
-      mma_commit(drain_bar);
-      mbar_wait_bounded(drain_bar, 0, kWaitLimit);
+      mma_commit_if(leader, drain_bar);
+      wait_warp(drain_bar, 0, kWaitLimit);
     }
   } else if ((warp >= 2 && warp < 6) || (C::kEpiGroups == 2 && warp >= 7 && warp < 11)) {
     // ------------------------------------------------------------ epilogue

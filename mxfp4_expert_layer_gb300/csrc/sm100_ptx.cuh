@@ -70,14 +70,31 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed is
+// suspended in hardware for up to `hint_ns` (woken when the phase completes) instead
+// of returning at once, so waiting warps take no issue slots from working ones.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: returns false when the phase has not completed `limit_ns`
 // nanoseconds after the first poll.  Callers turn that into an error status
-// instead of hanging the GPU.
+// instead of hanging the GPU.  Each poll may suspend the thread for up to 20 us (or
+// the limit, when shorter).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_suspend(bar, parity, hint)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
@@ -389,6 +406,85 @@ __device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t adesc, uint64
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
+}
+
+// ------------------------------------------------------------------ single-lane issue forms
+// For code that a whole warp runs in step with identical operands (so the compiler
+// can keep descriptors, tensor-memory addresses and loop state in the warp's uniform
+// registers): only the lane whose `issue` is set executes the instruction.  It is a
+// predicate on the instruction, not a branch around it, so control flow stays uniform.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4_if(bool issue, uint32_t taddr, uint64_t sdesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(sdesc), "r"((uint32_t)issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf4_if(bool issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %7, 0;\n\tsetp.ne.b32 q, %6, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], q;\n\t}" ::"r"(
+          d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate), "r"((uint32_t)issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16_if(bool issue, uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %5, 0;\n\tsetp.ne.b32 q, %4, 0;\n\t"
+      "@p tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"((uint32_t)issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_if(bool issue, uint64_t* bar, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+      "r"(bytes), "r"((uint32_t)issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint_if(bool issue, void* dst, const void* tmap, uint64_t* bar, int32_t c0,
+                                                    int32_t c1, int32_t c2, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %7, 0;\n\t"
+      "@p cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+      "%4, %5}], [%2], %6;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy),
+      "r"((uint32_t)issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_if(bool issue, void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "r"((uint32_t)issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void bulk_load_hint_if(bool issue, void* dst, const void* src, uint32_t bytes,
+                                                  uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %5, 0;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+      "%4;\n\t}" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy), "r"((uint32_t)issue)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_if(bool issue, uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+      "@p tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(smem_u32(bar)),
+      "r"((uint32_t)issue)
+      : "memory");
 }
 
 }  // namespace ptx

@@ -587,12 +587,16 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
               }
             }
           };
-          if (live <= 4)
-            encode(std::integral_constant<int, 4>{});
-          else if (live <= 8)
-            encode(std::integral_constant<int, 8>{});
-          else
-            encode(std::integral_constant<int, 16>{});
+          if constexpr (BM == 16) {
+            if (live <= 4)
+              encode(std::integral_constant<int, 4>{});
+            else if (live <= 8)
+              encode(std::integral_constant<int, 8>{});
+            else
+              encode(std::integral_constant<int, 16>{});
+          } else {
+            encode(std::integral_constant<int, 16>{});  // larger tiles: full chunks but the last
+          }
           epi_bar();  // s_xpose reused by the next chunk
         } else {
           // output features: M tile mt, or the pair 2 mt, 2 mt + 1 (va, vb)

@@ -312,9 +312,10 @@ int moe_tensor_peak(int kind, int mmas_per_sm, double* tflops, moe_stream_t stre
  * that gives up sets a bit of the workspace status word (moe_get_device_status), the
  * kernel drops its remaining work, waits (up to 1 s) for the copies and tensor-core
  * operations it has already issued, frees its tensor memory and exits: no trap, and
- * the context stays usable.  A limit shorter than the pipeline's own latency (a few
- * microseconds) makes waits give up on ordinary calls; that is how failure detection
- * is tested.  The pages have no counterpart of it.                                 */
+ * the context stays usable.  Limits under 2 us are polled without suspending the
+ * waiting thread, so a limit shorter than the pipeline's own latency (a copy landing
+ * takes about a microsecond even from L2) makes waits give up on ordinary calls;
+ * that is how failure detection is tested.  The pages have no counterpart of it.   */
 int moe_set_wait_limit_ns(unsigned long long ns);
 
 /* Synchronises `stream`, reads the workspace's device status word into *status

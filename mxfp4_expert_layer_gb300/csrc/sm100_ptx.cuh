@@ -69,11 +69,32 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t pa
   return ok != 0;
 }
 
+// Non-blocking poll: whether the phase with this parity has completed, now.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait: returns false when the phase has not completed `limit_ns`
 // nanoseconds after the first poll.  Callers turn that into an error status
 // instead of hanging the GPU.  Each poll may suspend the thread for up to 20 us (or
-// the limit, when shorter).
+// the limit, when shorter).  Limits under 2 us poll without suspending at all: a
+// blocking try_wait may itself wait for a hardware-chosen time, which would let a
+// short limit pass a phase that completes within that time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (limit_ns < 2000ull) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_test_wait(bar, parity))
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+  }
   if (mbar_try_wait(bar, parity)) return true;
   const uint32_t hint = limit_ns < 20000ull ? (uint32_t)limit_ns : 20000u;
   const uint64_t t0 = globaltimer_ns();

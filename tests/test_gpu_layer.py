@@ -274,7 +274,7 @@ def test_consecutive_calls_with_new_routing(name):
 
 
 @pytest.mark.parametrize("name,T", [("tiny", None), ("gptoss20b_b1", None), ("gptoss20b_b64", None),
-                                    ("gptoss20b_b64", 200)])
+                                    ("gptoss20b_b64", 200), ("gptoss20b_b64", 512)])
 def test_layer_norm_residual(name, T):
     """RMSNorm + residual in front of the layer: the router (cluster kernel for T <= 64,
     many-token kernel above) and the encoder normalise the rows themselves; the

@@ -492,6 +492,93 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
       epi_bar();  // row metadata visible
       const uint32_t acc_addr = tmem + lane_off + b * C::kAccCols;
 
+      // h = silu(g) * u of the 16 token columns from c0 (this thread's feature row m),
+      // computed for the tile's real tokens only (zero past them or past I)
+      auto silu_mul = [&](int c0, const float* va, const float* vb, float* h) {
+        const bool fvalid = feat < p.I;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) h[j] = (fvalid && c0 + j < nrows) ? silu_f(va[j]) * vb[j] : 0.f;
+      };
+      // h of 16 token columns -> shared memory, transposed so that threads hold runs of
+      // features of one token column, then encoded as kTerms E2M1 terms into the down
+      // GEMM's B layout
+      auto encode_h = [&](int c0, const float* h) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          if (c0 + j < nrows) s_xpose[j * kMTile + m] = h[j];
+        epi_bar();
+        // Each column's 4 MX blocks of 32 features are encoded by 128 / V threads, V
+        // values each (32 / V threads per block), with V the smallest of 4, 8 and 16
+        // whose 128-thread cover reaches the chunk's real columns: a tile with few
+        // tokens gives each thread a shorter dependent chain of terms.
+        const int live = min(16, nrows - c0);
+        uint8_t* sf = p.h_sf + ((size_t)tile * p.kg_out + mt) * (kSfAtomBytes * act_sf_atoms(BM));
+        auto encode = [&](auto v_tag) {
+          constexpr int V = decltype(v_tag)::value;
+          constexpr int kTpb = 32 / V;    // threads per MX block
+          constexpr int kTpc = 4 * kTpb;  // threads per column
+          const int j = et / kTpc, qb = (et % kTpc) / kTpb, sub = et % kTpb;
+          const int r = c0 + j;
+          float vv[V];
+          const float4* src = reinterpret_cast<const float4*>(s_xpose + j * kMTile + qb * 32 + sub * V);
+#pragma unroll
+          for (int i = 0; i < V / 4; ++i) {
+            const float4 f4 = src[i];
+            vv[4 * i] = f4.x;
+            vv[4 * i + 1] = f4.y;
+            vv[4 * i + 2] = f4.z;
+            vv[4 * i + 3] = f4.w;
+          }
+          const int feat0 = mt * kMTile + qb * 32 + sub * V;
+#pragma unroll
+          for (int t = 0; t < kTerms; ++t) {
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(vv[i]));
+#pragma unroll
+            for (int d = 1; d < kTpb; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+            const int pe = mx_e2m1_exponent(amax);
+            const float inv = pow2_int(-pe), sc = pow2_int(pe);
+            uint32_t w[(V + 7) / 8] = {};
+#pragma unroll
+            for (int i = 0; i < V / 2; ++i) {
+              const uint32_t pair = f32x2_to_e2m1x2(vv[2 * i] * inv, vv[2 * i + 1] * inv);
+              const float2 q = e2m1x2_to_f32x2(pair);
+              vv[2 * i] -= q.x * sc;
+              vv[2 * i + 1] -= q.y * sc;
+              w[i >> 2] |= pair << (8 * (i & 3));
+            }
+            // the column's 4 blocks start at lanes base, base + kTpb, ...: pack the exponents
+            const uint32_t e8 = static_cast<uint32_t>(pe + 127);
+            const int base = lane & ~(kTpc - 1);
+            const uint32_t word = __shfl_sync(0xffffffffu, e8, base) |
+                                  (__shfl_sync(0xffffffffu, e8, base + kTpb) << 8) |
+                                  (__shfl_sync(0xffffffffu, e8, base + 2 * kTpb) << 16) |
+                                  (__shfl_sync(0xffffffffu, e8, base + 3 * kTpb) << 24);
+            if (r < nrows) {
+              if (feat0 < i_pad) {
+                uint8_t* dst = p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM);
+                if constexpr (V == 16) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                else if constexpr (V == 8) *reinterpret_cast<uint32_t*>(dst) = w[0];
+                else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w[0]);
+              }
+              if (et % kTpc == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(t, r, BM), 0)) = word;
+            }
+          }
+        };
+        if constexpr (BM == 16) {
+          if (live <= 4)
+            encode(std::integral_constant<int, 4>{});
+          else if (live <= 8)
+            encode(std::integral_constant<int, 8>{});
+          else
+            encode(std::integral_constant<int, 16>{});
+        } else {
+          encode(std::integral_constant<int, 16>{});  // larger tiles: full chunks but the last
+        }
+        epi_bar();  // s_xpose reused by the next chunk
+      };
+
       // the math of 16 token columns starting at c0, given g/u (gate/up) or y (down)
       auto consume = [&](int c0, const float* va, const float* vb) {
         if constexpr (GATEUP && W16) {
@@ -521,83 +608,9 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
           }
           epi_bar();  // s_xpose reused by the next chunk
         } else if constexpr (GATEUP) {
-          // h = silu(g) * u -> shared memory, transposed so that threads hold runs of
-          // features of one token column (only the tile's real tokens are computed)
-          const bool fvalid = feat < p.I;
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            if (c0 + j < nrows) s_xpose[j * kMTile + m] = fvalid ? silu_f(va[j]) * vb[j] : 0.f;
-          epi_bar();
-          // Each column's 4 MX blocks of 32 features are encoded by 128 / V threads, V
-          // values each (32 / V threads per block), with V the smallest of 4, 8 and 16
-          // whose 128-thread cover reaches the chunk's real columns: a tile with few
-          // tokens gives each thread a shorter dependent chain of terms.
-          const int live = min(16, nrows - c0);
-          uint8_t* sf = p.h_sf + ((size_t)tile * p.kg_out + mt) * (kSfAtomBytes * act_sf_atoms(BM));
-          auto encode = [&](auto v_tag) {
-            constexpr int V = decltype(v_tag)::value;
-            constexpr int kTpb = 32 / V;    // threads per MX block
-            constexpr int kTpc = 4 * kTpb;  // threads per column
-            const int j = et / kTpc, qb = (et % kTpc) / kTpb, sub = et % kTpb;
-            const int r = c0 + j;
-            float vv[V];
-            const float4* src = reinterpret_cast<const float4*>(s_xpose + j * kMTile + qb * 32 + sub * V);
-#pragma unroll
-            for (int i = 0; i < V / 4; ++i) {
-              const float4 f4 = src[i];
-              vv[4 * i] = f4.x;
-              vv[4 * i + 1] = f4.y;
-              vv[4 * i + 2] = f4.z;
-              vv[4 * i + 3] = f4.w;
-            }
-            const int feat0 = mt * kMTile + qb * 32 + sub * V;
-#pragma unroll
-            for (int t = 0; t < kTerms; ++t) {
-              float amax = 0.f;
-#pragma unroll
-              for (int i = 0; i < V; ++i) amax = fmaxf(amax, fabsf(vv[i]));
-#pragma unroll
-              for (int d = 1; d < kTpb; d <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-              const int pe = mx_e2m1_exponent(amax);
-              const float inv = pow2_int(-pe), sc = pow2_int(pe);
-              uint32_t w[(V + 7) / 8] = {};
-#pragma unroll
-              for (int i = 0; i < V / 2; ++i) {
-                const uint32_t pair = f32x2_to_e2m1x2(vv[2 * i] * inv, vv[2 * i + 1] * inv);
-                const float2 q = e2m1x2_to_f32x2(pair);
-                vv[2 * i] -= q.x * sc;
-                vv[2 * i + 1] -= q.y * sc;
-                w[i >> 2] |= pair << (8 * (i & 3));
-              }
-              // the column's 4 blocks start at lanes base, base + kTpb, ...: pack the exponents
-              const uint32_t e8 = static_cast<uint32_t>(pe + 127);
-              const int base = lane & ~(kTpc - 1);
-              const uint32_t word = __shfl_sync(0xffffffffu, e8, base) |
-                                    (__shfl_sync(0xffffffffu, e8, base + kTpb) << 8) |
-                                    (__shfl_sync(0xffffffffu, e8, base + 2 * kTpb) << 16) |
-                                    (__shfl_sync(0xffffffffu, e8, base + 3 * kTpb) << 24);
-              if (r < nrows) {
-                if (feat0 < i_pad) {
-                  uint8_t* dst = p.h_q + act_offset(tile, t, r, feat0, p.max_tiles, BM);
-                  if constexpr (V == 16) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
-                  else if constexpr (V == 8) *reinterpret_cast<uint32_t*>(dst) = w[0];
-                  else *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(w[0]);
-                }
-                if (et % kTpc == 0) *reinterpret_cast<uint32_t*>(sf + sf_atom_offset(act_row(t, r, BM), 0)) = word;
-              }
-            }
-          };
-          if constexpr (BM == 16) {
-            if (live <= 4)
-              encode(std::integral_constant<int, 4>{});
-            else if (live <= 8)
-              encode(std::integral_constant<int, 8>{});
-            else
-              encode(std::integral_constant<int, 16>{});
-          } else {
-            encode(std::integral_constant<int, 16>{});  // larger tiles: full chunks but the last
-          }
-          epi_bar();  // s_xpose reused by the next chunk
+          float h[16];
+          silu_mul(c0, va, vb, h);
+          encode_h(c0, h);
         } else {
           // output features: M tile mt, or the pair 2 mt, 2 mt + 1 (va, vb)
           const int fa = (MPAIR ? 2 * mt : mt) * kMTile + m;
@@ -656,22 +669,81 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
       } else {
         // accumulator too large for registers (per-term MMAs): 16 columns at a time,
         // the groups taking alternate chunks
-        for (int c0 = 16 * eg; c0 < BM; c0 += 16 * C::kEpiGroups) {
-          if (c0 >= nrows) break;
-          uint32_t rg[16], ru[16];
-          float va[16], vb[16];
-          tmem_ld_32x32b_x16(acc_addr + c0, rg);
-          if (C::kA > 1) tmem_ld_32x32b_x16(acc_addr + C::kAccN + c0, ru);
-          tmem_wait_ld();
+        if constexpr (GATEUP && !W16) {
+          // h of all this thread's chunks first (BM / 16 / groups chunks of 16 values),
+          // then the accumulator goes back to the MMA warps, and the transposes and the
+          // long four-term encode run while the next unit's MMAs do
+          constexpr int kChunks = BM / 16 / C::kEpiGroups;
+          float hreg[kChunks][16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            va[j] = __uint_as_float(rg[j]);
-            vb[j] = C::kA > 1 ? __uint_as_float(ru[j]) : 0.f;
+          for (int i = 0; i < kChunks; ++i) {
+            const int c0 = 16 * (eg + C::kEpiGroups * i);
+            if (c0 < nrows) {
+              uint32_t rg[16], ru[16];
+              float va[16], vb[16];
+              tmem_ld_32x32b_x16(acc_addr + c0, rg);
+              tmem_ld_32x32b_x16(acc_addr + C::kAccN + c0, ru);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                va[j] = __uint_as_float(rg[j]);
+                vb[j] = __uint_as_float(ru[j]);
+              }
+              silu_mul(c0, va, vb, hreg[i]);
+            }
           }
-          consume(c0, va, vb);
+          tc_fence_before();
+          mbar_arrive(&acce_bar[b]);
+#pragma unroll
+          for (int i = 0; i < kChunks; ++i) {
+            const int c0 = 16 * (eg + C::kEpiGroups * i);
+            if (c0 < nrows) encode_h(c0, hreg[i]);
+          }
+        } else if constexpr (!GATEUP && !W16) {
+          // down: all this thread's chunks into registers, the accumulator back to the
+          // MMA warps, then the weighted slot stores
+          constexpr int kChunks = BM / 16 / C::kEpiGroups;
+          float ya[kChunks][16], yb[kChunks][16];
+#pragma unroll
+          for (int i = 0; i < kChunks; ++i) {
+            const int c0 = 16 * (eg + C::kEpiGroups * i);
+            if (c0 < nrows) {
+              uint32_t rg[16], ru[16];
+              tmem_ld_32x32b_x16(acc_addr + c0, rg);
+              if (C::kA > 1) tmem_ld_32x32b_x16(acc_addr + C::kAccN + c0, ru);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                ya[i][j] = __uint_as_float(rg[j]);
+                yb[i][j] = C::kA > 1 ? __uint_as_float(ru[j]) : 0.f;
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&acce_bar[b]);
+#pragma unroll
+          for (int i = 0; i < kChunks; ++i) {
+            const int c0 = 16 * (eg + C::kEpiGroups * i);
+            if (c0 < nrows) consume(c0, ya[i], yb[i]);
+          }
+        } else {
+          for (int c0 = 16 * eg; c0 < BM; c0 += 16 * C::kEpiGroups) {
+            if (c0 >= nrows) break;
+            uint32_t rg[16], ru[16];
+            float va[16], vb[16];
+            tmem_ld_32x32b_x16(acc_addr + c0, rg);
+            if (C::kA > 1) tmem_ld_32x32b_x16(acc_addr + C::kAccN + c0, ru);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              va[j] = __uint_as_float(rg[j]);
+              vb[j] = C::kA > 1 ? __uint_as_float(ru[j]) : 0.f;
+            }
+            consume(c0, va, vb);
+          }
+          tc_fence_before();
+          mbar_arrive(&acce_bar[b]);
         }
-        tc_fence_before();
-        mbar_arrive(&acce_bar[b]);
       }
 
       epi_bar();  // row metadata is reused by the next segment

@@ -87,6 +87,26 @@ size_t moe_prepared_weight_bytes(int E, int rows, int K, int kind);
 int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E, int rows, int K, int kind,
                         void* dst, size_t dst_bytes, moe_stream_t stream);
 
+/* One-time re-layout of bf16 expert weights for moe_forward_bf16 into the tiles its
+ * tensor-core kernels stream, one bulk copy each.  Tile (e, g, m, s) holds rows
+ * [128 m, 128 m + 128) of row group g of expert e (gate rows then up rows for
+ * gate/up, one group for down) and their values [64 s, 64 s + 64): 128 rows of
+ * 128 bytes, the 16-byte chunk c of row r stored at chunk c ^ (r % 8) (the 128-byte
+ * swizzle the MMA reads), rows past the group's end zero.  Tiles are ordered
+ * [E][groups][ceil(rows per group / 128)][K / 64], followed by one zero tile.  The
+ * values are copied unchanged.  The pages' Triton kernels read the weights as
+ * stored; this is a layout of this implementation (weights permuted once at load,
+ * as for MXFP4).
+ *   kind, rows, K: as moe_prepare_weights; rows a multiple of the group count, K a
+ *   multiple of 64.
+ *   w bf16 [E][rows][K]: device, 16-byte aligned, read only.
+ *   dst: device, moe_prepared_weight_bytes_bf16(...) bytes, 256-byte aligned, written.
+ * Returns MOE_OK, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_INVALID_ARG,
+ * MOE_ERR_WORKSPACE_TOO_SMALL or MOE_ERR_CUDA; asynchronous on `stream`.          */
+size_t moe_prepared_weight_bytes_bf16(int E, int rows, int K, int kind);
+int moe_prepare_weights_bf16(const uint16_t* w, int E, int rows, int K, int kind, void* dst, size_t dst_bytes,
+                             moe_stream_t stream);
+
 /* ------------------------------------------------------------------ sizes
  * Token rows per tile chosen for a shape (16, 64 or 128 from the mean tokens per
  * expert T*k/E; fixed per shape, never autotuned) and the bound on tile count.  */
@@ -244,10 +264,9 @@ int moe_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t
  *   - combine: as moe_forward.
  * Arguments:
  *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL;
- *   w_gateup bf16 [E, 2I, H], gate rows [0, I) then up rows [I, 2I);
- *   w_down bf16 [E, H, I].
- *   Both weight tensors are used as stored (no preparation step); all pointers are
- *   16-byte aligned.
+ *   w_gateup: moe_prepare_weights_bf16(MOE_WEIGHTS_GATEUP) of bf16 [E, 2I, H], gate
+ *   rows [0, I) then up rows [I, 2I); w_down: moe_prepare_weights_bf16(MOE_WEIGHTS_DOWN)
+ *   of bf16 [E, H, I].  All pointers are 16-byte aligned.
  *   workspace: moe_workspace_bytes(T, H, I, E, k) bytes, 256-byte aligned.
  *   out bf16 [T, H].
  *   topk_idx_out / topk_w_out: as moe_forward.

@@ -10,8 +10,8 @@ from .build import build, LIB_PATH  # noqa: F401
 
 def __getattr__(name):
     # torch-facing helpers are imported lazily so the C binding works without torch
-    if name in ("MoELayer", "MoELayerBF16", "prepare_weights", "workspace", "route", "build_tile_table", "tile_rows",
-                "max_tiles"):
+    if name in ("MoELayer", "MoELayerBF16", "prepare_weights", "prepare_weights_bf16", "workspace", "route",
+                "build_tile_table", "tile_rows", "max_tiles"):
         from . import api
         return getattr(api, name)
     raise AttributeError(name)

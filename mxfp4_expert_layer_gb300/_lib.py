@@ -35,6 +35,8 @@ SIGNATURES = {
     "moe_error_string": (ctypes.c_char_p, [_I]),
     "moe_prepared_weight_bytes": (_S, [_I, _I, _I, _I]),
     "moe_prepare_weights": (_I, [_P, _P, _I, _I, _I, _I, _P, _S, _P]),
+    "moe_prepared_weight_bytes_bf16": (_S, [_I, _I, _I, _I]),
+    "moe_prepare_weights_bf16": (_I, [_P, _I, _I, _I, _I, _P, _S, _P]),
     "moe_tile_rows": (_I, [_I, _I, _I]),
     "moe_max_tiles": (_I, [_I, _I, _I, _I]),
     "moe_workspace_bytes": (_S, [_I, _I, _I, _I, _I]),
@@ -99,6 +101,8 @@ def _call(name):
 moe_error_string = _call("moe_error_string")
 moe_prepared_weight_bytes = _call("moe_prepared_weight_bytes")
 moe_prepare_weights = _call("moe_prepare_weights")
+moe_prepared_weight_bytes_bf16 = _call("moe_prepared_weight_bytes_bf16")
+moe_prepare_weights_bf16 = _call("moe_prepare_weights_bf16")
 moe_tile_rows = _call("moe_tile_rows")
 moe_max_tiles = _call("moe_max_tiles")
 moe_workspace_bytes = _call("moe_workspace_bytes")

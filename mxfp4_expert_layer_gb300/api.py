@@ -43,6 +43,21 @@ def prepare_weights(codes: torch.Tensor, scales: torch.Tensor, kind: int) -> tor
     return dst
 
 
+def prepare_weights_bf16(w: torch.Tensor, kind: int) -> torch.Tensor:
+    """Raw bf16 expert weights [E, rows, K] (cuda) -> the prepared tile buffer
+    (uint8, cuda) that moe_forward_bf16 streams."""
+    _need_cuda(w)
+    E, rows, K = w.shape
+    nbytes = L.moe_prepared_weight_bytes_bf16(E, rows, K, kind)
+    if nbytes == 0:
+        raise ValueError(f"unsupported weight shape {tuple(w.shape)}")
+    w = w.contiguous()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    L.check("moe_prepare_weights_bf16", L.moe_prepare_weights_bf16(w.data_ptr(), E, rows, K, kind, dst.data_ptr(),
+                                                                    nbytes, _stream()))
+    return dst
+
+
 def workspace(T: int, H: int, I: int, E: int, k: int, device="cuda") -> torch.Tensor:
     n = L.moe_workspace_bytes(T, H, I, E, k)
     if n == 0:
@@ -176,12 +191,16 @@ class MoELayer:
 
 class MoELayerBF16:
     """The same layer with bf16 expert weights (moe_forward_bf16): w_gateup [E, 2I, H]
-    (gate rows, then up rows) and w_down [E, H, I], used as stored."""
+    (gate rows, then up rows) and w_down [E, H, I], prepared once into the tiles the
+    kernels stream (moe_prepare_weights_bf16); the layer keeps only the prepared
+    buffers."""
 
     def __init__(self, w_router: torch.Tensor, w_gateup: torch.Tensor, w_down: torch.Tensor, k: int,
                  router_bias: Optional[torch.Tensor] = None):
         E, two_i, H = w_gateup.shape
-        self.w_router, self.w_gateup, self.w_down = w_router, w_gateup.contiguous(), w_down.contiguous()
+        self.w_router = w_router
+        self.w_gateup = prepare_weights_bf16(w_gateup, L.MOE_WEIGHTS_GATEUP)
+        self.w_down = prepare_weights_bf16(w_down, L.MOE_WEIGHTS_DOWN)
         self.router_bias = router_bias
         self.H, self.I, self.E, self.k = H, two_i // 2, E, k
         self._ws = {}

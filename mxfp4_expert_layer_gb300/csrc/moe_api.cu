@@ -126,18 +126,6 @@ bool weight_map(CUtensorMap* out, const void* prepared, const PreparedLayout& P,
                   kb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-// bf16 weights of one family, row major [E * groups][rows per group][K], as a 3-D byte
-// map {2K bytes, rows per group, E * groups}: one box = 128 rows x 128 bytes (64
-// values, one pipeline stage) with the 128-byte swizzle; parts of a box past the
-// group's rows read as zero.
-bool weight_map16(CUtensorMap* out, const void* w, int E, int groups, int rows_per_group, int K) {
-  const cuuint64_t row_bytes = (cuuint64_t)K * 2;
-  cuuint64_t dims[3] = {row_bytes, (cuuint64_t)rows_per_group, (cuuint64_t)E * groups};
-  cuuint64_t strides[2] = {row_bytes, row_bytes * rows_per_group};
-  cuuint32_t box[3] = {128, (cuuint32_t)kMTile, 1};
-  return make_map(out, w, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
-}
-
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // Records a caller event; while the stream is being captured the record is made an
@@ -380,6 +368,32 @@ int moe_prepare_weights(const uint8_t* codes, const uint8_t* scales, int E, int 
   if (cudaMemcpyAsync(&h, flag, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
   return h ? MOE_ERR_NAN_SCALE : MOE_OK;
+}
+
+size_t moe_prepared_weight_bytes_bf16(int E, int rows, int K, int kind) {
+  if (E < 1 || rows < 1 || K < 64 || K % 64 || (kind != MOE_WEIGHTS_GATEUP && kind != MOE_WEIGHTS_DOWN)) return 0;
+  const int groups = kind == MOE_WEIGHTS_GATEUP ? 2 : 1;
+  if (rows % groups) return 0;
+  const size_t tiles = (size_t)E * groups * ceil_div(rows / groups, kMTile) * (K / 64);
+  return (tiles + 1) * kW16TileBytes;
+}
+
+int moe_prepare_weights_bf16(const uint16_t* w, int E, int rows, int K, int kind, void* dst, size_t dst_bytes,
+                             moe_stream_t stream) {
+  const size_t need = moe_prepared_weight_bytes_bf16(E, rows, K, kind);
+  if (need == 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!w || !dst || !aligned(w, 16) || !aligned(dst, 256)) return MOE_ERR_INVALID_ARG;
+  if (dst_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  PrepareBf16Params pp{};
+  pp.w = w;
+  pp.E = E;
+  pp.groups = kind == MOE_WEIGHTS_GATEUP ? 2 : 1;
+  pp.rows_per_group = rows / pp.groups;
+  pp.K = K;
+  pp.mt = ceil_div(pp.rows_per_group, kMTile);
+  pp.ks = K / 64;
+  pp.dst = static_cast<uint8_t*>(dst);
+  return cuda_status(launch_prepare_bf16(pp, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int moe_tile_rows(int T, int k, int E) {
@@ -635,7 +649,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
 
   // gate/up + SwiGLU (h in bf16, tile order), then down into the slots
   GemmParams g{};
-  if (!weight_map16(&g.tm_w, w_gateup, E, 2, I, H)) return MOE_ERR_CUDA;
+  g.w_tiles = reinterpret_cast<const uint8_t*>(w_gateup);
   g.w16 = 1;
   g.act_q = ws_ptr<uint8_t>(ws, L.x_q);
   g.tiles = tiles;
@@ -657,7 +671,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
   if (st != MOE_OK) return st;
 
   GemmParams d{};
-  if (!weight_map16(&d.tm_w, w_down, E, 1, H, I)) return MOE_ERR_CUDA;
+  d.w_tiles = reinterpret_cast<const uint8_t*>(w_down);
   d.w16 = 1;
   d.act_q = ws_ptr<uint8_t>(ws, L.h_q);
   d.tiles = tiles;

@@ -333,6 +333,42 @@ cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// bf16 weight tiles: one thread per 16-byte chunk of the output.  Chunk position
+// `pos` of row r holds the row's chunk pos ^ (r % 8) (the 128-byte swizzle), so the
+// eight threads of one tile row read the 128 source bytes of that row together.
+__global__ void prepare_bf16_kernel(PrepareBf16Params p) {
+  const long long ntiles = (long long)p.E * p.groups * p.mt * p.ks;
+  const long long total = (ntiles + 1) * 1024;  // 16-byte chunks, the zero tile included
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total;
+       q += (long long)gridDim.x * blockDim.x) {
+    const long long tile = q >> 10;
+    const int r = (int)(q & 1023) >> 3, c = ((int)q & 7) ^ (r & 7);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (tile < ntiles) {
+      long long t = tile;
+      const int s = (int)(t % p.ks);
+      t /= p.ks;
+      const int m = (int)(t % p.mt);
+      t /= p.mt;
+      const int g = (int)(t % p.groups);
+      const int e = (int)(t / p.groups);
+      const int row = m * kMTile + r;
+      if (row < p.rows_per_group)
+        v = __ldg(reinterpret_cast<const uint4*>(p.w + (((size_t)e * p.groups + g) * p.rows_per_group + row) * p.K +
+                                                 (size_t)s * 64) + c);
+    }
+    reinterpret_cast<uint4*>(p.dst)[q] = v;
+  }
+}
+
+cudaError_t launch_prepare_bf16(const PrepareBf16Params& p, cudaStream_t stream) {
+  const long long total = ((long long)p.E * p.groups * p.mt * p.ks + 1) * 1024;
+  const long long want = (total + kAuxThreads - 1) / kAuxThreads;
+  const int blocks = (int)(want < 4096 ? want : 4096);
+  prepare_bf16_kernel<<<blocks, kAuxThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 // out[a][i] = sum_t e2m1(q_t) * 2^(s_t - 127) for every valid tile row.
 __global__ void hidden_dequant_kernel(HiddenDequantParams p) {
   const int num_tiles = __ldcg(p.num_tiles);

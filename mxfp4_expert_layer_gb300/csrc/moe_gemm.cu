@@ -183,8 +183,8 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
     s_flags[0] = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&p.tm_w);
+  if constexpr (!W16) {  // bf16 weights come by bulk copy, with no tensor map
+    if (warp == 0 && lane == 0) tma_prefetch_desc(&p.tm_w);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -270,9 +270,19 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
         // tile past the matrix reads zeros (TMA fill) and scales of the last tile.
         const int mrow = GATEUP ? mt : (MPAIR ? 2 * mt + j : mt);
         const int grp = GATEUP ? j : 0;
+        if constexpr (W16) {
+          // bf16: the prepared 16 KB tile in one bulk copy (the zero tile after the
+          // last one for an M tile past the matrix)
+          static_assert(!W16 || C::kATileBytes == kW16TileBytes, "prepared bf16 tile");
+          const size_t ntiles = (size_t)p.E * p.w_groups * p.w_mt * p.kg;
+          const size_t ti =
+              mrow < p.w_mt ? (((size_t)expert * p.w_groups + grp) * p.w_mt + mrow) * p.kg + kk : ntiles;
+          bulk_load_hint_if(leader, a_tile(s, j), p.w_tiles + ti * kW16TileBytes, (uint32_t)kW16TileBytes,
+                            &full_bar[s], w_policy);
+          continue;
+        }
         tma_load_3d_hint_if(leader, a_tile(s, j), &p.tm_w, &full_bar[s], kk * C::kKBytes, mrow * kMTile,
                             expert * p.w_groups + grp, w_policy);
-        if constexpr (W16) continue;
         const int msf = min(mrow, p.w_mt - 1);
         const uint8_t* wsf =
             p.w_sf + (((size_t)expert * p.w_groups + grp) * p.w_mt + msf) * (size_t)p.kg_sf * kSfAtomBytes;

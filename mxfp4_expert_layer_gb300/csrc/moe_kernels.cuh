@@ -185,6 +185,7 @@ struct GemmParams {
   int grid;                // persistent CTAs (<= kMaxCtas)
   uint32_t* status;
   int w16;                 // bf16 weights and activations (act16_offset layout, no scales)
+  const uint8_t* w_tiles;  // bf16 weights prepared by moe_prepare_weights_bf16 (W16 kernels)
   uint64_t wait_ns;        // limit of each pipeline wait (ns); teardown drains wait up to 1 s
 };
 
@@ -216,6 +217,16 @@ struct PrepareParams {
   uint32_t* flag;          // set to 1 when a scale byte is 255
 };
 cudaError_t launch_prepare(const PrepareParams& p, cudaStream_t stream);
+
+// bf16 weights into swizzled 128-row x 64-value tiles (moe_prepare_weights_bf16).
+constexpr int kW16TileBytes = kMTile * 128;  // one prepared tile: 128 rows x 128 bytes
+struct PrepareBf16Params {
+  const uint16_t* w;       // [E][groups * rows_per_group][K]
+  int E, groups, rows_per_group, K;
+  int mt, ks;              // tiles per group along rows (rounded up) and along K
+  uint8_t* dst;            // [E * groups * mt * ks + 1][16 KB]
+};
+cudaError_t launch_prepare_bf16(const PrepareBf16Params& p, cudaStream_t stream);
 
 struct HiddenDequantParams {
   const int32_t* perm;

@@ -122,6 +122,16 @@ def test_host_argument_checks_return_codes(lib):
         L.MOE_ERR_UNSUPPORTED_SHAPE                            # tile rows must be 16, 64 or 128
     assert L.moe_prepare_weights(fake, fake, E, 2 * I, H, 5, fake, 1 << 40, None) == L.MOE_ERR_UNSUPPORTED_SHAPE
     assert L.moe_prepare_weights(fake, fake, E, 2 * I, H, 0, fake, 16, None) == L.MOE_ERR_WORKSPACE_TOO_SMALL
+    # bf16 weight tiles: (tiles + one zero tile) x 16 KB; K a multiple of 64, rows of whole groups
+    assert L.moe_prepared_weight_bytes_bf16(8, 2 * 14336, 4096, L.MOE_WEIGHTS_GATEUP) == (8 * 2 * 112 * 64 + 1) * 16384
+    assert L.moe_prepared_weight_bytes_bf16(2, 2 * 192, 128, L.MOE_WEIGHTS_GATEUP) == (2 * 2 * 2 * 2 + 1) * 16384
+    assert L.moe_prepared_weight_bytes_bf16(8, 4096, 14336 + 32, L.MOE_WEIGHTS_DOWN) == 0
+    assert L.moe_prepared_weight_bytes_bf16(8, 4097, 4096, L.MOE_WEIGHTS_GATEUP) == 0
+    assert L.moe_prepared_weight_bytes_bf16(8, 4096, 4096, 7) == 0
+    assert L.moe_prepare_weights_bf16(fake, E, H, I, L.MOE_WEIGHTS_DOWN, fake + 16, 1 << 40, None) == \
+        L.MOE_ERR_INVALID_ARG                                  # destination not 256-byte aligned
+    assert L.moe_prepare_weights_bf16(fake, E, H, I, L.MOE_WEIGHTS_DOWN, fake, 16, None) == \
+        L.MOE_ERR_WORKSPACE_TOO_SMALL
     st = ctypes.c_int(0)
     assert L.moe_get_device_status(None, 0, ctypes.byref(st), None) == L.MOE_ERR_INVALID_ARG
 

@@ -71,3 +71,40 @@ def test_dense_layer_is_bit_reproducible():
     _, a, ia, _ = run_dense(inp)
     _, b, ib, _ = run_dense(inp)
     assert np.array_equal(a, b) and np.array_equal(ia, ib)
+
+
+def swizzled_tiles(w: np.ndarray, groups: int) -> np.ndarray:
+    """The prepared bf16 layout restated in numpy (moe_prepare_weights_bf16): tiles of
+    128 rows x 64 values per (expert, row group, 128-row M tile, 64-value K stage),
+    rows past the group zero, 16-byte chunk c of row r stored at c ^ (r % 8), then one
+    zero tile.  Returns the bytes."""
+    E, rows, K = w.shape
+    rpg = rows // groups
+    mt, ks = -(-rpg // 128), K // 64
+    tiles = np.zeros((E, groups, mt, ks, 128, 8, 8), dtype=np.uint16)  # [.., row, chunk, value]
+    for e in range(E):
+        for g in range(groups):
+            for m in range(mt):
+                block = w[e, g * rpg + m * 128: g * rpg + min(rpg, (m + 1) * 128)]
+                for s in range(ks):
+                    vals = block[:, s * 64:(s + 1) * 64].reshape(-1, 8, 8)
+                    for r in range(vals.shape[0]):
+                        tiles[e, g, m, s, r, np.arange(8) ^ (r % 8)] = vals[r]
+    flat = tiles.reshape(-1, 128 * 64)
+    return np.concatenate([flat, np.zeros((1, 128 * 64), np.uint16)]).view(np.uint8).reshape(-1)
+
+
+@pytest.mark.parametrize("E,rows,K,kind", [(2, 2 * 192, 128, 0), (2, 128, 192, 1), (1, 2 * 64, 64, 0)])
+def test_prepare_weights_bf16_byte_exact(E, rows, K, kind):
+    """The prepared bf16 tiles, byte for byte: ragged M tiles (192 and 64 rows per
+    group), several K stages, both families."""
+    import torch
+    import mxfp4_expert_layer_gb300 as pkg
+    pkg.build()
+    rng = np.random.default_rng(E * 1000 + rows + K)
+    w = rng.integers(0, 1 << 16, size=(E, rows, K), dtype=np.uint16)
+    got = pkg.prepare_weights_bf16(to_dev(w), kind)
+    torch.cuda.synchronize()
+    want = swizzled_tiles(w, 2 if kind == 0 else 1)
+    assert got.numel() == want.size
+    assert np.array_equal(got.cpu().numpy(), want)

@@ -10,15 +10,15 @@
 // follows tokens per expert").
 //
 // Design (swap-AB): the MMA's M dimension is 128 weight rows (output features), N
-// covers the tile's token rows, K runs over the contraction in groups of 128 (one
-// pipeline stage).  A = the MXFP4 weights exactly as stored (packed E2M1 codes,
-// TMA-loaded with the 64-byte swizzle); B = the activations, encoded as four
-// packed E2M1 terms with their own E8M0 block scales.  kind::mxf4 consumes both
-// codes and both scale sets natively (K = 64 per instruction, scales copied into
-// tensor memory with tcgen05.cp).  For 16-row decode tiles the four terms are
-// concatenated along N (one N = 64 MMA per K step and weight tile; the epilogue
-// adds the four column groups); larger tiles run one MMA per term into the same
-// accumulator.
+// covers the tile's token rows, K runs over the contraction 256 values (one 128-byte
+// row segment) per pipeline stage.  A = the MXFP4 weights exactly as stored (packed
+// E2M1 codes, TMA boxes with the 128-byte swizzle); B = the activations, encoded as
+// four packed E2M1 terms with their own E8M0 block scales, one pre-swizzled bulk
+// copy per stage.  kind::mxf4 consumes both codes and both scale sets natively
+// (K = 64 per instruction, scales copied into tensor memory with tcgen05.cp).  For
+// 16-row decode tiles the four terms are concatenated along N (one N = 64 MMA per K
+// step and weight tile; the epilogue adds the four column groups); larger tiles run
+// one MMA per term into the same accumulator.
 //
 // Persistent CTAs (one per SM) take whole work units (expert tile x M tile)
 // round-robin.  Warp roles: warp 0 issues TMA loads into a ring of shared-memory
@@ -29,7 +29,8 @@
 // The W16 instances run the same kernel on bf16 weights and activations
 // ("triton-kernels" README, "Fused MoE Dispatch": the Mixtral-style layer):
 // kind::f16 MMAs with K = 16, 64-value stages of the same 128-byte rows, no scales,
-// and bf16 h written by the gate/up epilogue.
+// weights prepared into swizzled 16 KB tiles (one bulk copy each), and bf16 h
+// written by the gate/up epilogue.
 #include <type_traits>
 
 #include "moe_common.cuh"

@@ -260,7 +260,8 @@ int moe_forward_norm(const uint16_t* x, const uint16_t* residual, const uint16_t
  *   - routing: as moe_forward;
  *   - permute: bf16 rows of x into tile order;
  *   - gate/up and down: the grouped tcgen05 GEMMs with kind::f16 (bf16 x bf16,
- *     f32 accumulate); h is rounded to bf16 between them;
+ *     f32 accumulate); h is rounded to bf16 between them.  Tiles are 256 token rows
+ *     once T*k >= 256*E (N = 256 MMAs), else moe_tile_rows(T, k, E);
  *   - combine: as moe_forward.
  * Arguments:
  *   x bf16 [T, H]; w_router bf16 [E, H]; router_bias f32 [E] or NULL;

@@ -408,7 +408,10 @@ int moe_max_tiles(int T, int k, int E, int tile_rows) {
 
 size_t moe_workspace_bytes(int T, int H, int I, int E, int k) {
   if (check_shape(T, H, I, E, k) != MOE_OK) return 0;
-  return make_ws_layout(T, H, I, E, k, tile_rows_policy(T, k, E)).total;
+  // room for both layers' layouts (the bf16 layer may use 256-row tiles)
+  const size_t a = make_ws_layout(T, H, I, E, k, tile_rows_policy(T, k, E)).total;
+  const size_t b = make_ws_layout(T, H, I, E, k, tile_rows_policy_bf16(T, k, E)).total;
+  return a > b ? a : b;
 }
 
 int moe_route(const uint16_t* x, const uint16_t* w_router, const float* router_bias, int T, int H, int E, int k,
@@ -612,7 +615,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
   if (!aligned(x, 16) || !aligned(w_router, 16) || !aligned(out, 16) || !aligned(w_gateup, 16) ||
       !aligned(w_down, 16) || !aligned(workspace, 256))
     return MOE_ERR_INVALID_ARG;
-  const int bm = tile_rows_policy(T, k, E);
+  const int bm = tile_rows_policy_bf16(T, k, E);
   const WsLayout L = make_ws_layout(T, H, I, E, k, bm);
   if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -688,7 +691,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
   d.w_mt = ceil_div(H, kMTile);
   {
     const long long est_tiles = std::max<long long>(std::min(E, T * k), (long long)T * k / bm);
-    d.m_pair = (bm >= 64 && est_tiles * ceil_div(d.w_mt, 2) >= 2LL * persistent_ctas()) ? 1 : 0;
+    d.m_pair = (bm >= 64 && bm <= 128 && est_tiles * ceil_div(d.w_mt, 2) >= 2LL * persistent_ctas()) ? 1 : 0;
   }
   d.mt = d.m_pair ? ceil_div(d.w_mt, 2) : d.w_mt;
   d.rows_out = H;

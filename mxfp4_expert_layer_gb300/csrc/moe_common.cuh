@@ -52,6 +52,13 @@ __host__ __device__ inline int tile_rows_policy(int T, int k, int E) {
   return 128;
 }
 
+// bf16-weight layer: 256-row tiles once the mean tokens per expert fill them (an
+// N = 256 MMA carries twice the work of an N = 128 one for the same issued
+// instruction); below that the policy above.
+__host__ __device__ inline int tile_rows_policy_bf16(int T, int k, int E) {
+  return (long long)T * k >= 256LL * E ? 256 : tile_rows_policy(T, k, E);
+}
+
 __host__ __device__ inline int max_tiles_bound(int T, int k, int E, int bm) {
   long long tk = (long long)T * k;
   long long b = tk / bm + (E < tk ? E : tk);

@@ -84,7 +84,8 @@ struct GemmCfg {
   // accumulator (its long encode of h is latency-bound with one warp per scheduler)
   static constexpr int kEpiGroups = kLoadAll ? 1 : 2;
   static constexpr int kThreads = 224 + 128 * (kEpiGroups - 1);
-  static constexpr int kEpiGroupBytes = 16 * kMTile * 4 + 2 * 128 * 4;  // h transpose chunk + row metadata
+  static constexpr int kMetaRows = BM > 128 ? BM : 128;      // row metadata entries (down epilogue)
+  static constexpr int kEpiGroupBytes = 16 * kMTile * 4 + 2 * kMetaRows * 4;  // h transpose chunk + row metadata
   static constexpr int kEpiBytes = kEpiGroups * kEpiGroupBytes;
   static constexpr int kBarBytes = 2048;
   // two groups: the whole 227 KB a block may have (two stages of the largest tile);
@@ -471,7 +472,7 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
     const int et = threadIdx.x - (eg == 0 ? 64 : 224);  // 0..127 within the group
     float* s_xpose = reinterpret_cast<float*>(epi_smem + eg * C::kEpiGroupBytes);
     int* s_rowa = reinterpret_cast<int*>(s_xpose + 16 * kMTile);
-    float* s_roww = reinterpret_cast<float*>(s_rowa + 128);
+    float* s_roww = reinterpret_cast<float*>(s_rowa + C::kMetaRows);
     auto epi_bar = [eg]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + eg) : "memory"); };
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
     const int i_pad = (p.I + 63) / 64 * 64;  // h features written (zeros past I)
@@ -487,10 +488,10 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
       const int feat = mt * kMTile + m;
       if constexpr (!GATEUP) {
         // row metadata of the tile, staged before the accumulator is ready
-        if (et < nrows) {
-          const int a = __ldcg(p.perm + te.row_begin + et);
-          s_rowa[et] = a;
-          s_roww[et] = __ldcg(p.topk_w + a);
+        for (int r = et; r < nrows; r += 128) {
+          const int a = __ldcg(p.perm + te.row_begin + r);
+          s_rowa[r] = a;
+          s_roww[r] = __ldcg(p.topk_w + a);
         }
       }
       const bool ok = mbar_wait_bounded(&accf_bar[b], (si / C::kNumAcc) & 1, p.wait_ns);
@@ -783,6 +784,9 @@ static cudaError_t launch_gemm(const GemmParams& p, cudaStream_t stream) {
     case 16: return launch_gemm_t<16, GATEUP, MPAIR, W16>(p, stream);
     case 64: return launch_gemm_t<64, GATEUP, MPAIR, W16>(p, stream);
     case 128: return launch_gemm_t<128, GATEUP, MPAIR, W16>(p, stream);
+    case 256:  // bf16 only (no scale columns), unpaired down: the accumulators fit tensor memory
+      if constexpr (W16 && !MPAIR) return launch_gemm_t<256, GATEUP, MPAIR, W16>(p, stream);
+      return cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }

@@ -45,19 +45,23 @@ def check_dense(inp, tokens=None):
     (8, 256, 384, 4, 2, 16),      # dense_tiny shape
     (37, 512, 448, 6, 2, 16),     # ragged tiles, I not a multiple of 128
     (150, 256, 320, 8, 2, 64),
-    (600, 256, 256, 4, 2, 128),   # two epilogue groups
+    (400, 256, 256, 4, 2, 128),   # two epilogue groups
+    (600, 256, 256, 4, 2, 256),   # 256-row tiles (N = 256 MMAs), a 44-row last tile
+    (700, 256, 192, 2, 1, 256),   # 256-row tiles, an M tile of 64 real rows
     (1, 128, 192, 3, 3, 16),      # one token, every expert
 ])
 def test_dense_layer_shapes(T, H, I, E, k, bm):
+    """bm: the tile rows the bf16 layer uses -- the MXFP4 policy's, or 256 once the
+    mean tokens per expert reach 256."""
     from mxfp4_expert_layer_gb300 import _lib as L
     import mxfp4_expert_layer_gb300 as pkg
     pkg.build()
-    assert L.moe_tile_rows(T, k, E) == bm
+    assert (256 if T * k >= 256 * E else L.moe_tile_rows(T, k, E)) == bm
     check_dense(make_dense_layer(T, H, I, E, k, seed=T + H))
 
 
 def test_dense_mixtral_shapes_sampled():
-    # Mixtral-8x7B experts (H 4096, F 14336, 8 experts, top-2) at 2048 tokens (128-row
+    # Mixtral-8x7B experts (H 4096, F 14336, 8 experts, top-2) at 2048 tokens (256-row
     # tiles) and at its first 32 tokens (16-row tiles), sampled tokens against the oracle
     import dataclasses
     big = make_dense_config("mixtral_t2048")

@@ -428,11 +428,11 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
             }
           for (int i = at0 * C::kNbAtoms; i < at1 * C::kNbAtoms; ++i)
             tmem_cp_32x128b_warpx4_if(leader, sfb0 + 4 * i, smem_desc(sfb_addr0 + so + i * kSfAtomBytes, 0, 128, 0));
-          for (int ks = ks0; ks < ks1; ++ks) {  // K = 64 steps: 32 bytes of every operand row
-            if (kk * (C::kKStage / kMxBlock) + 2 * ks >= kblocks) break;  // both MX blocks are padding
-            const int a = ks >> 1;                    // K group (scale atom) of this step
-            const uint32_t idesc = idesc_mxf4(kMTile, C::kN, 2 * (ks & 1), 2 * (ks & 1));
-            if constexpr (C::kConcat) {
+          if constexpr (C::kConcat) {
+            for (int ks = ks0; ks < ks1; ++ks) {  // K = 64 steps: 32 bytes of every operand row
+              if (kk * (C::kKStage / kMxBlock) + 2 * ks >= kblocks) break;  // both MX blocks are padding
+              const int a = ks >> 1;                    // K group (scale atom) of this step
+              const uint32_t idesc = idesc_mxf4(kMTile, C::kN, 2 * (ks & 1), 2 * (ks & 1));
               const uint64_t bdesc = kdesc(b_addr0 + so + 32 * ks);
               const uint32_t acc = seg_first ? 0u : 1u;
               for (int j = j0; j < j1; ++j) {
@@ -440,17 +440,32 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
                 mma_mxf4_if(leader, acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
                             sfb0 + 4 * a * C::kNbAtoms, acc);
               }
-            } else {
-              for (int t = 0; t < kTerms; ++t) {
-                const uint64_t bdesc = kdesc(b_addr0 + so + t * BM * C::kKBytes + 32 * ks);
-                const uint32_t sfb = sfb0 + 4 * a * C::kNbAtoms + (t * BM) / 32;
-                const uint32_t acc = (seg_first && t == 0) ? 0u : 1u;
-                for (int j = j0; j < j1; ++j) {
-                  const uint64_t adesc = kdesc(a_addr0 + so + j * C::kATileBytes + 32 * ks);
-                  mma_mxf4_if(leader, acc_base + j * C::kAccN, adesc, bdesc, idesc, sfc + 4 * (j * C::kAtoms + a),
-                              sfb, acc);
-                }
-              }
+              seg_first = false;
+            }
+          } else {
+            // One weight tile per issuer (j0) and one MMA per term.  At N = BM <= 128 an
+            // MMA holds little tensor work, so the issuing thread's instructions set
+            // the rate: the stage's descriptors are built once and advanced by adds
+            // (the address field counts 16 bytes: 2 per 32-byte K step, BM * kKBytes / 16
+            // per term), and the K steps and terms are unrolled with constant
+            // instruction descriptors.
+            static_assert(C::kA == 1 || C::kIssuers == 2, "one weight tile per issuer");
+            const uint64_t ad0 = kdesc(a_addr0 + so + j0 * C::kATileBytes);
+            const uint64_t bd0 = kdesc(b_addr0 + so);
+            const uint32_t acc_j = acc_base + j0 * C::kAccN;
+            const uint32_t sfa_j = sfc + 4 * (j0 * C::kAtoms);
+            // K steps holding data: both MX blocks of a step past K are padding
+            const int nsteps = min(C::kKSteps, (kblocks - kk * (C::kKStage / kMxBlock) + 1) >> 1);
+#pragma unroll
+            for (int ks = 0; ks < C::kKSteps; ++ks) {
+              if (ks >= nsteps) break;
+              const uint32_t idesc = idesc_mxf4(kMTile, C::kN, 2 * (ks & 1), 2 * (ks & 1));
+#pragma unroll
+              for (int t = 0; t < kTerms; ++t)
+                mma_mxf4_if(leader, acc_j, ad0 + (uint64_t)(2 * ks),
+                            bd0 + (uint64_t)((t * BM * C::kKBytes) / 16 + 2 * ks), idesc,
+                            sfa_j + 4 * (ks >> 1), sfb0 + 4 * (ks >> 1) * C::kNbAtoms + (t * BM) / 32,
+                            (seg_first && ks == 0 && t == 0) ? 0u : 1u);
             }
             seg_first = false;
           }

@@ -403,16 +403,18 @@ __global__ void __launch_bounds__(GemmCfg<BM, GATEUP, MPAIR, W16>::kThreads, 1)
           tc_fence_after();
           const uint32_t so = (uint32_t)s * C::kStageBytes;
           if constexpr (W16) {
-            // bf16 x bf16: four K = 16 steps per 128-byte stage row, no scales
+            // bf16 x bf16: four K = 16 steps per 128-byte stage row, no scales; the
+            // descriptors advance by adds (2 units of 16 bytes per 32-byte step)
             constexpr uint32_t idesc16 = idesc_bf16(kMTile, C::kN);
-            for (int ks = 0; ks < C::kKSteps; ++ks) {
-              const uint64_t bdesc = smem_desc_kmajor_sw128(b_addr0 + so + 32 * ks);
-              const uint32_t acc = seg_first ? 0u : 1u;
-              for (int j = j0; j < j1; ++j)
-                mma_bf16_if(leader, acc_base + j * C::kAccN,
-                            smem_desc_kmajor_sw128(a_addr0 + so + j * C::kATileBytes + 32 * ks), bdesc, idesc16, acc);
-              seg_first = false;
+            const uint64_t bd0 = smem_desc_kmajor_sw128(b_addr0 + so);
+            for (int j = j0; j < j1; ++j) {
+              const uint64_t ad0 = smem_desc_kmajor_sw128(a_addr0 + so + j * C::kATileBytes);
+#pragma unroll
+              for (int ks = 0; ks < C::kKSteps; ++ks)
+                mma_bf16_if(leader, acc_base + j * C::kAccN, ad0 + (uint64_t)(2 * ks), bd0 + (uint64_t)(2 * ks), idesc16,
+                            (seg_first && ks == 0) ? 0u : 1u);
             }
+            seg_first = false;
             mma_commit_if(leader, &empty_bar[s]);
             continue;
           }

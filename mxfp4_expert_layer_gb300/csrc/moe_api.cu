@@ -179,9 +179,7 @@ int run_encode_permute_x(const uint16_t* x, const int32_t* idx, int T, int H, in
   q.wait_at_end = 1;
   q.scatter = 1;
   q.topk_idx = idx;
-  q.inv_perm = ws_ptr<int32_t>(ws, L.inv_perm);
-  q.offsets = ws_ptr<int32_t>(ws, L.offsets);
-  q.tile_first = ws_ptr<int32_t>(ws, L.tile_first);
+  q.pad_row = ws_ptr<int32_t>(ws, L.inv_perm);  // the routing wrote padded rows there
   q.E = E; q.k = k; q.bm = bm; q.max_tiles = L.max_tiles; q.kg_tile = L.kg_h;
   q.q_tile = ws_ptr<uint8_t>(ws, L.x_q);
   q.sf_tile = ws_ptr<uint8_t>(ws, L.x_sf);
@@ -540,7 +538,7 @@ static int forward_impl(const uint16_t* x, const uint16_t* w_router, const float
   r.inv_perm = ws_ptr<int32_t>(ws, L.inv_perm);
   r.tiles = tiles;
   r.num_tiles = num_tiles;
-  r.tile_first = ws_ptr<int32_t>(ws, L.tile_first);
+  r.pad_inv = 1;  // the permute step reads each assignment's padded row
   r.norm = norm;
   bool ev_ok = true;
   auto mark = [&](int i) {
@@ -636,7 +634,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
   r.inv_perm = ws_ptr<int32_t>(ws, L.inv_perm);
   r.tiles = tiles;
   r.num_tiles = num_tiles;
-  r.tile_first = ws_ptr<int32_t>(ws, L.tile_first);
+  r.pad_inv = 1;  // the permute step reads each assignment's padded row
   if (launch_route(r, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // permute: bf16 rows of x into tile order
@@ -644,9 +642,7 @@ int moe_forward_bf16(const uint16_t* x, const uint16_t* w_router, const float* r
   sx.x = x;
   sx.T = T; sx.H = H; sx.E = E; sx.k = k; sx.bm = bm; sx.max_tiles = L.max_tiles;
   sx.topk_idx = idx;
-  sx.inv_perm = r.inv_perm;
-  sx.offsets = r.offsets;
-  sx.tile_first = r.tile_first;
+  sx.pad_row = r.inv_perm;
   sx.q_tile = ws_ptr<uint8_t>(ws, L.x_q);
   if (launch_scatter_x16(sx, s) != cudaSuccess) return MOE_ERR_CUDA;
 

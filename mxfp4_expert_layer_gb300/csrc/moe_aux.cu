@@ -141,17 +141,16 @@ __global__ void __launch_bounds__(kNorm ? kEncodeNormMaxThreads : kAuxThreads) e
   ptx::pdl_launch_dependents();
   if (!p.scatter) return;
   // the permute step: this token's rows go to the tile rows of its k assignments
-  // (expert e, sorted row s: tile tile_first[e] + (s - offsets[e]) / bm)
+  // (padded row v: tile v / bm, row v % bm; an invalid expert has no row)
   for (int j0 = 0; j0 < p.k; j0 += 32) {
     int tile_j = -1, r_j = 0;
     if (j0 + lane < p.k) {
       const int a = t * p.k + j0 + lane;
       const int e = __ldcg(p.topk_idx + a);
-      const int srow = __ldcg(p.inv_perm + a);
-      if (e >= 0 && e < p.E) {
-        const int q = srow - __ldcg(p.offsets + e);
-        tile_j = __ldcg(p.tile_first + e) + q / p.bm;
-        r_j = q % p.bm;
+      const int prow = __ldcg(p.pad_row + a);
+      if (e >= 0 && e < p.E && prow >= 0) {
+        tile_j = prow / p.bm;
+        r_j = prow % p.bm;
       }
     }
     const int nj = min(32, p.k - j0);
@@ -192,11 +191,10 @@ __global__ void __launch_bounds__(kAuxThreads) scatter_x16_kernel(ScatterX16Para
   if (!live) return;
   for (int j = 0; j < p.k; ++j) {
     const int a = t * p.k + j;
-    const int e = __ldcg(p.topk_idx + a);
-    if (e < 0 || e >= p.E) continue;
-    const int q = __ldcg(p.inv_perm + a) - __ldcg(p.offsets + e);
-    const int tile = __ldcg(p.tile_first + e) + q / p.bm, r = q % p.bm;
-    if (tile < 0 || tile >= p.max_tiles) continue;
+    const int e = __ldcg(p.topk_idx + a), prow = __ldcg(p.pad_row + a);
+    if (e < 0 || e >= p.E || prow < 0) continue;
+    const int tile = prow / p.bm, r = prow % p.bm;
+    if (tile >= p.max_tiles) continue;
     *reinterpret_cast<uint4*>(p.q_tile + act16_offset(tile, r, 8 * v, p.max_tiles, p.bm)) = val;
   }
 }

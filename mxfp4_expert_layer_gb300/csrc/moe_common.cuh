@@ -99,10 +99,9 @@ struct WsLayout {
   size_t counts;         // i32 [E]
   size_t offsets;        // i32 [E + 1]
   size_t perm;           // i32 [T*k]
-  size_t inv_perm;       // i32 [T*k]
+  size_t inv_perm;       // i32 [T*k]: each assignment's padded row (tile x bm + row in tile)
   size_t tiles;          // TileEntry [max_tiles]
   size_t num_tiles;      // i32
-  size_t tile_first;     // i32 [E]: each expert's first tile
   size_t xt_q;           // x encoded per token: [kg_h][T][kTerms][64 bytes] packed E2M1
   size_t xt_sf;          // its E8M0 exponents: u32 [kg_h][T][kTerms] (4 MX blocks each)
   size_t x_q;            // x gathered into tile order (act_offset): kg_h * 128 values per row
@@ -142,7 +141,6 @@ inline WsLayout make_ws_layout(int T, int H, int I, int E, int k, int bm) {
   L.inv_perm = take(sizeof(int32_t) * tk);
   L.tiles = take(sizeof(TileEntry) * (size_t)L.max_tiles);
   L.num_tiles = take(sizeof(int32_t));
-  L.tile_first = take(sizeof(int32_t) * (size_t)E);
   L.xt_q = take((size_t)L.kg_h * T * kTerms * 64);
   L.xt_sf = take((size_t)L.kg_h * T * kTerms * sizeof(uint32_t));
   L.x_q = take((size_t)L.kg_h * L.pad_rows * kTerms * 64);

@@ -89,11 +89,14 @@ struct GemmCfg {
   static constexpr int kEpiBytes = kEpiGroups * kEpiGroupBytes;
   static constexpr int kBarBytes = 2048;
   // two groups: the whole 227 KB a block may have (two stages of the largest tile);
-  // one group: the depth measured best for the small tiles (a fifth BM=16 stage was slower)
+  // one group: the depth measured best for the small tiles (a fifth BM=16 stage was
+  // slower).  The split-K decode down GEMM stops at six: it issues its weight stages
+  // while gate/up still streams, and a seventh and eighth measured slower at batch 1.
   static constexpr int kSmemBudget =
       kEpiGroups == 2 ? 232448 - 1024 /*align*/ - kBarBytes - kEpiBytes : 216 * 1024 - kEpiBytes;
   static constexpr int kStagesRaw = kSmemBudget / kStageBytes;
-  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
+  static constexpr int kMaxStages = kSplitK ? 6 : 12;
+  static constexpr int kStages = kStagesRaw > kMaxStages ? kMaxStages : kStagesRaw;
   static constexpr int kSmemBytes = kStages * kStageBytes + 1024 /*align*/ + kBarBytes + kEpiBytes;
   static constexpr uint32_t kTxNoB = kA * kATileBytes + kSfBytes;                // all but the B codes
   // MMA issuers: with two weight tiles per stage each of two threads issues one

@@ -94,7 +94,7 @@ struct RouteParams {
   int build_table;          // also build the tile table (last block)
   int bm;
   int32_t *counts, *offsets, *perm, *inv_perm, *num_tiles;
-  int32_t* tile_first;      // i32 [E]: index of each expert's first tile (or null)
+  int pad_inv;              // inv_perm holds padded rows (tile x bm + row in tile), not sorted rows
   TileEntry* tiles;
   uint32_t* status;
   NormArgs norm;            // the router sees y = RMSNorm(x + residual) (norm.norm_w set)
@@ -117,9 +117,7 @@ struct EncodeXParams {
   // tile rows of the token's k assignments instead of q / sf
   int scatter;
   const int32_t* topk_idx;    // [T, k]
-  const int32_t* inv_perm;    // [T*k]: sorted row of each assignment
-  const int32_t* offsets;     // [E]: first sorted row of each expert
-  const int32_t* tile_first;  // [E]: first tile of each expert
+  const int32_t* pad_row;     // [T*k]: padded row of each assignment (tile x bm + row in tile)
   int E, k, bm, max_tiles, kg_tile;
   uint8_t* q_tile;            // GatherXParams::q layout
   uint8_t* sf_tile;           // GatherXParams::sf layout
@@ -134,9 +132,7 @@ struct ScatterX16Params {
   const uint16_t* x;          // bf16 [T, H]
   int T, H, E, k, bm, max_tiles;
   const int32_t* topk_idx;    // [T, k]
-  const int32_t* inv_perm;    // [T*k]
-  const int32_t* offsets;     // [E]
-  const int32_t* tile_first;  // [E]
+  const int32_t* pad_row;     // [T*k]: padded row of each assignment (tile x bm + row in tile)
   uint8_t* q_tile;            // act16_offset layout
 };
 cudaError_t launch_scatter_x16(const ScatterX16Params& p, cudaStream_t stream);

@@ -60,12 +60,15 @@ __device__ __forceinline__ bool topk_better(float v1, int i1, float v2, int i2) 
 // histograms into counts, row offsets, tile entries and per-warp bases (both
 // scans over experts in one pass), so the whole build takes three block barriers.
 // kSharedIdx: the top-k indices are in this block's shared memory (else global,
-// read through L2).
+// read through L2).  pad_inv: inv_perm receives each assignment's padded row (its
+// tile x bm + its row within the tile) instead of its sorted row, so that the
+// permute step finds the tile row with one load.
 template <bool kSharedIdx = false>
 __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, int E, int bm, int32_t* counts,
                                        int32_t* offsets, int32_t* perm, int32_t* inv_perm, TileEntry* tiles,
-                                       int32_t* num_tiles, uint32_t* status, int32_t* tile_first = nullptr) {
+                                       int32_t* num_tiles, uint32_t* status, bool pad_inv = false) {
   __shared__ int hist[kRouteWarps][kMaxExperts];
+  __shared__ int pad_delta[kMaxExperts];  // padded row minus sorted row, per expert
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid < E) {
 #pragma unroll
@@ -142,7 +145,7 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
       const int c = cnt[i];
       counts[e] = c;
       offsets[e] = off;
-      if (tile_first) tile_first[e] = t0;
+      pad_delta[e] = (t0 << lgbm) - off;
       int run = off;
 #pragma unroll
       for (int w = 0; w < kRouteWarps; ++w) {
@@ -182,7 +185,7 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
     __syncwarp();
     if (e >= 0) {
       perm[pos] = a;
-      inv_perm[a] = pos;
+      inv_perm[a] = pad_inv ? pos + pad_delta[e] : pos;
       if ((grp & lt_mask) == 0) hist[warp][e] += __popc(grp);
     }
     __syncwarp();
@@ -193,12 +196,13 @@ __device__ void build_tile_table_block(const int32_t* __restrict__ idx, int Tk, 
 // barrier (the decode shapes): lane a holds assignment a, lanes with equal experts
 // count themselves into one shared histogram row (__match_any_sync, no atomics), and
 // the scan, offsets, tiles and the stable scatter are those of the block version, so
-// the bits are identical.
+// the bits are identical (pad_inv as there).
 template <bool kSharedIdx = false>
 __device__ void build_tile_table_warp(const int32_t* __restrict__ idx, int Tk, int E, int bm, int32_t* counts,
                                       int32_t* offsets, int32_t* perm, int32_t* inv_perm, TileEntry* tiles,
-                                      int32_t* num_tiles, uint32_t* status, int32_t* tile_first = nullptr) {
+                                      int32_t* num_tiles, uint32_t* status, bool pad_inv = false) {
   __shared__ int whist[kMaxExperts];
+  __shared__ int wpad_delta[kMaxExperts];  // padded row minus sorted row, per expert
   const int lane = threadIdx.x & 31;
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int e = lane; e < E; e += 32) whist[e] = 0;
@@ -244,7 +248,7 @@ __device__ void build_tile_table_warp(const int32_t* __restrict__ idx, int Tk, i
     const int c = cnt[i];
     counts[e] = c;
     offsets[e] = off;
-    if (tile_first) tile_first[e] = t0;
+    wpad_delta[e] = (t0 << lgbm) - off;
     whist[e] = off;
     const int nt = (c + bm - 1) >> lgbm;
     for (int q = 0; q < nt; ++q) {
@@ -268,7 +272,7 @@ __device__ void build_tile_table_warp(const int32_t* __restrict__ idx, int Tk, i
   if (ea >= 0) {
     const int pos = whist[ea] + __popc(grp & lt_mask);
     perm[pos] = lane;
-    inv_perm[lane] = pos;
+    inv_perm[lane] = pad_inv ? pos + wpad_delta[ea] : pos;
   }
 }
 
@@ -504,7 +508,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     __threadfence();
   }
   build_tile_table_block(p.topk_idx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                         p.num_tiles, p.status, p.tile_first);
+                         p.num_tiles, p.status, p.pad_inv != 0);
 }
 
 // ------------------------------------------------------------------ decode routing
@@ -814,12 +818,12 @@ __global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kRouteThr
     if (warp != 0) return;
     if (!mbar_wait_cluster_bounded(bar_idx, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
     build_tile_table_warp<true>(sidx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                                p.num_tiles, p.status, p.tile_first);
+                                p.num_tiles, p.status, p.pad_inv != 0);
     return;
   }
   if (!mbar_wait_cluster_bounded(bar_idx, 0, kRouteWaitLimit)) report_status(p.status, kStatusTimeoutMain);
   build_tile_table_block<true>(sidx, p.T * p.k, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                               p.num_tiles, p.status, p.tile_first);
+                               p.num_tiles, p.status, p.pad_inv != 0);
 }
 
 // ------------------------------------------------------------------ many tokens
@@ -1035,10 +1039,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_mma_kernel(RouteParams p)
     for (int i = n4 * 4 + tid; i < Tk; i += kRouteThreads) sidx[i] = __ldcg(p.topk_idx + i);
     __syncthreads();
     build_tile_table_block<true>(sidx, Tk, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                                 p.num_tiles, p.status, p.tile_first);
+                                 p.num_tiles, p.status, p.pad_inv != 0);
   } else {
     build_tile_table_block(p.topk_idx, Tk, p.E, p.bm, p.counts, p.offsets, p.perm, p.inv_perm, p.tiles,
-                           p.num_tiles, p.status, p.tile_first);
+                           p.num_tiles, p.status, p.pad_inv != 0);
   }
 }
 
